@@ -1,0 +1,380 @@
+"""Benchmark of the fused row softmax on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all] [--impl ours|reference]
+
+One step is one rowsoftmax_fwd call (the whole hot path: load, max, exp,
+sum, normalise, store) over one batch of the workload.  The default workload
+is fp32 8192 x 5000 with row stride 5120.  Rank 0 prints one JSON line per
+workload with achieved HBM GB/s (bytes = M * N * (in + out element size)),
+rows/s, the roofline fraction of the kernel against the measured HBM copy
+bandwidth, the end-to-end figure through the C ABI with host buffers, the
+SM clocks sampled during the timed region, and the CPU oracle timed on a
+bounded sample of the same workload on the host cores.
+
+Under torchrun every rank runs the same workload on its own GPU (replicas,
+weak scaling, no collective on the data path); the timed region is bracketed
+by barriers and the max over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import ctypes
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "fp32_8192x5000_ld5120"
+L2_BYTES = 129 * 1024 * 1024
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+KERNEL_SOURCES = ["rs_common.cuh", "rs_rows.cuh", "rs_wide.cu", "rs_internal.h", "rowsoftmax_api.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "memory_bound_row_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when
+    there is none or the kernel sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = data.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def finish(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for rec in csv.reader(io.StringIO(out)):
+            if len(rec) < 10:
+                continue
+            rec = [r.strip() for r in rec]
+            try:
+                ts = time.mktime(time.strptime(rec[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + rec[0].split(".")[1]) if "." in rec[0] else 0.0
+                rows.append((ts, float(rec[2]), float(rec[3]), rec[5:]))
+            except (ValueError, IndexError):
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        use = inside or rows
+        if not use:
+            return None
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, val in zip(names, r[3][1:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, workloads):
+    """The CPU oracle timed on the host cores: each step is the oracle over a
+    bounded sample of rows of the workload (rank 0 only)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from memory_bound_row_gb300 import workloads as W
+
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    cores = os.cpu_count() or 1
+    for name in workloads:
+        w = W.WORKLOADS[name]
+        fmt = w.dtype
+        probe_rows = min(w.M, max(cores, 8))
+        xs = W.generate(w, "cpu", 0, probe_rows)
+        store = lambda t: t.view(torch.int16).numpy().view(np.uint16) if fmt == "bf16" else t.numpy()
+        x_np = store(xs[:, : w.N].contiguous())
+        t = time.perf_counter()
+        oracle.softmax_store(x_np, fmt, w.N, nthreads=cores)
+        per_row = (time.perf_counter() - t) / probe_rows
+        budget = 60.0  # seconds for the whole run
+        rows_per_step = max(1, min(probe_rows, int(budget / max(1, args.steps + args.warmup) / per_row)))
+        sample = x_np[:rows_per_step]
+        for _ in range(args.warmup):
+            oracle.softmax_store(sample, fmt, w.N, nthreads=cores)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.softmax_store(sample, fmt, w.N, nthreads=cores)
+        dt = (time.perf_counter() - t) / args.steps
+        nbytes = rows_per_step * w.N * 2 * w.elem_size
+        gbs = nbytes / dt / 1e9
+        sample_desc = f"{rows_per_step} of {w.M} rows per step ({w.description}), host oracle, fp64"
+        line = {
+            "impl": "reference", "metric": "achieved HBM GB/s (row softmax)", "value": round(gbs, 4),
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "rows_per_s": round(rows_per_step / dt, 2),
+            "config": {"workload": name, "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample_desc},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, x_dev, seconds: float = 8.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of rows on all host cores."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    cores = os.cpu_count() or 1
+    fmt = w.dtype
+
+    def host(rows):
+        t = x_dev[:rows, : w.N].cpu().contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if fmt == "bf16" else t.numpy()
+
+    probe = min(w.M, max(cores, 16))
+    xs = host(probe)
+    t = time.perf_counter()
+    oracle.softmax_store(xs, fmt, w.N, nthreads=cores)
+    per_row = (time.perf_counter() - t) / probe
+    rows = int(min(w.M, max(probe, seconds / max(per_row, 1e-9))))
+    xs = host(rows)
+    t = time.perf_counter()
+    oracle.softmax_store(xs, fmt, w.N, nthreads=cores)
+    dt = time.perf_counter() - t
+    nbytes = rows * w.N * 2 * w.elem_size
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of {w.M} rows, fp64 oracle writing {w.dtype}, {dt:.1f} s wall",
+            "rows_per_s": round(rows / dt, 2)}
+
+
+def run_ours(args, workloads):
+    import torch
+    import torch.distributed as dist
+
+    import memory_bound_row_gb300 as rs
+    from memory_bound_row_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    lib = rs._abi.load()
+    fwd = lib.rowsoftmax_fwd
+    peak, peak_src = measured_peaks()
+
+    for name in workloads:
+        w = W.WORKLOADS[name]
+        code = {"f32": rs.RS_F32, "f16": rs.RS_F16, "bf16": rs.RS_BF16}[w.dtype]
+        set_bytes = 2 * w.M * w.ld * w.elem_size
+        nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
+        xs = [W.generate(w, dev) for _ in range(1)]
+        xs += [xs[0].clone() for _ in range(nsets - 1)]
+        ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+        stream = torch.cuda.current_stream(dev)
+        s_handle = ctypes.c_void_p(stream.cuda_stream)
+        args_list = [(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr())) for x, y in zip(xs, ys)]
+
+        def step(i):
+            a, b = args_list[i % nsets]
+            rc = fwd(a, b, w.M, w.N, w.ld, w.ld, code, s_handle)
+            if rc != rs.RS_OK:
+                raise rs.RowSoftmaxError(rc, rs.rowsoftmax_last_cuda_error())
+
+        for i in range(max(3, args.warmup)):
+            step(i)
+        torch.cuda.synchronize()
+
+        # Device-timed region: K launches, an event pair around each.
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        sampler = ClockSampler(local) if rank == 0 else None
+        time.sleep(0.3 if sampler else 0)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_start()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(i)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_end()
+        if world > 1:
+            dist.barrier()
+        total_ms = starts[0].elapsed_time(ends[-1])
+        kern_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+        t = torch.tensor([total_ms], device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        clocks = sampler.finish() if sampler else None
+
+        ms_per_step = total_ms / args.steps
+        nbytes = w.algorithmic_bytes
+        value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+        achieved = nbytes / (kern_ms * 1e-3) / 1e9
+
+        # End to end through the C ABI with host buffers: pinned input copied
+        # in, the call, the output copied back, every step.
+        h_in = xs[0].cpu().pin_memory()
+        h_out = torch.empty_like(h_in).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
+        for i in range(2):
+            xs[0].copy_(h_in, non_blocking=True)
+            step(0)
+            h_out.copy_(ys[0], non_blocking=True)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for i in range(e2e_steps):
+            xs[0].copy_(h_in, non_blocking=True)
+            step(0)
+            h_out.copy_(ys[0], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        t = torch.tensor([e2e_ms], device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+        rc, flags = rs.rowsoftmax_device_status()
+        if rc != rs.RS_OK or flags:
+            raise RuntimeError(f"device status word {flags:#x} after the run")
+
+        if rank == 0:
+            rc, info = rs.rowsoftmax_device_info()
+            rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code, None, info)
+            line = {
+                "metric": "achieved HBM GB/s (row softmax)", "value": round(value, 2), "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+                "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "rows_per_s": round(world * w.M / (ms_per_step * 1e-3), 1),
+                "hbm_roofline_frac": round(value / world / peak, 4),
+                "config": {"workload": name, "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
+                           "bytes_per_step": nbytes, "parallelism": "replicas",
+                           "l2": f"{nsets} rotating input/output sets, {nsets * set_bytes / 1e6:.0f} MB "
+                                 f"(> 4x the 129 MB L2)",
+                           "kernel": rs.PATH_NAMES[plan["path"]], "plan": plan},
+                "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                             "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name),
+                             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
+                             if peak_src == "measured" else "fallback 6.8 TB/s",
+                             "kernel_ms": round(kern_ms, 5)},
+                "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                        "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
+                        "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
+                        "ms_per_step": round(e2e_ms, 4)},
+                "gpu_launches": args.steps,
+                "clocks": clocks,
+            }
+            if not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(w, xs[0])
+            print(json.dumps(line), flush=True)
+        del xs, ys, h_in, h_out
+        torch.cuda.empty_cache()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, help="a workload name, or 'all'")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from memory_bound_row_gb300 import workloads as W
+
+    names = W.ORDER if args.workload == "all" else [args.workload]
+    for n in names:
+        if n not in W.WORKLOADS:
+            raise SystemExit(f"unknown workload {n}; choose from {', '.join(W.ORDER)} or 'all'")
+    if args.impl == "reference":
+        run_reference(args, names)
+    else:
+        run_ours(args, names)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * rowsoftmax -- fused row-wise softmax for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * The operation is the fused row softmax of "stanleyjacob.dev: Triton",
+ * Part II, "Worked example: fused softmax": for every row r of a row-major
+ * 2-D tensor, load the row once, find its max m_r, and write
+ *
+ *     y[r][j] = exp(x[r][j] - m_r) / sum_k exp(x[r][k] - m_r),   0 <= j < N,
+ *
+ * once.  Arithmetic is fp32 whatever the storage type (the "fp32
+ * Accumulation" rule of the Hugging Face "triton-kernels" skill page,
+ * "Numerics"); the output is rounded to the storage type with
+ * round-to-nearest-even.  Rows longer than one thread block can hold are
+ * split over a thread-block cluster and combined with the online
+ * normaliser of Milakov and Gimelshein (mohakchugh.is-a.dev "Triton: Block-
+ * Level GPU Programming Without CUDA", "How Flash Attention Uses Triton"):
+ * partial pairs (m, l) merge as m = max(m1, m2),
+ * l = l1 * exp(m1 - m) + l2 * exp(m2 - m).
+ *
+ * Data model (the Triton tutorial's kernel arguments in_row_stride,
+ * out_row_stride and n_cols, taken from x.stride(0)):
+ *  - `in` and `out` are DEVICE pointers (memory the current CUDA device can
+ *    address: cudaMalloc, managed, or mapped pinned host memory), owned by the
+ *    caller, who keeps them alive until the work on `stream` is done;
+ *  - element (r, j) is at base + r * row_stride + j, in elements; the column
+ *    stride is 1; row strides are >= N; padding columns are never read or
+ *    written;
+ *  - `in` and `out` have the same storage type `dtype` (rs_dtype);
+ *  - in == out with equal strides (exact in-place) is allowed; any other
+ *    overlap of the two address ranges is rejected with RS_ERR_OVERLAP;
+ *  - pointers only need the alignment of one element; 16-byte aligned
+ *    pointers and strides unlock 16-byte vector accesses, anything else is
+ *    served by an element-wise kernel (no error).
+ *
+ * Special values follow the formula under IEEE rules: -inf entries give 0,
+ * a row that is all -inf gives NaN, a NaN or +inf anywhere in a row gives a
+ * NaN row.
+ *
+ * Execution: every call is asynchronous on `stream` (0 = legacy default
+ * stream), allocates no device memory, and never synchronises.  Errors in
+ * the arguments are reported before anything is launched.  Calls are safe
+ * from several host threads.
+ */
+#ifndef ROWSOFTMAX_H
+#define ROWSOFTMAX_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define RS_API __attribute__((visibility("default")))
+#else
+#define RS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage types.  Input and output share one. */
+typedef enum { RS_F32 = 0, RS_F16 = 1, RS_BF16 = 2 } rs_dtype;
+
+/* Return codes of every entry point. */
+typedef enum {
+    RS_OK = 0,
+    RS_ERR_INVALID_ARG = 1,        /* negative size, stride < N, null or mis-typed pointer, size overflow */
+    RS_ERR_UNSUPPORTED_DTYPE = 2,  /* dtype is not an rs_dtype */
+    RS_ERR_OVERLAP = 3,            /* in/out ranges overlap and the call is not exact in-place */
+    RS_ERR_CUDA = 4,               /* a CUDA runtime call or the launch failed */
+    RS_ERR_NOT_DEVICE_MEMORY = 5,  /* a pointer is not addressable by the current device */
+    RS_ERR_NO_PATH = 6             /* the forced options cannot serve this shape */
+} rs_status;
+
+/* Kernel families (see rs_plan). */
+typedef enum {
+    RS_PATH_AUTO = 0,     /* let the library choose (the default) */
+    RS_PATH_ROWS = 1,     /* single pass, the row held in registers; 1..1024 threads per row */
+    RS_PATH_CLUSTER = 2,  /* wide rows: a cluster of CTAs per row, each CTA stages its slice in
+                             shared memory with bulk asynchronous copies (TMA engine), online (m, l),
+                             partial pairs merged over distributed shared memory; reads HBM once */
+    RS_PATH_STREAM = 3    /* any row: a cluster per row streams its slice twice from global memory
+                             (online (m, l) on the first read, normalise on the second); reads 2x */
+} rs_path;
+
+/*
+ * Forcing options for tests and tuning.  Zero fields mean "choose".  A NULL
+ * rs_options pointer is the same as all zeros, i.e. rowsoftmax_fwd.
+ */
+typedef struct {
+    int path;             /* rs_path */
+    int threads_per_row;  /* RS_PATH_ROWS: 1,2,4,8,16,32 or a multiple of 32 up to 1024 */
+    int vec_per_thread;   /* RS_PATH_ROWS: 16-byte vectors (or elements, when scalar) per thread */
+    int block_threads;    /* threads per CTA (RS_PATH_ROWS: multiple of threads_per_row) */
+    int cluster_size;     /* RS_PATH_CLUSTER / RS_PATH_STREAM: CTAs per row, 1..16 */
+    int force_scalar;     /* 1: element-wise accesses even when 16-byte vectors would be legal */
+    int64_t grid_limit;   /* >0: cap on CTAs (rows loop inside the kernel); 0: one launch slot per row group */
+} rs_options;
+
+/* What a call would launch (filled by rowsoftmax_plan). */
+typedef struct {
+    int path;             /* rs_path actually chosen */
+    int dtype;
+    int vec_elems;        /* elements per access: 16/elem_size, or 1 for the element-wise kernels */
+    int threads_per_row;  /* RS_PATH_ROWS */
+    int vec_per_thread;   /* RS_PATH_ROWS */
+    int rows_per_cta;     /* RS_PATH_ROWS */
+    int block_threads;
+    int cluster_size;     /* CTAs per row (1 for RS_PATH_ROWS) */
+    int stages;           /* RS_PATH_CLUSTER: bulk-copy stages per CTA */
+    int64_t chunk_elems;  /* RS_PATH_CLUSTER / RS_PATH_STREAM: row slice per CTA */
+    int64_t grid;         /* CTAs launched */
+    size_t smem_bytes;    /* dynamic shared memory per CTA */
+} rs_plan;
+
+/* Device facts the planner needs; rowsoftmax_plan takes them explicitly so
+ * the heuristics can be inspected without a GPU. */
+typedef struct {
+    int sm_count;                  /* multiprocessors */
+    int max_smem_per_block_optin;  /* bytes, cudaDevAttrMaxSharedMemoryPerBlockOptin */
+    int max_smem_per_sm;           /* bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor */
+    int max_threads_per_sm;
+    int cc_major, cc_minor;
+} rs_device_info;
+
+/*
+ * y = softmax over each of the M rows of x (N columns).
+ *   in, out          device pointers to x and y (see the data model above)
+ *   M, N             rows and columns, >= 0; M == 0 or N == 0 is a no-op
+ *                    returning RS_OK; N < 2^31
+ *   in_row_stride    elements between the starts of consecutive rows of x, >= N
+ *   out_row_stride   the same for y, >= N
+ *   dtype            rs_dtype of both tensors
+ *   stream           CUDA stream the kernel is enqueued on
+ * Returns an rs_status.  RS_ERR_CUDA carries the CUDA error of the failing
+ * call, readable (and cleared) with rowsoftmax_last_cuda_error.
+ */
+RS_API int rowsoftmax_fwd(const void* in, void* out, int64_t M, int64_t N,
+                   int64_t in_row_stride, int64_t out_row_stride,
+                   int dtype, cudaStream_t stream);
+
+/* rowsoftmax_fwd with forcing options (tests, tuning sweeps).  The
+ * semantics and error behaviour are those of rowsoftmax_fwd; a forced
+ * configuration that cannot serve the shape returns RS_ERR_NO_PATH. */
+RS_API int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N,
+                      int64_t in_row_stride, int64_t out_row_stride,
+                      int dtype, cudaStream_t stream, const rs_options* opts);
+
+/* Host-only: validate the arguments exactly as rowsoftmax_fwd_ex does and
+ * describe the launch it would make on a device described by `dev` (no CUDA
+ * call is made; pointers are only inspected for alignment and overlap).
+ * Returns an rs_status; `plan` is filled on RS_OK (path 0 and grid 0 for an
+ * empty problem). */
+RS_API int rowsoftmax_plan(const void* in, const void* out, int64_t M, int64_t N,
+                    int64_t in_row_stride, int64_t out_row_stride, int dtype,
+                    const rs_options* opts, const rs_device_info* dev, rs_plan* plan);
+
+/* Host-only: fill `dev` for the current CUDA device.  Returns RS_OK or
+ * RS_ERR_CUDA. */
+RS_API int rowsoftmax_device_info(rs_device_info* dev);
+
+/* Static text for an rs_status value ("unknown status" otherwise). */
+RS_API const char* rowsoftmax_status_string(int status);
+
+/* The cudaError_t of the last RS_ERR_CUDA returned on this host thread (0 if
+ * none); reading it clears it. */
+RS_API int rowsoftmax_last_cuda_error(void);
+
+/*
+ * Device-side status word of the current device.  The cluster kernels bound
+ * every wait on an mbarrier; a wait that runs out sets bit 0 and the CTA
+ * abandons its row (the output row is then incomplete).  Reads the word
+ * (synchronously, with cudaMemcpyFromSymbol) into *flags and clears it when
+ * `clear` is nonzero.  Returns RS_OK or RS_ERR_CUDA.
+ */
+RS_API int rowsoftmax_device_status(unsigned int* flags, int clear);
+
+/*
+ * Host-only description of the register layout of RS_PATH_ROWS: element j of
+ * a row lives in thread (j / vec) mod threads, slot
+ * (j / (threads * vec)) * vec + j mod vec of that thread -- the group-cyclic
+ * layout of the nano-triton post ("The register layout"): consecutive 16-byte
+ * groups are dealt to the threads round robin, so a warp's accesses are
+ * adjacent and each thread's group is one 16-byte access.  Returns RS_OK, or
+ * RS_ERR_INVALID_ARG for j < 0, threads < 1 or vec < 1.
+ */
+RS_API int rowsoftmax_layout_owner(int64_t j, int threads, int vec, int* thread, int64_t* slot);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROWSOFTMAX_H */

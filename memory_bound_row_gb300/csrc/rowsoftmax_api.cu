@@ -1,0 +1,408 @@
+// The C ABI of include/rowsoftmax.h: argument validation, the planner that
+// picks a kernel family and launch shape, and the dispatch onto the
+// caller's stream.  Host code only; the kernels live in rs_rows_*.cu and
+// rs_wide.cu.
+#include <cuda_runtime.h>
+
+#include <limits.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "rowsoftmax.h"
+#include "rs_internal.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return RS_ERR_CUDA;
+}
+
+int elem_size(int dtype) { return dtype == RS_F32 ? 4 : 2; }
+
+// Largest accepted N: keeps every in-kernel element index (which may run a
+// 16-byte unit past N) inside int.
+constexpr int64_t kMaxN = (int64_t)INT_MAX - 64;
+constexpr int64_t kMaxGrid = (int64_t)INT_MAX;
+
+// Auto-planner knobs.
+constexpr int kRowsTargetValues = 32;             // fp32 values a thread holds (auto)
+constexpr int64_t kRowsMaxRowBytes = 32 * 1024;   // auto: rows up to this go to RS_PATH_ROWS
+constexpr int64_t kClusterTargetSlice = 64 * 1024;  // auto: bytes of row slice per CTA
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+bool valid_tpr(int tpr) {
+    if (tpr >= 1 && tpr <= 32) return (tpr & (tpr - 1)) == 0;
+    return tpr > 32 && tpr <= rs::kRowsMaxThreads && tpr % 32 == 0;
+}
+
+// The per-thread unit counts instantiated for (dtype, vec) and their number.
+const int* vpt_table(int dtype, int vec, int* n) {
+    if (vec == 1) {
+        *n = (int)(sizeof(rs::kVptScalar) / sizeof(int));
+        return rs::kVptScalar;
+    }
+    if (dtype == RS_F32) {
+        *n = (int)(sizeof(rs::kVptVecF32) / sizeof(int));
+        return rs::kVptVecF32;
+    }
+    *n = (int)(sizeof(rs::kVptVec16) / sizeof(int));
+    return rs::kVptVec16;
+}
+
+bool vpt_instantiated(int dtype, int vec, int vpt) {
+    int n = 0;
+    const int* t = vpt_table(dtype, vec, &n);
+    for (int i = 0; i < n; ++i)
+        if (t[i] == vpt) return true;
+    return false;
+}
+
+// Smallest instantiated count >= want, or 0.
+int vpt_at_least(int dtype, int vec, int64_t want) {
+    int n = 0;
+    const int* t = vpt_table(dtype, vec, &n);
+    for (int i = 0; i < n; ++i)
+        if (t[i] >= want) return t[i];
+    return 0;
+}
+
+int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o, rs_plan* p) {
+    int tpr = o.threads_per_row;
+    int vpt = o.vec_per_thread;
+    if (tpr && !valid_tpr(tpr)) return RS_ERR_INVALID_ARG;
+    if (vpt && !vpt_instantiated(dtype, vec, vpt)) return RS_ERR_NO_PATH;
+    if (!tpr) {
+        if (vpt) {
+            const int64_t need = ceil_div(units, vpt);
+            if (need <= 32) {
+                tpr = 1;
+                while (tpr < need) tpr <<= 1;
+            } else {
+                tpr = (int)round_up(need, 32);
+            }
+        } else {
+            const int vt = kRowsTargetValues / vec > 0 ? kRowsTargetValues / vec : 1;
+            const int64_t need = ceil_div(units, vt);
+            if (need <= 32) {
+                tpr = 1;
+                while (tpr < need) tpr <<= 1;
+            } else {
+                tpr = (int)round_up(need, 32);
+            }
+        }
+        if (tpr > rs::kRowsMaxThreads) return RS_ERR_NO_PATH;
+    }
+    if (!vpt) {
+        vpt = vpt_at_least(dtype, vec, ceil_div(units, tpr));
+        if (!vpt) return RS_ERR_NO_PATH;
+    }
+    if ((int64_t)tpr * vpt < units) return RS_ERR_NO_PATH;
+    if (vpt * vec > rs::kRowsMaxValuesPerThread) return RS_ERR_NO_PATH;
+    const int block_limit = rs::rows_block_limit(vpt, vec);
+    if (tpr > block_limit) return RS_ERR_NO_PATH;
+
+    int block = o.block_threads;
+    if (block) {
+        if (block % tpr != 0 || block % 32 != 0) return RS_ERR_INVALID_ARG;
+        if (block > block_limit) return RS_ERR_NO_PATH;
+    } else {
+        block = tpr >= 256 ? tpr : tpr * (256 / tpr);
+    }
+    const int rows_per_cta = block / tpr;
+    int64_t grid = ceil_div(M, rows_per_cta);
+    if (o.grid_limit > 0 && grid > o.grid_limit) grid = o.grid_limit;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+
+    p->path = RS_PATH_ROWS;
+    p->vec_elems = vec;
+    p->threads_per_row = tpr;
+    p->vec_per_thread = vpt;
+    p->rows_per_cta = rows_per_cta;
+    p->block_threads = block;
+    p->cluster_size = 1;
+    p->stages = 0;
+    p->chunk_elems = 0;
+    p->grid = grid;
+    p->smem_bytes = 0;
+    return RS_OK;
+}
+
+int plan_wide(int dtype, int path, int vec, int64_t M, int64_t N, const rs_options& o,
+              const rs_device_info& dev, rs_plan* p) {
+    const int es = elem_size(dtype);
+    const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kWideStaticSmem;
+    int cs = o.cluster_size;
+    if (cs && (cs < 1 || cs > rs::kMaxCluster)) return RS_ERR_INVALID_ARG;
+    if (path == RS_PATH_CLUSTER) {
+        if (vec == 1) return RS_ERR_NO_PATH;  // bulk copies need 16-byte units
+        if (!cs) {
+            for (int c = 1; c <= rs::kMaxCluster; c <<= 1) {
+                const int64_t slice = round_up(ceil_div(N, c), vec) * es;
+                if (slice <= kClusterTargetSlice || (c == rs::kMaxCluster && slice <= max_dyn)) {
+                    cs = c;
+                    break;
+                }
+                if (c == rs::kMaxCluster) break;
+            }
+            if (!cs) return RS_ERR_NO_PATH;
+        }
+    } else if (!cs) {
+        // Streaming: enough CTAs to cover the machine, at most kMaxClusterPortable per row.
+        cs = 1;
+        while (cs < rs::kMaxClusterPortable && M * cs < 2 * (int64_t)dev.sm_count) cs <<= 1;
+    }
+    const int64_t chunk = round_up(ceil_div(N, cs), vec);
+    if (chunk > kMaxN) return RS_ERR_NO_PATH;
+    int stages = 0;
+    size_t smem = 0;
+    if (path == RS_PATH_CLUSTER) {
+        smem = (size_t)round_up(chunk * es, 16);
+        if ((int64_t)smem > max_dyn) return RS_ERR_NO_PATH;
+        stages = (int)ceil_div(ceil_div(chunk, vec), rs::kWideUnitsPerStage);
+        if (stages > rs::kWideMaxStages) return RS_ERR_NO_PATH;
+    }
+    int64_t clusters = M;
+    if (o.grid_limit > 0 && clusters * cs > o.grid_limit) clusters = o.grid_limit / cs > 0 ? o.grid_limit / cs : 1;
+    if (clusters * cs > kMaxGrid) clusters = kMaxGrid / cs;
+
+    p->path = path;
+    p->vec_elems = vec;
+    p->threads_per_row = 0;
+    p->vec_per_thread = 0;
+    p->rows_per_cta = 1;
+    p->block_threads = rs::kWideThreads;
+    p->cluster_size = cs;
+    p->stages = stages;
+    p->chunk_elems = chunk;
+    p->grid = clusters * cs;
+    p->smem_bytes = smem;
+    return RS_OK;
+}
+
+int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t ldi,
+                      int64_t ldo, int dtype, const rs_options* opts, const rs_device_info* dev,
+                      rs_plan* p) {
+    memset(p, 0, sizeof(*p));
+    p->dtype = dtype;
+    if (dtype != RS_F32 && dtype != RS_F16 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED_DTYPE;
+    if (M < 0 || N < 0) return RS_ERR_INVALID_ARG;
+    rs_options o;
+    memset(&o, 0, sizeof(o));
+    if (opts) o = *opts;
+    if (o.path < RS_PATH_AUTO || o.path > RS_PATH_STREAM || o.grid_limit < 0 || o.vec_per_thread < 0 ||
+        o.threads_per_row < 0 || o.block_threads < 0 || o.cluster_size < 0)
+        return RS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return RS_OK;  // nothing to do, nothing launched
+    if (N > kMaxN) return RS_ERR_INVALID_ARG;
+    if (!in || !out) return RS_ERR_INVALID_ARG;
+    if (ldi < N || ldo < N) return RS_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    const uintptr_t ai = (uintptr_t)in, ao = (uintptr_t)out;
+    if (ai % es || ao % es) return RS_ERR_INVALID_ARG;
+    // Byte extent of each tensor: ((M-1)*ld + N) * es, checked for overflow.
+    if ((M - 1) > (INT64_MAX / es - N) / ldi || (M - 1) > (INT64_MAX / es - N) / ldo)
+        return RS_ERR_INVALID_ARG;
+    const uint64_t ext_i = (uint64_t)(((M - 1) * ldi + N) * es);
+    const uint64_t ext_o = (uint64_t)(((M - 1) * ldo + N) * es);
+    if (ai > UINTPTR_MAX - ext_i || ao > UINTPTR_MAX - ext_o) return RS_ERR_INVALID_ARG;
+    const bool overlap = ai < ao + ext_o && ao < ai + ext_i;
+    if (overlap && !(ai == ao && ldi == ldo)) return RS_ERR_OVERLAP;
+    if (!dev || dev->sm_count <= 0 || dev->max_smem_per_block_optin <= 0) return RS_ERR_INVALID_ARG;
+
+    const int kvec = 16 / es;
+    const bool strides_ok = M == 1 || (((ldi * es) % 16) == 0 && ((ldo * es) % 16) == 0);
+    const bool vec_ok = !o.force_scalar && ai % 16 == 0 && ao % 16 == 0 && strides_ok;
+    const int vec = vec_ok ? kvec : 1;
+    const int64_t units = ceil_div(N, vec);
+
+    int path = o.path;
+    if (path == RS_PATH_AUTO) {
+        int rc = RS_ERR_NO_PATH;
+        if (N * es <= kRowsMaxRowBytes) rc = plan_rows(dtype, vec, M, units, o, p);
+        if (rc == RS_OK) return RS_OK;
+        if (rc != RS_ERR_NO_PATH) return rc;
+        if (vec_ok) {
+            rc = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, p);
+            if (rc == RS_OK) return RS_OK;
+            if (rc != RS_ERR_NO_PATH) return rc;
+        }
+        return plan_wide(dtype, RS_PATH_STREAM, vec, M, N, o, *dev, p);
+    }
+    if (path == RS_PATH_ROWS) return plan_rows(dtype, vec, M, units, o, p);
+    return plan_wide(dtype, path, vec, M, N, o, *dev, p);
+}
+
+std::mutex g_dev_mu;
+bool g_dev_known[64];
+rs_device_info g_dev[64];
+
+int query_device(int dev, rs_device_info* info) {
+    memset(info, 0, sizeof(*info));
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&info->sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&info->max_smem_per_block_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                    dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&info->max_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&info->max_threads_per_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&info->cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&info->cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail_cuda(e);
+    }
+    return RS_OK;
+}
+
+int current_device(int* dev, rs_device_info* info) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail_cuda(e);
+    }
+    if (*dev < 0 || *dev >= 64) return fail_cuda(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_dev_known[*dev]) {
+        int rc = query_device(*dev, &g_dev[*dev]);
+        if (rc != RS_OK) return rc;
+        g_dev_known[*dev] = true;
+    }
+    *info = g_dev[*dev];
+    return RS_OK;
+}
+
+// The kernels dereference `p` directly: it must be memory the current
+// device can address at that same address.
+int check_device_pointer(const void* p, int dev) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return RS_ERR_NOT_DEVICE_MEMORY;
+    }
+    switch (a.type) {
+        case cudaMemoryTypeDevice:
+            return a.device == dev ? RS_OK : RS_ERR_NOT_DEVICE_MEMORY;
+        case cudaMemoryTypeManaged:
+            return RS_OK;
+        case cudaMemoryTypeHost:
+            return a.devicePointer != nullptr && (uintptr_t)a.devicePointer == (uintptr_t)p
+                       ? RS_OK
+                       : RS_ERR_NOT_DEVICE_MEMORY;
+        default:
+            return RS_ERR_NOT_DEVICE_MEMORY;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int rowsoftmax_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                    int64_t out_row_stride, int dtype, const rs_options* opts, const rs_device_info* dev,
+                    rs_plan* plan) {
+    if (!plan) return RS_ERR_INVALID_ARG;
+    return validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, opts, dev, plan);
+}
+
+int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                      int64_t out_row_stride, int dtype, cudaStream_t stream, const rs_options* opts) {
+    // Shape and argument errors first: they need no device.
+    rs_device_info probe;
+    memset(&probe, 0, sizeof(probe));
+    probe.sm_count = 1;
+    probe.max_smem_per_block_optin = 1;
+    rs_plan plan;
+    int rc = validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, nullptr, &probe, &plan);
+    if (rc != RS_OK && rc != RS_ERR_NO_PATH) return rc;
+    if (M == 0 || N == 0) return RS_OK;
+
+    int dev = 0;
+    rs_device_info info;
+    rc = current_device(&dev, &info);
+    if (rc != RS_OK) return rc;
+    if ((rc = check_device_pointer(in, dev)) != RS_OK) return rc;
+    if ((rc = check_device_pointer(out, dev)) != RS_OK) return rc;
+    rc = validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, opts, &info, &plan);
+    if (rc != RS_OK) return rc;
+
+    if (plan.path != RS_PATH_ROWS && plan.cluster_size > rs::kMaxClusterPortable) {
+        int n = 0;
+        cudaError_t e = rs::wide_max_active_clusters(plan, &n);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return fail_cuda(e);
+        }
+        if (n < 1) return RS_ERR_NO_PATH;
+    }
+
+    cudaError_t e = cudaSuccess;
+    const int n = (int)N;
+    if (plan.path == RS_PATH_ROWS) {
+        switch (dtype) {
+            case RS_F32: e = rs::launch_rows_f32(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+            case RS_F16: e = rs::launch_rows_f16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+            default: e = rs::launch_rows_bf16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+        }
+    } else {
+        e = rs::launch_wide(plan, in, out, M, n, in_row_stride, out_row_stride, stream);
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    return RS_OK;
+}
+
+int rowsoftmax_fwd(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                   int64_t out_row_stride, int dtype, cudaStream_t stream) {
+    return rowsoftmax_fwd_ex(in, out, M, N, in_row_stride, out_row_stride, dtype, stream, nullptr);
+}
+
+int rowsoftmax_device_info(rs_device_info* dev) {
+    if (!dev) return RS_ERR_INVALID_ARG;
+    int d = 0;
+    return current_device(&d, dev);
+}
+
+const char* rowsoftmax_status_string(int status) {
+    switch (status) {
+        case RS_OK: return "ok";
+        case RS_ERR_INVALID_ARG: return "invalid argument";
+        case RS_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+        case RS_ERR_OVERLAP: return "input and output overlap (only exact in-place is allowed)";
+        case RS_ERR_CUDA: return "CUDA error";
+        case RS_ERR_NOT_DEVICE_MEMORY: return "pointer is not addressable by the current device";
+        case RS_ERR_NO_PATH: return "no kernel configuration serves this shape with these options";
+        default: return "unknown status";
+    }
+}
+
+int rowsoftmax_last_cuda_error(void) {
+    const int e = t_last_cuda_error;
+    t_last_cuda_error = 0;
+    return e;
+}
+
+int rowsoftmax_device_status(unsigned int* flags, int clear) {
+    if (!flags) return RS_ERR_INVALID_ARG;
+    cudaError_t e = rs::read_device_status(flags, clear != 0);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail_cuda(e);
+    }
+    return RS_OK;
+}
+
+int rowsoftmax_layout_owner(int64_t j, int threads, int vec, int* thread, int64_t* slot) {
+    if (j < 0 || threads < 1 || vec < 1 || !thread || !slot) return RS_ERR_INVALID_ARG;
+    *thread = (int)((j / vec) % threads);
+    *slot = (j / ((int64_t)threads * vec)) * vec + j % vec;
+    return RS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+// Device-side building blocks shared by the row-softmax kernels:
+// storage-type traits, 16-byte and element-wise global accesses, the
+// "safe max" used in every exp(x - m), and the warp reductions.
+//
+// Arithmetic is fp32 for every storage type (the "fp32 Accumulation" rule,
+// Hugging Face "triton-kernels" skill page, "Numerics").
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rowsoftmax.h"
+
+namespace rs {
+
+constexpr float kNegInf = -__builtin_inff();
+
+// ---------------------------------------------------------------------------
+// Storage traits.  kVec is the number of elements in one 16-byte access.
+// ---------------------------------------------------------------------------
+template <int DT> struct Traits;
+
+template <> struct Traits<RS_F32> {
+    using storage = float;
+    static constexpr int kVec = 4;
+    __device__ static __forceinline__ float load1(const storage* p) { return __ldcs(p); }
+    __device__ static __forceinline__ void store1(storage* p, float v) { __stcs(p, v); }
+    __device__ static __forceinline__ void unpack(const uint4& u, float* v) {
+        v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+        v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+    }
+    __device__ static __forceinline__ uint4 pack(const float* v) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                          __float_as_uint(v[2]), __float_as_uint(v[3]));
+    }
+};
+
+template <> struct Traits<RS_BF16> {
+    using storage = __nv_bfloat16;
+    static constexpr int kVec = 8;
+    // bf16 is the upper half of an fp32 bit pattern: widening is a shift.
+    __device__ static __forceinline__ float widen(unsigned short b) {
+        return __uint_as_float(((unsigned int)b) << 16);
+    }
+    __device__ static __forceinline__ float load1(const storage* p) {
+        return widen(__ldcs(reinterpret_cast<const unsigned short*>(p)));
+    }
+    __device__ static __forceinline__ void store1(storage* p, float v) {
+        __nv_bfloat16 b = __float2bfloat16_rn(v);
+        __stcs(reinterpret_cast<unsigned short*>(p), *reinterpret_cast<unsigned short*>(&b));
+    }
+    __device__ static __forceinline__ void unpack2(unsigned int w, float* v) {
+        v[0] = __uint_as_float(w << 16);
+        v[1] = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ static __forceinline__ unsigned int pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<unsigned int*>(&h);
+    }
+    __device__ static __forceinline__ void unpack(const uint4& u, float* v) {
+        unpack2(u.x, v); unpack2(u.y, v + 2); unpack2(u.z, v + 4); unpack2(u.w, v + 6);
+    }
+    __device__ static __forceinline__ uint4 pack(const float* v) {
+        return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+    }
+};
+
+template <> struct Traits<RS_F16> {
+    using storage = __half;
+    static constexpr int kVec = 8;
+    __device__ static __forceinline__ float load1(const storage* p) {
+        unsigned short b = __ldcs(reinterpret_cast<const unsigned short*>(p));
+        return __half2float(*reinterpret_cast<__half*>(&b));
+    }
+    __device__ static __forceinline__ void store1(storage* p, float v) {
+        __half h = __float2half_rn(v);
+        __stcs(reinterpret_cast<unsigned short*>(p), *reinterpret_cast<unsigned short*>(&h));
+    }
+    __device__ static __forceinline__ void unpack2(unsigned int w, float* v) {
+        float2 f = __half22float2(*reinterpret_cast<__half2*>(&w));
+        v[0] = f.x; v[1] = f.y;
+    }
+    __device__ static __forceinline__ unsigned int pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<unsigned int*>(&h);
+    }
+    __device__ static __forceinline__ void unpack(const uint4& u, float* v) {
+        unpack2(u.x, v); unpack2(u.y, v + 2); unpack2(u.z, v + 4); unpack2(u.w, v + 6);
+    }
+    __device__ static __forceinline__ uint4 pack(const float* v) {
+        return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Access of one "unit" of VEC elements starting at element `base` of a row:
+// VEC == Traits::kVec is one 16-byte access (the caller guarantees alignment),
+// VEC == 1 is one element.  Units that run past n are filled with -inf on
+// load and clipped on store, element by element (masked tail).
+// ---------------------------------------------------------------------------
+template <int DT, int VEC>
+__device__ __forceinline__ void load_unit(const typename Traits<DT>::storage* row, int base, int n,
+                                          float* v) {
+    using T = Traits<DT>;
+    if (VEC == T::kVec && base + VEC <= n) {
+        T::unpack(__ldcs(reinterpret_cast<const uint4*>(row + base)), v);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v[e] = (base + e < n) ? T::load1(row + base + e) : kNegInf;
+    }
+}
+
+template <int DT, int VEC>
+__device__ __forceinline__ void store_unit(typename Traits<DT>::storage* row, int base, int n,
+                                           const float* v) {
+    using T = Traits<DT>;
+    if (VEC == T::kVec && base + VEC <= n) {
+        __stcs(reinterpret_cast<uint4*>(row + base), T::pack(v));
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (base + e < n) T::store1(row + base + e, v[e]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// exp(x - m) is always taken against safe(m): a max of -inf (a row, or part
+// of one, with no finite entry) is replaced by 0 so that -inf entries give
+// exp(-inf) = 0 instead of (-inf) - (-inf) = NaN.  Partial sums that belong
+// to a -inf max carry weight 0 in a merge (0 * NaN stays NaN, so a NaN input
+// still reaches the result).  A row with no finite entry ends with a zero
+// sum, and 0 * (1/0) gives the NaN row that the plain formula gives.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float safe_max(float m) { return m == kNegInf ? 0.0f : m; }
+
+// Weight of a partial sum taken against max m when the merged max is ms.
+__device__ __forceinline__ float rescale(float m, float ms) {
+    return m == kNegInf ? 0.0f : __expf(m - ms);
+}
+
+// Reductions over aligned groups of `width` lanes (width a power of two, <= 32).
+__device__ __forceinline__ float group_max(float v, int width) {
+    for (int o = width >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float group_sum(float v, int width) {
+    for (int o = width >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Online-normaliser merge of (m, l) pairs over aligned groups of `width` lanes:
+// m = max(m1, m2), l = l1 * exp(m1 - m) + l2 * exp(m2 - m).
+__device__ __forceinline__ void group_merge(float& m, float& l, int width) {
+    for (int o = width >> 1; o > 0; o >>= 1) {
+        float mo = __shfl_xor_sync(0xffffffffu, m, o);
+        float lo = __shfl_xor_sync(0xffffffffu, l, o);
+        float mn = fmaxf(m, mo);
+        float ms = safe_max(mn);
+        l = l * rescale(m, ms) + lo * rescale(mo, ms);
+        m = mn;
+    }
+}
+
+}  // namespace rs

@@ -1,0 +1,60 @@
+// Internal contract between the C-ABI layer (rowsoftmax_api.cu), the
+// planner and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+#include "rowsoftmax.h"
+
+namespace rs {
+
+// Per-thread unit counts instantiated for RS_PATH_ROWS.  A unit is one
+// 16-byte access (4 fp32 or 8 fp16/bf16 elements) or, for the element-wise
+// kernels, one element.  The planner picks only from these lists and the
+// launchers dispatch over exactly the same lists.
+#define RS_VPT_VEC_F32 1, 2, 3, 4, 5, 6, 8, 10, 12, 16
+#define RS_VPT_VEC_16 1, 2, 3, 4, 5, 6, 8
+#define RS_VPT_SCALAR 1, 2, 4, 8, 16
+
+constexpr int kVptVecF32[] = {RS_VPT_VEC_F32};
+constexpr int kVptVec16[] = {RS_VPT_VEC_16};
+constexpr int kVptScalar[] = {RS_VPT_SCALAR};
+
+// Upper bound on fp32 values a thread holds in RS_PATH_ROWS (register budget).
+constexpr int kRowsMaxValuesPerThread = 64;
+constexpr int kRowsMaxThreads = 1024;
+
+// Largest CTA an RS_PATH_ROWS instance is compiled for.  1024 threads leave
+// 64 registers a thread, enough for up to 8 units and 32 values; larger
+// instances are compiled for 512 threads (128 registers) so they do not spill.
+constexpr int rows_block_limit(int vpt, int vec) { return (vpt <= 8 && vpt * vec <= 32) ? 1024 : 512; }
+
+// Cluster kernels (RS_PATH_CLUSTER / RS_PATH_STREAM).
+constexpr int kWideThreads = 256;      // threads per CTA
+constexpr int kWideUnitsPerThread = 4; // units per thread per stage
+constexpr int kWideUnitsPerStage = kWideThreads * kWideUnitsPerThread;
+constexpr int kWideMaxStages = 16;     // mbarriers per CTA
+constexpr int kMaxClusterPortable = 8;
+constexpr int kMaxCluster = 16;        // needs the non-portable cluster-size opt-in
+constexpr size_t kWideStaticSmem = 1024;  // upper bound of the kernel's static shared memory
+
+// Launchers.  Each returns the CUDA error of the launch (cudaSuccess if it
+// was enqueued).  Arguments were validated and planned by the caller.
+cudaError_t launch_rows_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                            int64_t ldi, int64_t ldo, cudaStream_t s);
+cudaError_t launch_rows_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                            int64_t ldi, int64_t ldo, cudaStream_t s);
+cudaError_t launch_rows_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                             int64_t ldi, int64_t ldo, cudaStream_t s);
+cudaError_t launch_wide(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                        int64_t ldi, int64_t ldo, cudaStream_t s);
+
+// Number of clusters of the planned wide kernel that fit on the device at
+// once (0: the cluster shape cannot be scheduled).
+cudaError_t wide_max_active_clusters(const rs_plan& p, int* n);
+
+// Device status word (owned by the cluster-kernel translation unit).
+cudaError_t read_device_status(unsigned int* flags, bool clear);
+
+}  // namespace rs

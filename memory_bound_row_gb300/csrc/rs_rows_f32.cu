@@ -1,0 +1,15 @@
+// RS_PATH_ROWS instances for fp32 storage.
+#include "rs_rows.cuh"
+
+namespace rs {
+
+cudaError_t launch_rows_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                            int64_t ldi, int64_t ldo, cudaStream_t s) {
+    if (p.vec_elems == Traits<RS_F32>::kVec)
+        return RowsDispatch<RS_F32, Traits<RS_F32>::kVec, RS_VPT_VEC_F32>::go(p, in, out, M, N, ldi, ldo, s);
+    if (p.vec_elems == 1)
+        return RowsDispatch<RS_F32, 1, RS_VPT_SCALAR>::go(p, in, out, M, N, ldi, ldo, s);
+    return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace rs

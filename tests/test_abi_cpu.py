@@ -1,0 +1,194 @@
+"""CPU checks of the C-ABI library: it loads, exports every entry point that
+include/rowsoftmax.h declares, rejects bad arguments before touching a
+device, and plans the launches described in its header.  No kernel runs."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import memory_bound_row_gb300 as rs
+from memory_bound_row_gb300 import _abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rowsoftmax.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "group_cyclic_layout.txt")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"RS_API\s+[\w\s\*]*?\b(rowsoftmax_\w+)\s*\(", text)))
+
+
+def gb300():
+    d = rs.rs_device_info()
+    d.sm_count = 152
+    d.max_smem_per_block_optin = 232448
+    d.max_smem_per_sm = 233472
+    d.max_threads_per_sm = 2048
+    d.cc_major, d.cc_minor = 10, 3
+    return d
+
+
+def test_library_exports_every_declared_entry_point():
+    declared = _declared()
+    assert len(declared) >= 8
+    lib = ctypes.CDLL(_abi.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(_abi.EXPORTED) == declared
+
+
+def test_status_strings():
+    for code in range(7):
+        assert rs.rowsoftmax_status_string(code) != "unknown status"
+    assert rs.rowsoftmax_status_string(99) == "unknown status"
+
+
+A = 1 << 20  # a 16-byte aligned fake address; validation fails before it is used
+
+
+@pytest.mark.parametrize(
+    "args,status",
+    [
+        ((A, A + (1 << 16), 4, 8, 8, 8, 7), rs.RS_ERR_UNSUPPORTED_DTYPE),
+        ((A, A + (1 << 16), -1, 8, 8, 8, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+        ((A, A + (1 << 16), 4, -8, 8, 8, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+        ((0, A, 4, 8, 8, 8, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+        ((A, 0, 4, 8, 8, 8, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+        ((A, A + (1 << 16), 4, 8, 7, 8, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+        ((A, A + (1 << 16), 4, 8, 8, 7, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+        ((A + 1, A + (1 << 16), 4, 8, 8, 8, rs.RS_F16), rs.RS_ERR_INVALID_ARG),
+        ((A + 2, A + (1 << 16), 4, 8, 8, 8, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+        ((A, A + 64, 4, 8, 8, 8, rs.RS_F32), rs.RS_ERR_OVERLAP),
+        ((A, A, 4, 8, 8, 16, rs.RS_F32), rs.RS_ERR_OVERLAP),
+        ((A, A + 4, 1, 8, 8, 8, rs.RS_F32), rs.RS_ERR_OVERLAP),
+        ((A, A + (1 << 16), 2, (1 << 31), 1 << 31, 1 << 31, rs.RS_F16), rs.RS_ERR_INVALID_ARG),
+        ((A, A + (1 << 16), 1 << 62, 8, 1 << 20, 8, rs.RS_F32), rs.RS_ERR_INVALID_ARG),
+    ],
+)
+def test_bad_arguments_are_rejected_before_any_device_call(args, status):
+    assert rs.rowsoftmax_fwd(*args, 0) == status
+    rc, _ = rs.rowsoftmax_plan(*args, None, gb300())
+    assert rc == status
+
+
+def test_empty_problems_are_a_noop():
+    assert rs.rowsoftmax_fwd(0, 0, 0, 8, 8, 8, rs.RS_F32, 0) == rs.RS_OK
+    assert rs.rowsoftmax_fwd(0, 0, 8, 0, 0, 0, rs.RS_BF16, 0) == rs.RS_OK
+    rc, plan = rs.rowsoftmax_plan(0, 0, 0, 8, 8, 8, rs.RS_F32, None, gb300())
+    assert rc == rs.RS_OK and plan["grid"] == 0
+
+
+def test_exact_in_place_is_accepted_by_the_planner():
+    rc, plan = rs.rowsoftmax_plan(A, A, 64, 1000, 1024, 1024, rs.RS_F32, None, gb300())
+    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_ROWS
+
+
+def test_disjoint_interleaved_layout_is_rejected_as_overlap():
+    # Ranges are compared, not element sets: interleaved rows count as overlap.
+    rc, _ = rs.rowsoftmax_plan(A, A + 32, 4, 8, 16, 16, rs.RS_F32, None, gb300())
+    assert rc == rs.RS_ERR_OVERLAP
+
+
+def _plan(M, N, dtype, ld=None, opts=None, a=A, b=A + (1 << 40)):
+    rc, plan = rs.rowsoftmax_plan(a, b, M, N, ld or N, ld or N, dtype, opts, gb300())
+    assert rc == rs.RS_OK, rs.rowsoftmax_status_string(rc)
+    return plan
+
+
+def _covers(plan, N):
+    units = -(-N // plan["vec_elems"])
+    if plan["path"] == rs.RS_PATH_ROWS:
+        return plan["threads_per_row"] * plan["vec_per_thread"] >= units
+    return plan["cluster_size"] * plan["chunk_elems"] >= N
+
+
+def test_plans_for_the_benchmark_workloads():
+    p = _plan(1024, 1024, rs.RS_F32)
+    assert (p["path"], p["vec_elems"], p["threads_per_row"]) == (rs.RS_PATH_ROWS, 4, 32)
+    p = _plan(8192, 5000, rs.RS_F32, ld=5120)
+    assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 4 and _covers(p, 5000)
+    p = _plan(32768, 8192, rs.RS_BF16)
+    assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 8 and _covers(p, 8192)
+    p = _plan(512, 131072, rs.RS_F16)
+    assert p["path"] == rs.RS_PATH_CLUSTER and p["cluster_size"] >= 2 and _covers(p, 131072)
+    assert p["smem_bytes"] <= 232448 - 1024 and p["grid"] == 512 * p["cluster_size"]
+    p = _plan(1 << 20, 2048, rs.RS_BF16)
+    assert p["path"] == rs.RS_PATH_ROWS and _covers(p, 2048)
+
+
+def test_misaligned_data_gets_the_element_wise_kernels():
+    p = _plan(1823, 781, rs.RS_F32)  # stride 781 * 4 bytes is not a multiple of 16
+    assert p["vec_elems"] == 1 and _covers(p, 781)
+    p = _plan(16, 1024, rs.RS_F32, a=A + 4)
+    assert p["vec_elems"] == 1
+    p = _plan(16, 1024, rs.RS_BF16, b=A + (1 << 40) + 2)
+    assert p["vec_elems"] == 1
+    p = _plan(1, 1000, rs.RS_F16, ld=1001)  # one row: its stride does not matter
+    assert p["vec_elems"] == 8
+
+
+@pytest.mark.parametrize("dtype", [rs.RS_F32, rs.RS_F16, rs.RS_BF16])
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 9, 31, 32, 33, 255, 1000, 4096, 5000, 8192, 8193, 16384,
+                               65536, 131072, 1 << 20, 1 << 24])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_auto_plan_always_covers_the_row(dtype, N, aligned):
+    a = A if aligned else A + 2 * (1 if dtype else 2)
+    p = _plan(3, N, dtype, a=a)
+    assert _covers(p, N)
+    if p["path"] == rs.RS_PATH_CLUSTER:
+        assert p["vec_elems"] > 1 and p["stages"] <= 16 and p["smem_bytes"] % 16 == 0
+        assert (p["chunk_elems"] * (4 if dtype == rs.RS_F32 else 2)) % 16 == 0
+    if p["path"] == rs.RS_PATH_ROWS:
+        assert p["block_threads"] % p["threads_per_row"] == 0 and p["block_threads"] <= 1024
+
+
+def test_forced_options():
+    o = {"path": rs.RS_PATH_ROWS, "threads_per_row": 64, "vec_per_thread": 4}
+    p = _plan(100, 1000, rs.RS_F32, opts=o)
+    assert (p["threads_per_row"], p["vec_per_thread"]) == (64, 4)
+    rc, _ = rs.rowsoftmax_plan(A, A + (1 << 40), 100, 1000, 1000, 1000, rs.RS_F32,
+                               {"path": rs.RS_PATH_ROWS, "threads_per_row": 32, "vec_per_thread": 4}, gb300())
+    assert rc == rs.RS_ERR_NO_PATH  # 32 threads x 4 units of 4 cannot hold 1000 elements
+    rc, _ = rs.rowsoftmax_plan(A, A + (1 << 40), 100, 1000, 1000, 1000, rs.RS_F32,
+                               {"path": rs.RS_PATH_ROWS, "threads_per_row": 48}, gb300())
+    assert rc == rs.RS_ERR_INVALID_ARG
+    rc, _ = rs.rowsoftmax_plan(A + 4, A + (1 << 40), 100, 1000, 1000, 1000, rs.RS_F32,
+                               {"path": rs.RS_PATH_CLUSTER}, gb300())
+    assert rc == rs.RS_ERR_NO_PATH  # bulk copies need 16-byte alignment
+    p = _plan(7, 100000, rs.RS_BF16, opts={"path": rs.RS_PATH_STREAM, "cluster_size": 3})
+    assert p["cluster_size"] == 3 and _covers(p, 100000)
+    p = _plan(7, 1000, rs.RS_BF16, opts={"path": rs.RS_PATH_CLUSTER, "cluster_size": 16})
+    assert p["cluster_size"] == 16 and p["grid"] == 7 * 16
+    p = _plan(1000, 1000, rs.RS_F32, opts={"grid_limit": 5})
+    assert p["grid"] == 5
+
+
+def test_layout_owner_matches_the_pages_worked_example():
+    with open(GOLDEN) as f:
+        lines = [ln for ln in f if ln.strip() and not ln.startswith("#")]
+    for ln in lines:
+        head, owners = ln.split("|")
+        threads, vec = map(int, head.split())
+        want = list(map(int, owners.split()))
+        got = [rs.rowsoftmax_layout_owner(j, threads, vec)[1] for j in range(len(want))]
+        assert got == want
+
+
+def test_layout_owner_is_a_bijection():
+    threads, vec, n = 32, 4, 32 * 4 * 5
+    seen = set()
+    for j in range(n):
+        rc, t, s = rs.rowsoftmax_layout_owner(j, threads, vec)
+        assert rc == rs.RS_OK
+        seen.add((t, s))
+        # 16-byte groups: elements of one group share a thread and fill consecutive slots
+        assert t == (j // vec) % threads
+    assert len(seen) == n
+    assert rs.rowsoftmax_layout_owner(-1, 2, 2)[0] == rs.RS_ERR_INVALID_ARG
