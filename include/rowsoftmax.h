@@ -79,8 +79,11 @@ typedef enum {
     RS_PATH_CLUSTER = 2,  /* wide rows: a cluster of CTAs per row, each CTA stages its slice in
                              shared memory with bulk asynchronous copies (TMA engine), online (m, l),
                              partial pairs merged over distributed shared memory; reads HBM once */
-    RS_PATH_STREAM = 3    /* any row: a cluster per row streams its slice twice from global memory
+    RS_PATH_STREAM = 3,   /* any row: a cluster per row streams its slice twice from global memory
                              (online (m, l) on the first read, normalise on the second); reads 2x */
+    RS_PATH_RING = 4      /* single pass as RS_PATH_ROWS, but a persistent grid whose CTAs stage the
+                             next row groups in a ring of shared-memory stages filled by bulk
+                             asynchronous copies (TMA engine); 16-byte aligned data only */
 } rs_path;
 
 /*
@@ -93,6 +96,7 @@ typedef struct {
     int vec_per_thread;   /* RS_PATH_ROWS: 16-byte vectors (or elements, when scalar) per thread */
     int block_threads;    /* threads per CTA (RS_PATH_ROWS: multiple of threads_per_row) */
     int cluster_size;     /* RS_PATH_CLUSTER / RS_PATH_STREAM: CTAs per row, 1..16 */
+    int stages;           /* RS_PATH_RING: shared-memory stages per CTA, 2..8 */
     int force_scalar;     /* 1: element-wise accesses even when 16-byte vectors would be legal */
     int64_t grid_limit;   /* >0: cap on CTAs (rows loop inside the kernel); 0: one launch slot per row group */
 } rs_options;
@@ -102,12 +106,12 @@ typedef struct {
     int path;             /* rs_path actually chosen */
     int dtype;
     int vec_elems;        /* elements per access: 16/elem_size, or 1 for the element-wise kernels */
-    int threads_per_row;  /* RS_PATH_ROWS */
-    int vec_per_thread;   /* RS_PATH_ROWS */
-    int rows_per_cta;     /* RS_PATH_ROWS */
+    int threads_per_row;  /* RS_PATH_ROWS / RS_PATH_RING */
+    int vec_per_thread;   /* RS_PATH_ROWS / RS_PATH_RING */
+    int rows_per_cta;     /* RS_PATH_ROWS; rows per stage for RS_PATH_RING */
     int block_threads;
-    int cluster_size;     /* CTAs per row (1 for RS_PATH_ROWS) */
-    int stages;           /* RS_PATH_CLUSTER: bulk-copy stages per CTA */
+    int cluster_size;     /* CTAs per row (1 for RS_PATH_ROWS / RS_PATH_RING) */
+    int stages;           /* RS_PATH_CLUSTER: bulk-copy stages per CTA; RS_PATH_RING: ring depth */
     int64_t chunk_elems;  /* RS_PATH_CLUSTER / RS_PATH_STREAM: row slice per CTA */
     int64_t grid;         /* CTAs launched */
     size_t smem_bytes;    /* dynamic shared memory per CTA */

@@ -21,6 +21,7 @@ from ._abi import (  # noqa: F401
     RS_OK,
     RS_PATH_AUTO,
     RS_PATH_CLUSTER,
+    RS_PATH_RING,
     RS_PATH_ROWS,
     RS_PATH_STREAM,
     rowsoftmax_device_info,

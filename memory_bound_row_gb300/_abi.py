@@ -24,8 +24,9 @@ RS_ERR_CUDA = 4
 RS_ERR_NOT_DEVICE_MEMORY = 5
 RS_ERR_NO_PATH = 6
 # rs_path
-RS_PATH_AUTO, RS_PATH_ROWS, RS_PATH_CLUSTER, RS_PATH_STREAM = 0, 1, 2, 3
-PATH_NAMES = {RS_PATH_AUTO: "auto", RS_PATH_ROWS: "rows", RS_PATH_CLUSTER: "cluster", RS_PATH_STREAM: "stream"}
+RS_PATH_AUTO, RS_PATH_ROWS, RS_PATH_CLUSTER, RS_PATH_STREAM, RS_PATH_RING = 0, 1, 2, 3, 4
+PATH_NAMES = {RS_PATH_AUTO: "auto", RS_PATH_ROWS: "rows", RS_PATH_CLUSTER: "cluster", RS_PATH_STREAM: "stream",
+              RS_PATH_RING: "ring"}
 
 EXPORTED = (
     "rowsoftmax_fwd",
@@ -46,6 +47,7 @@ class rs_options(ctypes.Structure):
         ("vec_per_thread", ctypes.c_int),
         ("block_threads", ctypes.c_int),
         ("cluster_size", ctypes.c_int),
+        ("stages", ctypes.c_int),
         ("force_scalar", ctypes.c_int),
         ("grid_limit", ctypes.c_int64),
     ]

@@ -33,6 +33,8 @@ constexpr int64_t kMaxGrid = (int64_t)INT_MAX;
 constexpr int kRowsTargetValues = 32;             // fp32 values a thread holds (auto)
 constexpr int64_t kRowsMaxRowBytes = 32 * 1024;   // auto: rows up to this go to RS_PATH_ROWS
 constexpr int64_t kClusterTargetSlice = 64 * 1024;  // auto: bytes of row slice per CTA
+constexpr int64_t kRingMinRowBytes = 512;           // auto: shorter rows stay on RS_PATH_ROWS
+constexpr int64_t kRingTargetSmem = 64 * 1024;      // auto: ring bytes per CTA (stages x stage)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -88,7 +90,10 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
                 tpr = (int)round_up(need, 32);
             }
         } else {
-            const int vt = kRowsTargetValues / vec > 0 ? kRowsTargetValues / vec : 1;
+            int n_inst = 0;
+            const int* inst = vpt_table(dtype, vec, &n_inst);
+            int vt = kRowsTargetValues / vec > 0 ? kRowsTargetValues / vec : 1;
+            if (vt > inst[n_inst - 1]) vt = inst[n_inst - 1];
             const int64_t need = ceil_div(units, vt);
             if (need <= 32) {
                 tpr = 1;
@@ -131,6 +136,52 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
     p->chunk_elems = 0;
     p->grid = grid;
     p->smem_bytes = 0;
+    return RS_OK;
+}
+
+// Resident CTAs of one SM for a kernel of `block` threads and `smem` dynamic
+// bytes, assuming the register budget its launch bound allows.
+int64_t ctas_per_sm(const rs_device_info& dev, int block, size_t smem, int regs_per_thread) {
+    int64_t by_threads = dev.max_threads_per_sm > 0 ? dev.max_threads_per_sm / block : 1;
+    int64_t by_regs = 65536 / ((int64_t)block * regs_per_thread);
+    int64_t by_smem = dev.max_smem_per_sm > 0 ? (int64_t)dev.max_smem_per_sm / (int64_t)(smem + 2048) : 1;
+    int64_t n = by_threads;
+    if (by_regs < n) n = by_regs;
+    if (by_smem < n) n = by_smem;
+    if (n > 32) n = 32;
+    return n < 1 ? 1 : n;
+}
+
+int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_options& o,
+              const rs_device_info& dev, rs_plan* p) {
+    if (vec == 1) return RS_ERR_NO_PATH;  // bulk copies need 16-byte units
+    if (o.stages && (o.stages < 2 || o.stages > rs::kRingMaxStages)) return RS_ERR_INVALID_ARG;
+    rs_options ro = o;
+    ro.grid_limit = 0;
+    int rc = plan_rows(dtype, vec, M, units, ro, p);
+    if (rc != RS_OK) return rc;
+    const int64_t slot = (N / vec) * 16;
+    const int64_t stage = slot * p->rows_per_cta;
+    if (stage <= 0) return RS_ERR_NO_PATH;
+    const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kRingStaticSmem;
+    int stages = o.stages;
+    if (!stages) {
+        int64_t s = kRingTargetSmem / stage;
+        if (s < 2) s = 2;
+        if (s > rs::kRingMaxStages) s = rs::kRingMaxStages;
+        stages = (int)s;
+    }
+    const int64_t smem = stage * stages;
+    if (smem > max_dyn || stage >= (1 << 20)) return RS_ERR_NO_PATH;  // mbarrier tx count < 2^20
+    const int regs = rs::rows_block_limit(p->vec_per_thread, vec) == 1024 ? 64 : 128;
+    const int64_t groups = ceil_div(M, p->rows_per_cta);
+    int64_t grid = (int64_t)dev.sm_count * ctas_per_sm(dev, p->block_threads, (size_t)smem, regs);
+    if (grid > groups) grid = groups;
+    if (o.grid_limit > 0 && grid > o.grid_limit) grid = o.grid_limit;
+    p->path = RS_PATH_RING;
+    p->stages = stages;
+    p->smem_bytes = (size_t)smem;
+    p->grid = grid;
     return RS_OK;
 }
 
@@ -196,8 +247,8 @@ int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int
     rs_options o;
     memset(&o, 0, sizeof(o));
     if (opts) o = *opts;
-    if (o.path < RS_PATH_AUTO || o.path > RS_PATH_STREAM || o.grid_limit < 0 || o.vec_per_thread < 0 ||
-        o.threads_per_row < 0 || o.block_threads < 0 || o.cluster_size < 0)
+    if (o.path < RS_PATH_AUTO || o.path > RS_PATH_RING || o.grid_limit < 0 || o.vec_per_thread < 0 ||
+        o.threads_per_row < 0 || o.block_threads < 0 || o.cluster_size < 0 || o.stages < 0)
         return RS_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return RS_OK;  // nothing to do, nothing launched
     if (N > kMaxN) return RS_ERR_INVALID_ARG;
@@ -225,6 +276,10 @@ int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int
     int path = o.path;
     if (path == RS_PATH_AUTO) {
         int rc = RS_ERR_NO_PATH;
+        if (vec_ok && N * es >= kRingMinRowBytes && N * es <= kRowsMaxRowBytes)
+            rc = plan_ring(dtype, vec, M, N, units, o, *dev, p);
+        if (rc == RS_OK) return RS_OK;
+        if (rc != RS_ERR_NO_PATH) return rc;
         if (N * es <= kRowsMaxRowBytes) rc = plan_rows(dtype, vec, M, units, o, p);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
@@ -236,6 +291,7 @@ int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int
         return plan_wide(dtype, RS_PATH_STREAM, vec, M, N, o, *dev, p);
     }
     if (path == RS_PATH_ROWS) return plan_rows(dtype, vec, M, units, o, p);
+    if (path == RS_PATH_RING) return plan_ring(dtype, vec, M, N, units, o, *dev, p);
     return plan_wide(dtype, path, vec, M, N, o, *dev, p);
 }
 
@@ -333,7 +389,8 @@ int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t i
     rc = validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, opts, &info, &plan);
     if (rc != RS_OK) return rc;
 
-    if (plan.path != RS_PATH_ROWS && plan.cluster_size > rs::kMaxClusterPortable) {
+    if ((plan.path == RS_PATH_CLUSTER || plan.path == RS_PATH_STREAM) &&
+        plan.cluster_size > rs::kMaxClusterPortable) {
         int n = 0;
         cudaError_t e = rs::wide_max_active_clusters(plan, &n);
         if (e != cudaSuccess) {
@@ -350,6 +407,12 @@ int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t i
             case RS_F32: e = rs::launch_rows_f32(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
             case RS_F16: e = rs::launch_rows_f16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
             default: e = rs::launch_rows_bf16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+        }
+    } else if (plan.path == RS_PATH_RING) {
+        switch (dtype) {
+            case RS_F32: e = rs::launch_ring_f32(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+            case RS_F16: e = rs::launch_ring_f16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+            default: e = rs::launch_ring_bf16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
         }
     } else {
         e = rs::launch_wide(plan, in, out, M, n, in_row_stride, out_row_stride, stream);
@@ -390,7 +453,11 @@ int rowsoftmax_last_cuda_error(void) {
 
 int rowsoftmax_device_status(unsigned int* flags, int clear) {
     if (!flags) return RS_ERR_INVALID_ARG;
-    cudaError_t e = rs::read_device_status(flags, clear != 0);
+    *flags = 0;
+    cudaError_t e = rs::read_status_wide(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_f32(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_f16(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_bf16(flags, clear != 0);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return fail_cuda(e);

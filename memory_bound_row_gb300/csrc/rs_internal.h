@@ -30,6 +30,10 @@ constexpr int kRowsMaxThreads = 1024;
 // instances are compiled for 512 threads (128 registers) so they do not spill.
 constexpr int rows_block_limit(int vpt, int vec) { return (vpt <= 8 && vpt * vec <= 32) ? 1024 : 512; }
 
+// Persistent ring kernel (RS_PATH_RING).
+constexpr int kRingMaxStages = 8;
+constexpr size_t kRingStaticSmem = 1024;  // upper bound of the kernel's static shared memory
+
 // Cluster kernels (RS_PATH_CLUSTER / RS_PATH_STREAM).
 constexpr int kWideThreads = 256;      // threads per CTA
 constexpr int kWideUnitsPerThread = 4; // units per thread per stage
@@ -47,6 +51,12 @@ cudaError_t launch_rows_f16(const rs_plan& p, const void* in, void* out, int64_t
                             int64_t ldi, int64_t ldo, cudaStream_t s);
 cudaError_t launch_rows_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
                              int64_t ldi, int64_t ldo, cudaStream_t s);
+cudaError_t launch_ring_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                            int64_t ldi, int64_t ldo, cudaStream_t s);
+cudaError_t launch_ring_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                            int64_t ldi, int64_t ldo, cudaStream_t s);
+cudaError_t launch_ring_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                             int64_t ldi, int64_t ldo, cudaStream_t s);
 cudaError_t launch_wide(const rs_plan& p, const void* in, void* out, int64_t M, int N,
                         int64_t ldi, int64_t ldo, cudaStream_t s);
 
@@ -54,7 +64,11 @@ cudaError_t launch_wide(const rs_plan& p, const void* in, void* out, int64_t M, 
 // once (0: the cluster shape cannot be scheduled).
 cudaError_t wide_max_active_clusters(const rs_plan& p, int* n);
 
-// Device status word (owned by the cluster-kernel translation unit).
-cudaError_t read_device_status(unsigned int* flags, bool clear);
+// Device status words, one per translation unit with bounded waits; each
+// ORs its word into *flags (and clears it when asked).
+cudaError_t read_status_f32(unsigned int* flags, bool clear);
+cudaError_t read_status_f16(unsigned int* flags, bool clear);
+cudaError_t read_status_bf16(unsigned int* flags, bool clear);
+cudaError_t read_status_wide(unsigned int* flags, bool clear);
 
 }  // namespace rs

@@ -1,0 +1,239 @@
+// RS_PATH_RING: persistent single-pass row softmax whose input rows are
+// staged through a ring of shared-memory stages by bulk asynchronous copies.
+//
+// The arithmetic is that of RS_PATH_ROWS (rs_rows.cuh): one group of `tpr`
+// threads per row, the row in registers as 16-byte group-cyclic units, a
+// warp-local max, one exp per element, per-warp (m, l) pairs merged with the
+// online normaliser.  What changes is where the bytes in flight live.  A
+// register-resident row costs registers for every byte being fetched, which
+// caps the bytes in flight per SM well below what HBM needs to stay busy.
+// Here each CTA keeps `stages` groups of rows in flight in shared memory:
+// one thread issues a cp.async.bulk (TMA engine) copy per row into the next
+// free stage, with completion counted on that stage's mbarrier, while all
+// threads compute on the oldest stage.  Each CTA loops over row groups
+// blockIdx.x, blockIdx.x + gridDim.x, ... (a persistent grid sized to the
+// resident CTAs), so copies for later groups overlap the compute and the
+// stores of the current one.  The multi-stage ring with deferred consumption
+// is the scheme the nano-triton post describes for its matmul ("Version 2: a
+// cp.async pipeline"), applied to rows and carried by the bulk-copy engine.
+//
+// The last partial 16-byte unit of a row (N not a multiple of 16 bytes) is
+// read straight from global memory.  Waits are bounded (rs_async.cuh); a wait
+// that runs out flags the device status word, and the CTA lets its copies in
+// flight land (bounded again) and stops.
+#pragma once
+
+#include <mutex>
+
+#include "rs_async.cuh"
+#include "rs_common.cuh"
+#include "rs_internal.h"
+
+namespace rs {
+
+template <int DT, int VPT>
+__global__ void __launch_bounds__(rows_block_limit(VPT, Traits<DT>::kVec))
+ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, int stages) {
+    using T = Traits<DT>;
+    using S = typename T::storage;
+    constexpr int VEC = T::kVec;
+    const S* in = static_cast<const S*>(in_);
+    S* out = static_cast<S*>(out_);
+
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kRingMaxStages];
+    __shared__ float2 part[2][32];
+
+    const int rpg = blockDim.x / tpr;  // rows per group (one group per stage)
+    const int grp = threadIdx.x / tpr;
+    const int t = threadIdx.x - grp * tpr;
+    const int width = tpr < 32 ? tpr : 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int wpr = tpr >> 5;
+
+    const int units_full = N / VEC;                  // whole 16-byte units per row (bulk-copied)
+    const uint32_t slot = (uint32_t)units_full * 16u;  // bytes of one row in a stage
+    const size_t stage_bytes = (size_t)slot * rpg;
+    const int64_t groups = (M + rpg - 1) / rpg;
+
+    // Thread 0: fill stage s with row group g.
+    auto issue = [&](int s, int64_t g) {
+        const int64_t r0 = g * rpg;
+        const int nrows = (int)(M - r0 < rpg ? M - r0 : rpg);
+        if (slot == 0) {
+            mbar_arrive(&full[s]);
+            return;
+        }
+        mbar_arrive_expect_tx(&full[s], slot * (uint32_t)nrows);
+        unsigned char* dst = ring + (size_t)s * stage_bytes;
+        for (int k = 0; k < nrows; ++k) bulk_load(dst + (size_t)k * slot, in + (r0 + k) * ldi, slot, &full[s]);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            const int64_t g = blockIdx.x + (int64_t)s * gridDim.x;
+            if (g < groups) issue(s, g);
+        }
+    }
+
+    bool abort = false;
+    int s = 0;
+    uint32_t parity = 0;
+    int64_t it = 0;
+    for (int64_t g = blockIdx.x; g < groups; g += gridDim.x, ++it) {
+        if (!abort && !mbar_wait_bounded(&full[s], parity)) {
+            abort = true;
+            flag_timeout();
+        }
+        const int64_t row = g * rpg + grp;
+        const bool active = row < M;
+        const unsigned char* srow = ring + (size_t)s * stage_bytes + (size_t)grp * slot;
+
+        float v[VPT][VEC];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int u = t + k * tpr;
+            if (active && u < units_full) {
+                T::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)u * 16), v[k]);
+            } else if (active && u * VEC < N) {
+                load_unit<DT, VEC>(in + row * ldi, u * VEC, N, v[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = kNegInf;
+            }
+        }
+
+        float m = kNegInf;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = group_max(m, width);
+        const float ms = safe_max(m);
+
+        float l = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = __expf(v[k][e] - ms);
+                l += v[k][e];
+            }
+        l = group_sum(l, width);
+
+        float c;
+        if (tpr <= 32) {
+            c = 1.0f / l;
+        } else {
+            float2* p = part[it & 1];
+            if (lane == 0) p[warp] = make_float2(m, l);
+            __syncthreads();
+            const int w0 = (warp / wpr) * wpr;
+            float pm = kNegInf, pl = 0.0f;
+            if (lane < wpr) {
+                const float2 q = p[w0 + lane];
+                pm = q.x;
+                pl = q.y;
+            }
+            const float mrow = group_max(pm, 32);
+            const float mrs = safe_max(mrow);
+            const float srow_sum = group_sum(pl * rescale(pm, mrs), 32);
+            c = rescale(m, mrs) / srow_sum;
+        }
+
+        if (active) {
+            S* yr = out + row * ldo;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+                store_unit<DT, VEC>(yr, (t + k * tpr) * VEC, N, v[k]);
+            }
+        }
+
+        // Every thread is done with stage s; refill it with the group
+        // `stages` iterations ahead.
+        if (__syncthreads_or(abort)) {
+            abort = true;
+            break;
+        }
+        if (threadIdx.x == 0) {
+            const int64_t gn = g + (int64_t)stages * gridDim.x;
+            if (gn < groups) {
+                fence_proxy_async_smem();
+                issue(s, gn);
+            }
+        }
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+
+    if (abort && threadIdx.x == 0) {
+        // Let the copies of iterations it .. it + stages - 1 land before the
+        // shared memory is released (iteration j used stage j % stages with
+        // parity (j / stages) & 1).
+        for (int64_t j = it; j < it + stages; ++j) {
+            const int64_t gj = blockIdx.x + j * gridDim.x;
+            if (gj >= groups) break;
+            (void)mbar_wait_bounded(&full[j % stages], (uint32_t)((j / stages) & 1));
+        }
+    }
+}
+
+template <int DT, int VPT>
+cudaError_t launch_ring_one(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                            int64_t ldo, cudaStream_t s) {
+    auto kern = ring_kernel<DT, VPT>;
+    // The dynamic shared-memory ceiling is a per-device attribute: raise it to
+    // the device maximum once per device for this instance.
+    static std::mutex mu;
+    static bool ready[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!ready[dev]) {
+            int optin = 0;
+            err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            if (err != cudaSuccess) return err;
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       optin - (int)kRingStaticSmem);
+            if (err != cudaSuccess) return err;
+            ready[dev] = true;
+        }
+    }
+    kern<<<(unsigned)p.grid, p.block_threads, p.smem_bytes, s>>>(in, out, M, N, ldi, ldo, p.threads_per_row,
+                                                                 p.stages);
+    return cudaGetLastError();
+}
+
+template <int DT, int... Vs>
+struct RingDispatch;
+
+template <int DT>
+struct RingDispatch<DT> {
+    static cudaError_t go(const rs_plan&, const void*, void*, int64_t, int, int64_t, int64_t, cudaStream_t) {
+        return cudaErrorInvalidConfiguration;
+    }
+};
+
+template <int DT, int V0, int... Vs>
+struct RingDispatch<DT, V0, Vs...> {
+    static cudaError_t go(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                          int64_t ldo, cudaStream_t s) {
+        if (p.vec_per_thread == V0) return launch_ring_one<DT, V0>(p, in, out, M, N, ldi, ldo, s);
+        return RingDispatch<DT, Vs...>::go(p, in, out, M, N, ldi, ldo, s);
+    }
+};
+
+}  // namespace rs

@@ -1,4 +1,5 @@
-// RS_PATH_ROWS instances for fp32 storage.
+// RS_PATH_ROWS and RS_PATH_RING instances for f32 storage.
+#include "rs_ring.cuh"
 #include "rs_rows.cuh"
 
 namespace rs {
@@ -11,5 +12,13 @@ cudaError_t launch_rows_f32(const rs_plan& p, const void* in, void* out, int64_t
         return RowsDispatch<RS_F32, 1, RS_VPT_SCALAR>::go(p, in, out, M, N, ldi, ldo, s);
     return cudaErrorInvalidConfiguration;
 }
+
+cudaError_t launch_ring_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
+                            int64_t ldi, int64_t ldo, cudaStream_t s) {
+    if (p.vec_elems != Traits<RS_F32>::kVec) return cudaErrorInvalidConfiguration;
+    return RingDispatch<RS_F32, RS_VPT_VEC_F32>::go(p, in, out, M, N, ldi, ldo, s);
+}
+
+cudaError_t read_status_f32(unsigned int* flags, bool clear) { return read_unit_status(flags, clear); }
 
 }  // namespace rs

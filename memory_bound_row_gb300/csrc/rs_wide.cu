@@ -29,78 +29,13 @@
 
 #include <mutex>
 
+#include "rs_async.cuh"
 #include "rs_common.cuh"
 #include "rs_internal.h"
 
 namespace cg = cooperative_groups;
 
 namespace rs {
-
-__device__ unsigned int g_status;
-
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per mbarrier wait
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16) from global to this CTA's shared
-// memory; both addresses 16-byte aligned.  Completion is signalled on `bar`.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return true;
-}
 
 template <int DT, int VEC, bool STAGED>
 __global__ void __launch_bounds__(kWideThreads)
@@ -169,7 +104,7 @@ wide_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         for (int s = 0; s < stages; ++s) {
             if (STAGED && !abort && !mbar_wait_bounded(&bars[s], parity)) {
                 abort = true;
-                atomicOr(&g_status, 1u);
+                flag_timeout();
             }
             float v[kWideUnitsPerThread][VEC];
 #pragma unroll
@@ -370,11 +305,6 @@ cudaError_t wide_max_active_clusters(const rs_plan& p, int* n) {
     }
 }
 
-cudaError_t read_device_status(unsigned int* flags, bool clear) {
-    cudaError_t err = cudaMemcpyFromSymbol(flags, g_status, sizeof(unsigned int));
-    if (err != cudaSuccess || !clear) return err;
-    const unsigned int zero = 0;
-    return cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned int));
-}
+cudaError_t read_status_wide(unsigned int* flags, bool clear) { return read_unit_status(flags, clear); }
 
 }  // namespace rs

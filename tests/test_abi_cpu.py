@@ -87,7 +87,7 @@ def test_empty_problems_are_a_noop():
 
 def test_exact_in_place_is_accepted_by_the_planner():
     rc, plan = rs.rowsoftmax_plan(A, A, 64, 1000, 1024, 1024, rs.RS_F32, None, gb300())
-    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_ROWS
+    assert rc == rs.RS_OK and plan["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING)
 
 
 def test_disjoint_interleaved_layout_is_rejected_as_overlap():
@@ -104,23 +104,44 @@ def _plan(M, N, dtype, ld=None, opts=None, a=A, b=A + (1 << 40)):
 
 def _covers(plan, N):
     units = -(-N // plan["vec_elems"])
-    if plan["path"] == rs.RS_PATH_ROWS:
+    if plan["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING):
         return plan["threads_per_row"] * plan["vec_per_thread"] >= units
     return plan["cluster_size"] * plan["chunk_elems"] >= N
 
 
 def test_plans_for_the_benchmark_workloads():
     p = _plan(1024, 1024, rs.RS_F32)
-    assert (p["path"], p["vec_elems"], p["threads_per_row"]) == (rs.RS_PATH_ROWS, 4, 32)
+    assert (p["path"], p["vec_elems"], p["threads_per_row"]) == (rs.RS_PATH_RING, 4, 32)
     p = _plan(8192, 5000, rs.RS_F32, ld=5120)
-    assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 4 and _covers(p, 5000)
+    assert p["path"] == rs.RS_PATH_RING and p["vec_elems"] == 4 and _covers(p, 5000)
     p = _plan(32768, 8192, rs.RS_BF16)
-    assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 8 and _covers(p, 8192)
+    assert p["path"] == rs.RS_PATH_RING and p["vec_elems"] == 8 and _covers(p, 8192)
     p = _plan(512, 131072, rs.RS_F16)
     assert p["path"] == rs.RS_PATH_CLUSTER and p["cluster_size"] >= 2 and _covers(p, 131072)
     assert p["smem_bytes"] <= 232448 - 1024 and p["grid"] == 512 * p["cluster_size"]
     p = _plan(1 << 20, 2048, rs.RS_BF16)
-    assert p["path"] == rs.RS_PATH_ROWS and _covers(p, 2048)
+    assert p["path"] == rs.RS_PATH_RING and _covers(p, 2048)
+
+
+def test_ring_plan_is_persistent_and_fits_shared_memory():
+    for M, N, dt in [(8192, 5000, rs.RS_F32), (32768, 8192, rs.RS_BF16), (1 << 20, 2048, rs.RS_BF16),
+                     (7, 300, rs.RS_F16)]:
+        p = _plan(M, N, dt, ld=-(-N // 8) * 8)
+        assert p["path"] == rs.RS_PATH_RING
+        assert 2 <= p["stages"] <= 8
+        es = 4 if dt == rs.RS_F32 else 2
+        stage = (N * es // 16) * 16 * p["rows_per_cta"]
+        assert p["smem_bytes"] == stage * p["stages"] <= 232448 - 1024
+        groups = -(-M // p["rows_per_cta"])
+        assert p["grid"] <= min(groups, 152 * 32)
+    p = _plan(8192, 5000, rs.RS_F32, ld=5120, opts={"path": rs.RS_PATH_RING, "stages": 3})
+    assert p["stages"] == 3
+    rc, _ = rs.rowsoftmax_plan(A, A + (1 << 40), 10, 1000, 1000, 1000, rs.RS_F32,
+                               {"path": rs.RS_PATH_RING, "stages": 9}, gb300())
+    assert rc == rs.RS_ERR_INVALID_ARG
+    rc, _ = rs.rowsoftmax_plan(A + 4, A + (1 << 40), 10, 1000, 1000, 1000, rs.RS_F32,
+                               {"path": rs.RS_PATH_RING}, gb300())
+    assert rc == rs.RS_ERR_NO_PATH
 
 
 def test_misaligned_data_gets_the_element_wise_kernels():
@@ -142,11 +163,15 @@ def test_auto_plan_always_covers_the_row(dtype, N, aligned):
     a = A if aligned else A + 2 * (1 if dtype else 2)
     p = _plan(3, N, dtype, a=a)
     assert _covers(p, N)
+    if N <= 4096:  # short rows stay single-pass, aligned or not
+        assert p["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING)
     if p["path"] == rs.RS_PATH_CLUSTER:
         assert p["vec_elems"] > 1 and p["stages"] <= 16 and p["smem_bytes"] % 16 == 0
         assert (p["chunk_elems"] * (4 if dtype == rs.RS_F32 else 2)) % 16 == 0
-    if p["path"] == rs.RS_PATH_ROWS:
+    if p["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING):
         assert p["block_threads"] % p["threads_per_row"] == 0 and p["block_threads"] <= 1024
+    if p["path"] == rs.RS_PATH_RING:
+        assert p["vec_elems"] > 1 and p["smem_bytes"] <= 232448 - 1024
 
 
 def test_forced_options():

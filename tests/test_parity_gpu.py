@@ -67,6 +67,16 @@ def _input(M, N, dtype, ld=None, kind="normal1", seed=0):
     return W.generate(w, "cuda")
 
 
+def _aligned(M, N, dtype, kind="normal1", seed=0):
+    """Input and output views whose rows start on 16-byte boundaries (row
+    stride rounded up), so the 16-byte vector and bulk-copy kernels apply."""
+    vec = 4 if dtype == "f32" else 8
+    ld = -(-N // vec) * vec
+    x = _input(M, N, dtype, ld=ld, kind=kind, seed=seed)[:, :N]
+    out = torch.empty((M, ld), dtype=DT[dtype], device="cuda")[:, :N]
+    return x, out
+
+
 ROWS_SHAPES = [(1, 1), (3, 2), (5, 3), (37, 7), (64, 8), (33, 33), (300, 100), (17, 255), (129, 781),
                (64, 1000), (1024, 1024), (40, 2048), (20, 4097), (30, 5000), (16, 8192), (9, 12345)]
 
@@ -89,8 +99,8 @@ def test_rows_path_thread_shapes(dtype, tpr, vpt):
         pytest.skip("instance compiled for 512 threads")
     N = max(1, tpr * vpt * vec - 3)  # a ragged last unit
     M = 37
-    x = _input(M, N, dtype, seed=tpr * 100 + vpt)
-    y = _run(x, options={"path": rs.RS_PATH_ROWS, "threads_per_row": tpr, "vec_per_thread": vpt})
+    x, out = _aligned(M, N, dtype, seed=tpr * 100 + vpt)
+    y = _run(x, out=out, options={"path": rs.RS_PATH_ROWS, "threads_per_row": tpr, "vec_per_thread": vpt})
     _check(x, y, what=f"rows tpr={tpr} vpt={vpt}")
 
 
@@ -106,11 +116,11 @@ def test_rows_path_element_wise(dtype, N):
 @pytest.mark.parametrize("cs", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("N", [8, 1000, 4104, 65536, 100003])
 def test_cluster_path(dtype, cs, N):
-    x = _input(11, N, dtype, kind="normal_spike", seed=cs * 7 + N)
+    x, out = _aligned(11, N, dtype, kind="normal_spike", seed=cs * 7 + N)
     opts = {"path": rs.RS_PATH_CLUSTER, "cluster_size": cs}
     if not _servable(x, opts):
         pytest.skip("slice larger than shared memory")
-    y = _run(x, options=opts)
+    y = _run(x, out=out, options=opts)
     _check(x, y, what=f"cluster cs={cs} N={N}")
 
 
@@ -119,12 +129,40 @@ def test_cluster_path(dtype, cs, N):
 @pytest.mark.parametrize("scalar", [0, 1])
 @pytest.mark.parametrize("N", [3, 1000, 70001])
 def test_stream_path(dtype, cs, scalar, N):
-    x = _input(9, N, dtype, kind="uniform20_offset", seed=cs + N)
-    y = _run(x, options={"path": rs.RS_PATH_STREAM, "cluster_size": cs, "force_scalar": scalar})
+    x, out = _aligned(9, N, dtype, kind="uniform20_offset", seed=cs + N)
+    y = _run(x, out=out, options={"path": rs.RS_PATH_STREAM, "cluster_size": cs, "force_scalar": scalar})
     _check(x, y, what=f"stream cs={cs} scalar={scalar} N={N}")
 
 
-@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_CLUSTER, rs.RS_PATH_STREAM])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [8, 100, 1001, 2048, 5000, 8192, 12345])
+@pytest.mark.parametrize("stages", [2, 3, 8])
+def test_ring_path(dtype, N, stages):
+    x, out = _aligned(300, N, dtype, kind="uniform20_offset", seed=N + stages)
+    opts = {"path": rs.RS_PATH_RING, "stages": stages}
+    if not _servable(x, opts):
+        pytest.skip("ring does not fit shared memory")
+    y = _run(x, out=out, options=opts)
+    _check(x, y, what=f"ring N={N} stages={stages}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("tpr,vpt", [(1, 1), (4, 2), (32, 8), (64, 4), (160, 8), (256, 4), (1024, 1)])
+@pytest.mark.parametrize("grid_limit", [0, 3])
+def test_ring_thread_shapes_and_wraparound(dtype, tpr, vpt, grid_limit):
+    vec = 4 if dtype == "f32" else 8
+    if vpt * vec > 32 and tpr > 512:
+        pytest.skip("instance compiled for 512 threads")
+    N = max(vec + 1, tpr * vpt * vec - 5)
+    x, out = _aligned(97, N, dtype, seed=tpr + vpt)
+    opts = {"path": rs.RS_PATH_RING, "threads_per_row": tpr, "vec_per_thread": vpt, "grid_limit": grid_limit}
+    if not _servable(x, opts):
+        pytest.skip("ring does not fit shared memory")
+    y = _run(x, out=out, options=opts)
+    _check(x, y, what=f"ring tpr={tpr} vpt={vpt} grid_limit={grid_limit}")
+
+
+@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_CLUSTER, rs.RS_PATH_STREAM])
 def test_grid_limit_makes_ctas_loop_over_rows(path):
     x = _input(1000, 512, "bf16", seed=5)
     y = _run(x, options={"path": path, "grid_limit": 16})
@@ -134,7 +172,7 @@ def test_grid_limit_makes_ctas_loop_over_rows(path):
 def test_paths_agree_on_the_same_input():
     x = _input(64, 6000, "f32", kind="normal2_const", seed=9)
     ref = oracle_rows(x, 6000)
-    for opts in [None, {"path": rs.RS_PATH_ROWS}, {"path": rs.RS_PATH_CLUSTER, "cluster_size": 4},
+    for opts in [None, {"path": rs.RS_PATH_ROWS}, {"path": rs.RS_PATH_RING}, {"path": rs.RS_PATH_CLUSTER, "cluster_size": 4},
                  {"path": rs.RS_PATH_STREAM, "cluster_size": 2}, {"path": rs.RS_PATH_ROWS, "force_scalar": 1}]:
         compare(_run(x, options=opts), ref, "f32", f"opts={opts}")
 
@@ -166,19 +204,23 @@ def test_misaligned_pointers_use_element_wise_access(dtype, shift):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("N", [100, 8192, 70000])
-def test_in_place(dtype, N):
-    x = _input(13, N, dtype, seed=N)
+@pytest.mark.parametrize("path", [rs.RS_PATH_AUTO, rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_STREAM])
+def test_in_place(dtype, N, path):
+    x = _input(300, N, dtype, seed=N)
+    opts = {"path": path, "grid_limit": 7}
+    if not _servable(x, opts):
+        pytest.skip("configuration does not serve this shape")
     ref = oracle_rows(x, N)
-    y = _run(x, out=x)
+    y = _run(x, out=x, options=opts)
     assert y.data_ptr() == x.data_ptr()
     compare(x, ref, dtype, "in-place")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_CLUSTER, rs.RS_PATH_STREAM])
+@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_CLUSTER, rs.RS_PATH_STREAM])
 def test_special_values(dtype, path):
     N = 300
-    x = _input(8, N, dtype, seed=1)
+    x, out = _aligned(8, N, dtype, seed=1)
     x[0] = -math.inf                  # all -inf: NaN row
     x[1, 17] = math.nan               # NaN: NaN row
     x[2, 200] = math.inf              # +inf: NaN row
@@ -187,7 +229,7 @@ def test_special_values(dtype, path):
     x[5, 150:] = -math.inf            # a -inf suffix
     x[6, ::2] = -math.inf
     x[7, 5] = 1e4 if dtype != "f16" else 6e4
-    y = _run(x, options={"path": path})
+    y = _run(x, out=out, options={"path": path})
     _check(x, y, what=f"special path={path}")
     yd = decode(y)
     assert yd[3, 0] == 1.0 and np.all(yd[3, 1:] == 0.0)
@@ -291,4 +333,4 @@ def test_benchmark_launch_configuration_is_the_auto_plan():
     x = W.generate(w, "cuda", 0, 4)
     rc, plan = rs.rowsoftmax_plan(x.data_ptr(), x.data_ptr() + (1 << 40), w.M, w.N, w.ld, w.ld, rs.RS_F32, None,
                                   dev)
-    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_ROWS
+    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_RING
