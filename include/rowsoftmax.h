@@ -86,6 +86,14 @@ typedef enum {
                              asynchronous copies (TMA engine); 16-byte aligned data only */
 } rs_path;
 
+/* Where RS_PATH_RING keeps a row between its passes. */
+typedef enum {
+    RS_RING_AUTO = 0,
+    RS_RING_REGISTERS = 1,  /* fp32 copies in registers: one exp per element */
+    RS_RING_REREAD = 2      /* re-read the staged row from shared memory in each pass: two exps per
+                               element, far fewer registers, more resident warps */
+} rs_ring_values;
+
 /*
  * Forcing options for tests and tuning.  Zero fields mean "choose".  A NULL
  * rs_options pointer is the same as all zeros, i.e. rowsoftmax_fwd.
@@ -97,6 +105,7 @@ typedef struct {
     int block_threads;    /* threads per CTA (RS_PATH_ROWS: multiple of threads_per_row) */
     int cluster_size;     /* RS_PATH_CLUSTER / RS_PATH_STREAM: CTAs per row, 1..16 */
     int stages;           /* RS_PATH_RING: shared-memory stages per CTA, 2..8 */
+    int ring_values;      /* RS_PATH_RING: rs_ring_values */
     int force_scalar;     /* 1: element-wise accesses even when 16-byte vectors would be legal */
     int64_t grid_limit;   /* >0: cap on CTAs (rows loop inside the kernel); 0: one launch slot per row group */
 } rs_options;
@@ -112,6 +121,7 @@ typedef struct {
     int block_threads;
     int cluster_size;     /* CTAs per row (1 for RS_PATH_ROWS / RS_PATH_RING) */
     int stages;           /* RS_PATH_CLUSTER: bulk-copy stages per CTA; RS_PATH_RING: ring depth */
+    int ring_values;      /* RS_PATH_RING: RS_RING_REGISTERS or RS_RING_REREAD */
     int64_t chunk_elems;  /* RS_PATH_CLUSTER / RS_PATH_STREAM: row slice per CTA */
     int64_t grid;         /* CTAs launched */
     size_t smem_bytes;    /* dynamic shared memory per CTA */

@@ -24,6 +24,9 @@ from ._abi import (  # noqa: F401
     RS_PATH_RING,
     RS_PATH_ROWS,
     RS_PATH_STREAM,
+    RS_RING_AUTO,
+    RS_RING_REGISTERS,
+    RS_RING_REREAD,
     rowsoftmax_device_info,
     rowsoftmax_device_status,
     rowsoftmax_fwd,

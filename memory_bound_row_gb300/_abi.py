@@ -25,6 +25,7 @@ RS_ERR_NOT_DEVICE_MEMORY = 5
 RS_ERR_NO_PATH = 6
 # rs_path
 RS_PATH_AUTO, RS_PATH_ROWS, RS_PATH_CLUSTER, RS_PATH_STREAM, RS_PATH_RING = 0, 1, 2, 3, 4
+RS_RING_AUTO, RS_RING_REGISTERS, RS_RING_REREAD = 0, 1, 2
 PATH_NAMES = {RS_PATH_AUTO: "auto", RS_PATH_ROWS: "rows", RS_PATH_CLUSTER: "cluster", RS_PATH_STREAM: "stream",
               RS_PATH_RING: "ring"}
 
@@ -48,6 +49,7 @@ class rs_options(ctypes.Structure):
         ("block_threads", ctypes.c_int),
         ("cluster_size", ctypes.c_int),
         ("stages", ctypes.c_int),
+        ("ring_values", ctypes.c_int),
         ("force_scalar", ctypes.c_int),
         ("grid_limit", ctypes.c_int64),
     ]
@@ -64,6 +66,7 @@ class rs_plan(ctypes.Structure):
         ("block_threads", ctypes.c_int),
         ("cluster_size", ctypes.c_int),
         ("stages", ctypes.c_int),
+        ("ring_values", ctypes.c_int),
         ("chunk_elems", ctypes.c_int64),
         ("grid", ctypes.c_int64),
         ("smem_bytes", ctypes.c_size_t),

@@ -75,7 +75,8 @@ int vpt_at_least(int dtype, int vec, int64_t want) {
     return 0;
 }
 
-int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o, rs_plan* p) {
+int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o, rs_plan* p,
+              bool registers_hold_row = true) {
     int tpr = o.threads_per_row;
     int vpt = o.vec_per_thread;
     if (tpr && !valid_tpr(tpr)) return RS_ERR_INVALID_ARG;
@@ -110,7 +111,7 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
     }
     if ((int64_t)tpr * vpt < units) return RS_ERR_NO_PATH;
     if (vpt * vec > rs::kRowsMaxValuesPerThread) return RS_ERR_NO_PATH;
-    const int block_limit = rs::rows_block_limit(vpt, vec);
+    const int block_limit = registers_hold_row ? rs::rows_block_limit(vpt, vec) : rs::kRingRereadThreads;
     if (tpr > block_limit) return RS_ERR_NO_PATH;
 
     int block = o.block_threads;
@@ -156,9 +157,12 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
               const rs_device_info& dev, rs_plan* p) {
     if (vec == 1) return RS_ERR_NO_PATH;  // bulk copies need 16-byte units
     if (o.stages && (o.stages < 2 || o.stages > rs::kRingMaxStages)) return RS_ERR_INVALID_ARG;
+    if (o.ring_values < RS_RING_AUTO || o.ring_values > RS_RING_REREAD) return RS_ERR_INVALID_ARG;
+    const int values = o.ring_values == RS_RING_AUTO ? (dtype == RS_F32 ? RS_RING_REGISTERS : RS_RING_REREAD)
+                                                     : o.ring_values;
     rs_options ro = o;
     ro.grid_limit = 0;
-    int rc = plan_rows(dtype, vec, M, units, ro, p);
+    int rc = plan_rows(dtype, vec, M, units, ro, p, values == RS_RING_REGISTERS);
     if (rc != RS_OK) return rc;
     const int64_t slot = (N / vec) * 16;
     const int64_t stage = slot * p->rows_per_cta;
@@ -173,20 +177,84 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     }
     const int64_t smem = stage * stages;
     if (smem > max_dyn || stage >= (1 << 20)) return RS_ERR_NO_PATH;  // mbarrier tx count < 2^20
-    const int regs = rs::rows_block_limit(p->vec_per_thread, vec) == 1024 ? 64 : 128;
+    const int regs = values == RS_RING_REREAD ? rs::kRingRereadRegs
+                     : (rs::rows_block_limit(p->vec_per_thread, vec) == 1024 ? 64 : 128);
     const int64_t groups = ceil_div(M, p->rows_per_cta);
     int64_t grid = (int64_t)dev.sm_count * ctas_per_sm(dev, p->block_threads, (size_t)smem, regs);
     if (grid > groups) grid = groups;
     if (o.grid_limit > 0 && grid > o.grid_limit) grid = o.grid_limit;
     p->path = RS_PATH_RING;
+    p->ring_values = values;
     p->stages = stages;
     p->smem_bytes = (size_t)smem;
     p->grid = grid;
     return RS_OK;
 }
 
+// RS_PATH_CLUSTER with the slice in registers: a persistent grid of clusters,
+// each CTA holding VPT (1, 2 or 4) 16-byte units a thread of its slice.
+int plan_cluster_hold(int dtype, int vec, int64_t M, int64_t N, const rs_options& o, const rs_device_info& dev,
+                      rs_plan* p) {
+    const int es = elem_size(dtype);
+    const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kWideStaticSmem;
+    if (o.stages && (o.stages < 1 || o.stages > 2)) return RS_ERR_INVALID_ARG;
+    int cs = o.cluster_size;
+    int block = 0, vpt = 0;
+    int64_t chunk = 0;
+    for (int c = cs ? cs : 1; c <= (cs ? cs : rs::kMaxCluster); c <<= 1) {
+        chunk = round_up(ceil_div(N, c), vec);
+        const int64_t units = chunk / vec;
+        for (int b : {rs::kWideHoldThreads, 256}) {
+            if (o.block_threads && b != o.block_threads) continue;
+            for (int v : {1, 2, 4}) {
+                if (o.vec_per_thread && v != o.vec_per_thread) continue;
+                if ((int64_t)b * v >= units) {
+                    block = b;
+                    vpt = v;
+                    break;
+                }
+            }
+            if (vpt) break;
+        }
+        if (vpt) {
+            cs = c;
+            break;
+        }
+        if (cs) break;
+    }
+    if (!vpt) return RS_ERR_NO_PATH;
+    const size_t slot = (size_t)round_up(chunk * es, 16);
+    const int64_t resident_ctas = (int64_t)dev.sm_count * ctas_per_sm(dev, block, 2 * slot, 64);
+    int64_t clusters = resident_ctas / cs;
+    if (clusters < 1) clusters = 1;
+    if (clusters > M) clusters = M;
+    if (o.grid_limit > 0 && clusters * cs > o.grid_limit) clusters = o.grid_limit / cs > 0 ? o.grid_limit / cs : 1;
+    if (clusters * cs > kMaxGrid) clusters = kMaxGrid / cs;
+    const int slots = o.stages ? o.stages : (clusters < M ? 2 : 1);
+    if ((int64_t)(slots * slot) > max_dyn) return RS_ERR_NO_PATH;
+    p->path = RS_PATH_CLUSTER;
+    p->ring_values = RS_RING_REGISTERS;
+    p->vec_elems = vec;
+    p->threads_per_row = block;
+    p->vec_per_thread = vpt;
+    p->rows_per_cta = 1;
+    p->block_threads = block;
+    p->cluster_size = cs;
+    p->stages = slots;
+    p->chunk_elems = chunk;
+    p->grid = clusters * cs;
+    p->smem_bytes = slots * slot;
+    return RS_OK;
+}
+
 int plan_wide(int dtype, int path, int vec, int64_t M, int64_t N, const rs_options& o,
               const rs_device_info& dev, rs_plan* p) {
+    if (path == RS_PATH_CLUSTER && vec > 1 &&
+        (o.ring_values == RS_RING_REGISTERS || o.ring_values == RS_RING_AUTO)) {
+        const int rc = plan_cluster_hold(dtype, vec, M, N, o, dev, p);
+        if (rc == RS_OK || o.ring_values == RS_RING_REGISTERS) return rc;
+    }
+    if (o.ring_values < RS_RING_AUTO || o.ring_values > RS_RING_REREAD) return RS_ERR_INVALID_ARG;
     const int es = elem_size(dtype);
     const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kWideStaticSmem;
     int cs = o.cluster_size;
@@ -213,17 +281,21 @@ int plan_wide(int dtype, int path, int vec, int64_t M, int64_t N, const rs_optio
     if (chunk > kMaxN) return RS_ERR_NO_PATH;
     int stages = 0;
     size_t smem = 0;
+    int64_t clusters = M;
+    if (o.grid_limit > 0 && clusters * cs > o.grid_limit) clusters = o.grid_limit / cs > 0 ? o.grid_limit / cs : 1;
+    if (clusters * cs > kMaxGrid) clusters = kMaxGrid / cs;
     if (path == RS_PATH_CLUSTER) {
-        smem = (size_t)round_up(chunk * es, 16);
+        // One slot per CTA when every cluster serves one row; two (the next
+        // row's slice in flight) when clusters loop over rows.
+        const int slots = clusters < M ? 2 : 1;
+        smem = slots * (size_t)round_up(chunk * es, 16);
         if ((int64_t)smem > max_dyn) return RS_ERR_NO_PATH;
         stages = (int)ceil_div(ceil_div(chunk, vec), rs::kWideUnitsPerStage);
         if (stages > rs::kWideMaxStages) return RS_ERR_NO_PATH;
     }
-    int64_t clusters = M;
-    if (o.grid_limit > 0 && clusters * cs > o.grid_limit) clusters = o.grid_limit / cs > 0 ? o.grid_limit / cs : 1;
-    if (clusters * cs > kMaxGrid) clusters = kMaxGrid / cs;
 
     p->path = path;
+    p->ring_values = path == RS_PATH_CLUSTER ? RS_RING_REREAD : RS_RING_AUTO;
     p->vec_elems = vec;
     p->threads_per_row = 0;
     p->vec_per_thread = 0;
@@ -334,6 +406,41 @@ int current_device(int* dev, rs_device_info* info) {
     return RS_OK;
 }
 
+// cudaOccupancyMaxActiveClusters for a planned cluster launch, cached by
+// device and launch shape (the query costs far more than a launch).
+struct ClusterKey {
+    int dev, dtype, path, values, vec, vpt, block, cs;
+    size_t smem;
+    bool operator==(const ClusterKey& o) const {
+        return dev == o.dev && dtype == o.dtype && path == o.path && values == o.values && vec == o.vec &&
+               vpt == o.vpt && block == o.block && cs == o.cs && smem == o.smem;
+    }
+};
+std::mutex g_cluster_mu;
+ClusterKey g_cluster_keys[64];
+int g_cluster_vals[64];
+int g_cluster_n = 0;
+
+cudaError_t max_active_clusters_cached(int dev, const rs_plan& p, int* n) {
+    const ClusterKey k{dev, p.dtype, p.path, p.ring_values, p.vec_elems, p.vec_per_thread, p.block_threads,
+                       p.cluster_size, p.smem_bytes};
+    {
+        std::lock_guard<std::mutex> lock(g_cluster_mu);
+        for (int i = 0; i < g_cluster_n; ++i)
+            if (g_cluster_keys[i] == k) {
+                *n = g_cluster_vals[i];
+                return cudaSuccess;
+            }
+    }
+    cudaError_t e = rs::wide_max_active_clusters(p, n);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_cluster_mu);
+    const int slot = g_cluster_n < 64 ? g_cluster_n++ : (int)(k.smem % 64);
+    g_cluster_keys[slot] = k;
+    g_cluster_vals[slot] = *n;
+    return cudaSuccess;
+}
+
 // The kernels dereference `p` directly: it must be memory the current
 // device can address at that same address.
 int check_device_pointer(const void* p, int dev) {
@@ -389,15 +496,19 @@ int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t i
     rc = validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, opts, &info, &plan);
     if (rc != RS_OK) return rc;
 
+    const bool persistent_cluster = plan.path == RS_PATH_CLUSTER && plan.ring_values == RS_RING_REGISTERS;
     if ((plan.path == RS_PATH_CLUSTER || plan.path == RS_PATH_STREAM) &&
-        plan.cluster_size > rs::kMaxClusterPortable) {
+        (plan.cluster_size > rs::kMaxClusterPortable || persistent_cluster)) {
         int n = 0;
-        cudaError_t e = rs::wide_max_active_clusters(plan, &n);
+        cudaError_t e = max_active_clusters_cached(dev, plan, &n);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             return fail_cuda(e);
         }
         if (n < 1) return RS_ERR_NO_PATH;
+        // A persistent grid larger than what is co-resident would leave its
+        // last clusters to run after the others, each with many rows.
+        if (persistent_cluster && plan.grid / plan.cluster_size > n) plan.grid = (int64_t)n * plan.cluster_size;
     }
 
     cudaError_t e = cudaSuccess;

@@ -135,10 +135,29 @@ __device__ __forceinline__ void store_unit(typename Traits<DT>::storage* row, in
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float safe_max(float m) { return m == kNegInf ? 0.0f : m; }
 
+// log2(e): exp(d) = 2^(d * log2(e)).
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^y with the hardware base-2 exponential (PTX ex2.approx.ftz.f32: relative
+// error about 2^-22; results below the smallest normal flush to zero, which
+// is below every tolerance of this library).  2^(-inf) = 0, 2^NaN = NaN.
+__device__ __forceinline__ float ex2_approx(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
+// exp(x - ms): the difference is formed first (exact when x is near ms),
+// then scaled into base 2.
+__device__ __forceinline__ float exp_diff(float x, float ms) { return ex2_approx((x - ms) * kLog2e); }
+
 // Weight of a partial sum taken against max m when the merged max is ms.
 __device__ __forceinline__ float rescale(float m, float ms) {
-    return m == kNegInf ? 0.0f : __expf(m - ms);
+    return m == kNegInf ? 0.0f : exp_diff(m, ms);
 }
+
+// Smallest power of two >= n (n in 1..32).
+__device__ __forceinline__ int pow2_ceil(int n) { return n <= 1 ? 1 : 1 << (32 - __clz(n - 1)); }
 
 // Reductions over aligned groups of `width` lanes (width a power of two, <= 32).
 __device__ __forceinline__ float group_max(float v, int width) {

@@ -30,6 +30,13 @@ constexpr int kRowsMaxThreads = 1024;
 // instances are compiled for 512 threads (128 registers) so they do not spill.
 constexpr int rows_block_limit(int vpt, int vec) { return (vpt <= 8 && vpt * vec <= 32) ? 1024 : 512; }
 
+// RS_PATH_RING instances that re-read shared memory are compiled for at most
+// kRingRereadThreads threads and kRingRereadMinCtas resident CTAs of that size,
+// which caps them at 40 registers a thread.
+constexpr int kRingRereadThreads = 512;
+constexpr int kRingRereadMinCtas = 3;
+constexpr int kRingRereadRegs = 40;
+
 // Persistent ring kernel (RS_PATH_RING).
 constexpr int kRingMaxStages = 8;
 constexpr size_t kRingStaticSmem = 1024;  // upper bound of the kernel's static shared memory
@@ -42,6 +49,8 @@ constexpr int kWideMaxStages = 16;     // mbarriers per CTA
 constexpr int kMaxClusterPortable = 8;
 constexpr int kMaxCluster = 16;        // needs the non-portable cluster-size opt-in
 constexpr size_t kWideStaticSmem = 1024;  // upper bound of the kernel's static shared memory
+constexpr int kWideHoldThreads = 512;     // max threads per CTA of the register-holding cluster kernel
+constexpr int kWideHoldMaxVpt = 4;        // units per thread it is instantiated for: 1, 2, 4
 
 // Launchers.  Each returns the CUDA error of the launch (cudaSuccess if it
 // was enqueued).  Arguments were validated and planned by the caller.

@@ -28,11 +28,31 @@
 #include "rs_async.cuh"
 #include "rs_common.cuh"
 #include "rs_internal.h"
+#include "rs_rowmath.cuh"
 
 namespace rs {
 
-template <int DT, int VPT>
-__global__ void __launch_bounds__(rows_block_limit(VPT, Traits<DT>::kVec))
+// HOLD = true keeps the thread's units in registers as fp32 (one exp per
+// element).  HOLD = false keeps only the staged copy in shared memory and
+// reads it once per pass (max, sum of exps, normalise-and-store), taking the
+// exp twice per element: fewer registers, so more CTAs and warps per SM.
+template <int DT, int VPT, bool HOLD>
+__device__ __forceinline__ void ring_unit(const unsigned char* srow, const typename Traits<DT>::storage* grow,
+                                          int u, int units_full, int N, bool active, float* f) {
+    constexpr int VEC = Traits<DT>::kVec;
+    if (active && u < units_full) {
+        Traits<DT>::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)u * 16), f);
+    } else if (active && u * VEC < N) {
+        load_unit<DT, VEC>(grow, u * VEC, N, f);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = kNegInf;
+    }
+}
+
+template <int DT, int VPT, bool HOLD>
+__global__ void __launch_bounds__(HOLD ? rows_block_limit(VPT, Traits<DT>::kVec) : kRingRereadThreads,
+                                  HOLD ? 1 : kRingRereadMinCtas)
 ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, int stages) {
     using T = Traits<DT>;
     using S = typename T::storage;
@@ -94,66 +114,74 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         const int64_t row = g * rpg + grp;
         const bool active = row < M;
         const unsigned char* srow = ring + (size_t)s * stage_bytes + (size_t)grp * slot;
+        const S* grow = in + (active ? row : 0) * ldi;
 
-        float v[VPT][VEC];
+        if (HOLD) {
+            float v[VPT][VEC];
+            if (active && (t + (VPT - 1) * tpr) < units_full) {
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int u = t + k * tpr;
-            if (active && u < units_full) {
-                T::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)u * 16), v[k]);
-            } else if (active && u * VEC < N) {
-                load_unit<DT, VEC>(in + row * ldi, u * VEC, N, v[k]);
+                for (int k = 0; k < VPT; ++k)
+                    T::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)(t + k * tpr) * 16), v[k]);
             } else {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] = kNegInf;
+                for (int k = 0; k < VPT; ++k)
+                    ring_unit<DT, VPT, HOLD>(srow, grow, t + k * tpr, units_full, N, active, v[k]);
             }
-        }
-
-        float m = kNegInf;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
-        m = group_max(m, width);
-        const float ms = safe_max(m);
-
-        float l = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                v[k][e] = __expf(v[k][e] - ms);
-                l += v[k][e];
-            }
-        l = group_sum(l, width);
-
-        float c;
-        if (tpr <= 32) {
-            c = 1.0f / l;
+            const float c = row_exp_and_scale<VPT, VEC>(v, tpr, part[it & 1]);
+            if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v, c);
         } else {
-            float2* p = part[it & 1];
-            if (lane == 0) p[warp] = make_float2(m, l);
-            __syncthreads();
-            const int w0 = (warp / wpr) * wpr;
-            float pm = kNegInf, pl = 0.0f;
-            if (lane < wpr) {
-                const float2 q = p[w0 + lane];
-                pm = q.x;
-                pl = q.y;
-            }
-            const float mrow = group_max(pm, 32);
-            const float mrs = safe_max(mrow);
-            const float srow_sum = group_sum(pl * rescale(pm, mrs), 32);
-            c = rescale(m, mrs) / srow_sum;
-        }
-
-        if (active) {
-            S* yr = out + row * ldo;
-#pragma unroll
+            float f[VEC];
+            float m = kNegInf;
+#pragma unroll 1
             for (int k = 0; k < VPT; ++k) {
+                ring_unit<DT, VPT, HOLD>(srow, grow, t + k * tpr, units_full, N, active, f);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] *= c;
-                store_unit<DT, VEC>(yr, (t + k * tpr) * VEC, N, v[k]);
+                for (int e = 0; e < VEC; ++e) m = fmaxf(m, f[e]);
+            }
+            m = group_max(m, width);
+            const float ms = safe_max(m);
+
+            float l = 0.0f;
+            asm volatile("" ::: "memory");  // re-read the stage, do not keep it in registers
+#pragma unroll 1
+            for (int k = 0; k < VPT; ++k) {
+                ring_unit<DT, VPT, HOLD>(srow, grow, t + k * tpr, units_full, N, active, f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) l += exp_diff(f[e], ms);
+            }
+            l = group_sum(l, width);
+
+            float c;
+            if (tpr <= 32) {
+                c = 1.0f / l;
+            } else {
+                float2* p = part[it & 1];
+                if (lane == 0) p[warp] = make_float2(m, l);
+                __syncthreads();
+                const int w0 = (warp / wpr) * wpr;
+                const int ww = pow2_ceil(wpr);
+                float pm = kNegInf, pl = 0.0f;
+                if (lane < wpr) {
+                    const float2 q = p[w0 + lane];
+                    pm = q.x;
+                    pl = q.y;
+                }
+                const float mrow = __shfl_sync(0xffffffffu, group_max(pm, ww), 0);
+                const float mrs = safe_max(mrow);
+                const float srow_sum = __shfl_sync(0xffffffffu, group_sum(pl * rescale(pm, mrs), ww), 0);
+                c = rescale(m, mrs) / srow_sum;
+            }
+
+            if (active) {
+                S* yr = out + row * ldo;
+                asm volatile("" ::: "memory");
+#pragma unroll 1
+                for (int k = 0; k < VPT; ++k) {
+                    ring_unit<DT, VPT, HOLD>(srow, grow, t + k * tpr, units_full, N, active, f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) f[e] = exp_diff(f[e], ms) * c;
+                    store_unit<DT, VEC>(yr, (t + k * tpr) * VEC, N, f);
+                }
             }
         }
 
@@ -188,10 +216,10 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
     }
 }
 
-template <int DT, int VPT>
+template <int DT, int VPT, bool HOLD>
 cudaError_t launch_ring_one(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                             int64_t ldo, cudaStream_t s) {
-    auto kern = ring_kernel<DT, VPT>;
+    auto kern = ring_kernel<DT, VPT, HOLD>;
     // The dynamic shared-memory ceiling is a per-device attribute: raise it to
     // the device maximum once per device for this instance.
     static std::mutex mu;
@@ -231,7 +259,10 @@ template <int DT, int V0, int... Vs>
 struct RingDispatch<DT, V0, Vs...> {
     static cudaError_t go(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                           int64_t ldo, cudaStream_t s) {
-        if (p.vec_per_thread == V0) return launch_ring_one<DT, V0>(p, in, out, M, N, ldi, ldo, s);
+        if (p.vec_per_thread == V0) {
+            if (p.ring_values == RS_RING_REREAD) return launch_ring_one<DT, V0, false>(p, in, out, M, N, ldi, ldo, s);
+            return launch_ring_one<DT, V0, true>(p, in, out, M, N, ldi, ldo, s);
+        }
         return RingDispatch<DT, Vs...>::go(p, in, out, M, N, ldi, ldo, s);
     }
 };

@@ -19,14 +19,14 @@
 
 #include "rs_common.cuh"
 #include "rs_internal.h"
+#include "rs_rowmath.cuh"
 
 namespace rs {
 
 template <int DT, int VEC, int VPT>
 __global__ void __launch_bounds__(rows_block_limit(VPT, VEC))
 rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr) {
-    using T = Traits<DT>;
-    using S = typename T::storage;
+    using S = typename Traits<DT>::storage;
     const S* in = static_cast<const S*>(in_);
     S* out = static_cast<S*>(out_);
     __shared__ float2 part[2][32];  // per-warp (m, l), double-buffered over row iterations
@@ -34,75 +34,15 @@ rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
     const int rows_per_cta = blockDim.x / tpr;
     const int grp = threadIdx.x / tpr;
     const int t = threadIdx.x - grp * tpr;
-    const int width = tpr < 32 ? tpr : 32;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int wpr = tpr >> 5;  // warps per row (0 when a row is narrower than a warp)
 
     int it = 0;
     for (int64_t rb = blockIdx.x; rb * rows_per_cta < M; rb += gridDim.x, ++it) {
         const int64_t row = rb * rows_per_cta + grp;
         const bool active = row < M;
-
         float v[VPT][VEC];
-        if (active) {
-            const S* xr = in + row * ldi;
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) load_unit<DT, VEC>(xr, (t + k * tpr) * VEC, N, v[k]);
-        } else {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] = kNegInf;
-        }
-
-        float m = kNegInf;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
-        m = group_max(m, width);
-        const float ms = safe_max(m);
-
-        float l = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                v[k][e] = __expf(v[k][e] - ms);
-                l += v[k][e];
-            }
-        l = group_sum(l, width);
-
-        float c;  // y = exp(x - m_w) * c
-        if (tpr <= 32) {
-            c = 1.0f / l;
-        } else {
-            float2* p = part[it & 1];
-            if (lane == 0) p[warp] = make_float2(m, l);
-            __syncthreads();
-            const int w0 = (warp / wpr) * wpr;
-            float pm = kNegInf, pl = 0.0f;
-            if (lane < wpr) {
-                const float2 q = p[w0 + lane];
-                pm = q.x;
-                pl = q.y;
-            }
-            const float mrow = group_max(pm, 32);
-            const float mrs = safe_max(mrow);
-            const float srow = group_sum(pl * rescale(pm, mrs), 32);
-            c = rescale(m, mrs) / srow;
-        }
-
-        if (active) {
-            S* yr = out + row * ldo;
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] *= c;
-                store_unit<DT, VEC>(yr, (t + k * tpr) * VEC, N, v[k]);
-            }
-        }
+        load_row_units<DT, VEC, VPT>(in + (active ? row : 0) * ldi, t, tpr, N, active, v);
+        const float c = row_exp_and_scale<VPT, VEC>(v, tpr, part[it & 1]);
+        if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v, c);
     }
 }
 

@@ -118,7 +118,8 @@ def test_plans_for_the_benchmark_workloads():
     assert p["path"] == rs.RS_PATH_RING and p["vec_elems"] == 8 and _covers(p, 8192)
     p = _plan(512, 131072, rs.RS_F16)
     assert p["path"] == rs.RS_PATH_CLUSTER and p["cluster_size"] >= 2 and _covers(p, 131072)
-    assert p["smem_bytes"] <= 232448 - 1024 and p["grid"] == 512 * p["cluster_size"]
+    assert p["smem_bytes"] <= 232448 - 1024 and p["grid"] % p["cluster_size"] == 0
+    assert p["grid"] <= 512 * p["cluster_size"]  # persistent clusters loop over rows
     p = _plan(1 << 20, 2048, rs.RS_BF16)
     assert p["path"] == rs.RS_PATH_RING and _covers(p, 2048)
 

@@ -115,9 +115,11 @@ def test_rows_path_element_wise(dtype, N):
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("cs", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("N", [8, 1000, 4104, 65536, 100003])
-def test_cluster_path(dtype, cs, N):
+@pytest.mark.parametrize("values", [rs.RS_RING_REGISTERS, rs.RS_RING_REREAD])
+@pytest.mark.parametrize("grid_limit", [0, 2])
+def test_cluster_path(dtype, cs, N, values, grid_limit):
     x, out = _aligned(11, N, dtype, kind="normal_spike", seed=cs * 7 + N)
-    opts = {"path": rs.RS_PATH_CLUSTER, "cluster_size": cs}
+    opts = {"path": rs.RS_PATH_CLUSTER, "cluster_size": cs, "grid_limit": grid_limit * cs, "ring_values": values}
     if not _servable(x, opts):
         pytest.skip("slice larger than shared memory")
     y = _run(x, out=out, options=opts)
@@ -137,9 +139,10 @@ def test_stream_path(dtype, cs, scalar, N):
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("N", [8, 100, 1001, 2048, 5000, 8192, 12345])
 @pytest.mark.parametrize("stages", [2, 3, 8])
-def test_ring_path(dtype, N, stages):
+@pytest.mark.parametrize("values", [rs.RS_RING_REGISTERS, rs.RS_RING_REREAD])
+def test_ring_path(dtype, N, stages, values):
     x, out = _aligned(300, N, dtype, kind="uniform20_offset", seed=N + stages)
-    opts = {"path": rs.RS_PATH_RING, "stages": stages}
+    opts = {"path": rs.RS_PATH_RING, "stages": stages, "ring_values": values}
     if not _servable(x, opts):
         pytest.skip("ring does not fit shared memory")
     y = _run(x, out=out, options=opts)
@@ -147,15 +150,15 @@ def test_ring_path(dtype, N, stages):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("tpr,vpt", [(1, 1), (4, 2), (32, 8), (64, 4), (160, 8), (256, 4), (1024, 1)])
+@pytest.mark.parametrize("tpr,vpt", [(1, 1), (4, 2), (32, 8), (64, 4), (160, 8), (256, 4), (512, 2), (1024, 1)])
 @pytest.mark.parametrize("grid_limit", [0, 3])
-def test_ring_thread_shapes_and_wraparound(dtype, tpr, vpt, grid_limit):
+@pytest.mark.parametrize("values", [rs.RS_RING_REGISTERS, rs.RS_RING_REREAD])
+def test_ring_thread_shapes_and_wraparound(dtype, tpr, vpt, grid_limit, values):
     vec = 4 if dtype == "f32" else 8
-    if vpt * vec > 32 and tpr > 512:
-        pytest.skip("instance compiled for 512 threads")
     N = max(vec + 1, tpr * vpt * vec - 5)
     x, out = _aligned(97, N, dtype, seed=tpr + vpt)
-    opts = {"path": rs.RS_PATH_RING, "threads_per_row": tpr, "vec_per_thread": vpt, "grid_limit": grid_limit}
+    opts = {"path": rs.RS_PATH_RING, "threads_per_row": tpr, "vec_per_thread": vpt, "grid_limit": grid_limit,
+            "ring_values": values}
     if not _servable(x, opts):
         pytest.skip("ring does not fit shared memory")
     y = _run(x, out=out, options=opts)
@@ -172,7 +175,9 @@ def test_grid_limit_makes_ctas_loop_over_rows(path):
 def test_paths_agree_on_the_same_input():
     x = _input(64, 6000, "f32", kind="normal2_const", seed=9)
     ref = oracle_rows(x, 6000)
-    for opts in [None, {"path": rs.RS_PATH_ROWS}, {"path": rs.RS_PATH_RING}, {"path": rs.RS_PATH_CLUSTER, "cluster_size": 4},
+    for opts in [None, {"path": rs.RS_PATH_ROWS}, {"path": rs.RS_PATH_RING, "ring_values": rs.RS_RING_REGISTERS},
+                 {"path": rs.RS_PATH_RING, "ring_values": rs.RS_RING_REREAD}, {"path": rs.RS_PATH_CLUSTER, "cluster_size": 4},
+                 {"path": rs.RS_PATH_CLUSTER, "cluster_size": 2, "ring_values": rs.RS_RING_REREAD},
                  {"path": rs.RS_PATH_STREAM, "cluster_size": 2}, {"path": rs.RS_PATH_ROWS, "force_scalar": 1}]:
         compare(_run(x, options=opts), ref, "f32", f"opts={opts}")
 
