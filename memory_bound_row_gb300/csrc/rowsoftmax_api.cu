@@ -34,7 +34,7 @@ constexpr int kRowsTargetValues = 32;             // fp32 values a thread holds 
 constexpr int64_t kRowsMaxRowBytes = 32 * 1024;   // auto: rows up to this go to RS_PATH_ROWS
 constexpr int64_t kClusterTargetSlice = 64 * 1024;  // auto: bytes of row slice per CTA
 constexpr int64_t kRingMinRowBytes = 512;           // auto: shorter rows stay on RS_PATH_ROWS
-constexpr int64_t kRingTargetSmem = 64 * 1024;      // auto: ring bytes per CTA (stages x stage)
+constexpr int kRingDefaultStages = 2;               // auto: more stages cost resident CTAs (measured)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -158,8 +158,7 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     if (vec == 1) return RS_ERR_NO_PATH;  // bulk copies need 16-byte units
     if (o.stages && (o.stages < 2 || o.stages > rs::kRingMaxStages)) return RS_ERR_INVALID_ARG;
     if (o.ring_values < RS_RING_AUTO || o.ring_values > RS_RING_REREAD) return RS_ERR_INVALID_ARG;
-    const int values = o.ring_values == RS_RING_AUTO ? (dtype == RS_F32 ? RS_RING_REGISTERS : RS_RING_REREAD)
-                                                     : o.ring_values;
+    const int values = o.ring_values == RS_RING_AUTO ? RS_RING_REGISTERS : o.ring_values;
     rs_options ro = o;
     ro.grid_limit = 0;
     int rc = plan_rows(dtype, vec, M, units, ro, p, values == RS_RING_REGISTERS);
@@ -168,13 +167,7 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     const int64_t stage = slot * p->rows_per_cta;
     if (stage <= 0) return RS_ERR_NO_PATH;
     const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kRingStaticSmem;
-    int stages = o.stages;
-    if (!stages) {
-        int64_t s = kRingTargetSmem / stage;
-        if (s < 2) s = 2;
-        if (s > rs::kRingMaxStages) s = rs::kRingMaxStages;
-        stages = (int)s;
-    }
+    const int stages = o.stages ? o.stages : kRingDefaultStages;
     const int64_t smem = stage * stages;
     if (smem > max_dyn || stage >= (1 << 20)) return RS_ERR_NO_PATH;  // mbarrier tx count < 2^20
     const int regs = values == RS_RING_REREAD ? rs::kRingRereadRegs
@@ -201,20 +194,23 @@ int plan_cluster_hold(int dtype, int vec, int64_t M, int64_t N, const rs_options
     int cs = o.cluster_size;
     int block = 0, vpt = 0;
     int64_t chunk = 0;
+    // Candidate (threads, units a thread) shapes, most values a thread first;
+    // 8 units a thread are compiled for 256-thread CTAs only.
+    static const int kShapes[][2] = {{256, 8}, {512, 4}, {256, 4}, {512, 2}, {256, 2}, {512, 1}, {256, 1}};
     for (int c = cs ? cs : 1; c <= (cs ? cs : rs::kMaxCluster); c <<= 1) {
         chunk = round_up(ceil_div(N, c), vec);
         const int64_t units = chunk / vec;
-        for (int b : {rs::kWideHoldThreads, 256}) {
-            if (o.block_threads && b != o.block_threads) continue;
-            for (int v : {1, 2, 4}) {
-                if (o.vec_per_thread && v != o.vec_per_thread) continue;
-                if ((int64_t)b * v >= units) {
-                    block = b;
-                    vpt = v;
-                    break;
-                }
+        int64_t best_cap = 0;
+        for (const auto& sh : kShapes) {
+            if (o.block_threads && sh[0] != o.block_threads) continue;
+            if (o.vec_per_thread && sh[1] != o.vec_per_thread) continue;
+            const int64_t cap = (int64_t)sh[0] * sh[1];
+            if (cap < units) continue;
+            if (!vpt || cap < best_cap) {  // the tightest fit; ties keep the earlier (more values a thread)
+                block = sh[0];
+                vpt = sh[1];
+                best_cap = cap;
             }
-            if (vpt) break;
         }
         if (vpt) {
             cs = c;
@@ -224,7 +220,7 @@ int plan_cluster_hold(int dtype, int vec, int64_t M, int64_t N, const rs_options
     }
     if (!vpt) return RS_ERR_NO_PATH;
     const size_t slot = (size_t)round_up(chunk * es, 16);
-    const int64_t resident_ctas = (int64_t)dev.sm_count * ctas_per_sm(dev, block, 2 * slot, 64);
+    const int64_t resident_ctas = (int64_t)dev.sm_count * ctas_per_sm(dev, block, 2 * slot, vpt == 8 ? 128 : 64);
     int64_t clusters = resident_ctas / cs;
     if (clusters < 1) clusters = 1;
     if (clusters > M) clusters = M;
@@ -348,7 +344,10 @@ int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int
     int path = o.path;
     if (path == RS_PATH_AUTO) {
         int rc = RS_ERR_NO_PATH;
-        if (vec_ok && N * es >= kRingMinRowBytes && N * es <= kRowsMaxRowBytes)
+        // 16-bit rows: the ring (bytes in flight in shared memory, not in
+        // registers); fp32 rows: the register kernel, whose fp32 values cost
+        // no more registers than the bytes they came from.
+        if (dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes && N * es <= kRowsMaxRowBytes)
             rc = plan_ring(dtype, vec, M, N, units, o, *dev, p);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;

@@ -170,17 +170,13 @@ __device__ __forceinline__ float group_sum(float v, int width) {
     return v;
 }
 
-// Online-normaliser merge of (m, l) pairs over aligned groups of `width` lanes:
-// m = max(m1, m2), l = l1 * exp(m1 - m) + l2 * exp(m2 - m).
+// Online-normaliser merge of the (m, l) pairs of aligned groups of `width`
+// lanes: m = max_i m_i, l = sum_i l_i * exp(m_i - m).  The max is reduced
+// first, so each lane takes one exp rather than two per butterfly step.
 __device__ __forceinline__ void group_merge(float& m, float& l, int width) {
-    for (int o = width >> 1; o > 0; o >>= 1) {
-        float mo = __shfl_xor_sync(0xffffffffu, m, o);
-        float lo = __shfl_xor_sync(0xffffffffu, l, o);
-        float mn = fmaxf(m, mo);
-        float ms = safe_max(mn);
-        l = l * rescale(m, ms) + lo * rescale(mo, ms);
-        m = mn;
-    }
+    const float mm = group_max(m, width);
+    l = group_sum(l * rescale(m, safe_max(mm)), width);
+    m = mm;
 }
 
 }  // namespace rs

@@ -50,7 +50,7 @@ constexpr int kMaxClusterPortable = 8;
 constexpr int kMaxCluster = 16;        // needs the non-portable cluster-size opt-in
 constexpr size_t kWideStaticSmem = 1024;  // upper bound of the kernel's static shared memory
 constexpr int kWideHoldThreads = 512;     // max threads per CTA of the register-holding cluster kernel
-constexpr int kWideHoldMaxVpt = 4;        // units per thread it is instantiated for: 1, 2, 4
+constexpr int kWideHoldMaxVpt = 8;        // units per thread it is instantiated for: 1, 2, 4, 8 (8: 256 threads)
 
 // Launchers.  Each returns the CUDA error of the launch (cudaSuccess if it
 // was enqueued).  Arguments were validated and planned by the caller.

@@ -240,7 +240,7 @@ wide_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
 // Merges: warps -> CTA through shared memory, CTAs -> cluster through
 // distributed shared memory, all with the (m, l) operator.
 template <int DT, int VPT>
-__global__ void __launch_bounds__(kWideHoldThreads, 2)
+__global__ void __launch_bounds__(VPT <= 4 ? kWideHoldThreads : kWideHoldThreads / 2, 2)
 wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int chunk, int nslots) {
     using T = Traits<DT>;
     using S = typename T::storage;
@@ -361,7 +361,9 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             pm = q.x;
             pl = q.y;
         }
-        group_merge(pm, pl, 32);
+        group_merge(pm, pl, pow2_ceil(nwarps));  // lanes 0..nwarps-1 hold the CTA's pair
+        pm = __shfl_sync(0xffffffffu, pm, 0);
+        pl = __shfl_sync(0xffffffffu, pl, 0);
 
         // Cluster merge: warp 0 pushes this CTA's pair into slot `rank` of
         // every CTA's receive buffer (st.async, counted on their barrier); all
@@ -382,7 +384,9 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             qm = q.x;
             ql = q.y;
         }
-        group_merge(qm, ql, 32);
+        group_merge(qm, ql, pow2_ceil(cs));
+        qm = __shfl_sync(0xffffffffu, qm, 0);
+        ql = __shfl_sync(0xffffffffu, ql, 0);
         const float c = rescale(m, safe_max(qm)) / ql;
         __syncwarp();
         if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
@@ -503,6 +507,7 @@ static cudaError_t launch_wide_dt(const rs_plan& p, const void* in, void* out, i
             case 1: return launch_hold_one<DT, 1>(p, in, out, M, N, ldi, ldo, s);
             case 2: return launch_hold_one<DT, 2>(p, in, out, M, N, ldi, ldo, s);
             case 4: return launch_hold_one<DT, 4>(p, in, out, M, N, ldi, ldo, s);
+            case 8: return launch_hold_one<DT, 8>(p, in, out, M, N, ldi, ldo, s);
             default: return cudaErrorInvalidConfiguration;
         }
     }
@@ -570,6 +575,7 @@ static cudaError_t max_clusters_dt(const rs_plan& p, int* n) {
             case 1: return max_clusters_hold<DT, 1>(p, n);
             case 2: return max_clusters_hold<DT, 2>(p, n);
             case 4: return max_clusters_hold<DT, 4>(p, n);
+            case 8: return max_clusters_hold<DT, 8>(p, n);
             default: return cudaErrorInvalidConfiguration;
         }
     }

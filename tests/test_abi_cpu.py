@@ -110,14 +110,19 @@ def _covers(plan, N):
 
 
 def test_plans_for_the_benchmark_workloads():
+    # fp32: register-resident rows; 16-bit: the bulk-copy ring; vocabulary-
+    # sized rows: persistent clusters holding their slices in registers.
     p = _plan(1024, 1024, rs.RS_F32)
-    assert (p["path"], p["vec_elems"], p["threads_per_row"]) == (rs.RS_PATH_RING, 4, 32)
+    assert (p["path"], p["vec_elems"], p["threads_per_row"]) == (rs.RS_PATH_ROWS, 4, 32)
     p = _plan(8192, 5000, rs.RS_F32, ld=5120)
-    assert p["path"] == rs.RS_PATH_RING and p["vec_elems"] == 4 and _covers(p, 5000)
+    assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 4 and _covers(p, 5000)
     p = _plan(32768, 8192, rs.RS_BF16)
     assert p["path"] == rs.RS_PATH_RING and p["vec_elems"] == 8 and _covers(p, 8192)
+    assert p["ring_values"] == rs.RS_RING_REGISTERS and p["stages"] == 2
     p = _plan(512, 131072, rs.RS_F16)
-    assert p["path"] == rs.RS_PATH_CLUSTER and p["cluster_size"] >= 2 and _covers(p, 131072)
+    assert p["path"] == rs.RS_PATH_CLUSTER and p["ring_values"] == rs.RS_RING_REGISTERS
+    assert p["cluster_size"] >= 2 and _covers(p, 131072)
+    assert p["block_threads"] * p["vec_per_thread"] * 8 >= p["chunk_elems"]
     assert p["smem_bytes"] <= 232448 - 1024 and p["grid"] % p["cluster_size"] == 0
     assert p["grid"] <= 512 * p["cluster_size"]  # persistent clusters loop over rows
     p = _plan(1 << 20, 2048, rs.RS_BF16)
@@ -127,7 +132,7 @@ def test_plans_for_the_benchmark_workloads():
 def test_ring_plan_is_persistent_and_fits_shared_memory():
     for M, N, dt in [(8192, 5000, rs.RS_F32), (32768, 8192, rs.RS_BF16), (1 << 20, 2048, rs.RS_BF16),
                      (7, 300, rs.RS_F16)]:
-        p = _plan(M, N, dt, ld=-(-N // 8) * 8)
+        p = _plan(M, N, dt, ld=-(-N // 8) * 8, opts={"path": rs.RS_PATH_RING})
         assert p["path"] == rs.RS_PATH_RING
         assert 2 <= p["stages"] <= 8
         es = 4 if dt == rs.RS_F32 else 2

@@ -338,4 +338,4 @@ def test_benchmark_launch_configuration_is_the_auto_plan():
     x = W.generate(w, "cuda", 0, 4)
     rc, plan = rs.rowsoftmax_plan(x.data_ptr(), x.data_ptr() + (1 << 40), w.M, w.N, w.ld, w.ld, rs.RS_F32, None,
                                   dev)
-    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_RING
+    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_ROWS
