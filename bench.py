@@ -132,6 +132,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The max of x over all ranks of the process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processed `steps` steps of its own
+    replica of the workload in at most max_ms milliseconds."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -240,11 +257,14 @@ def run_ours(args, workloads):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     lib = rs._abi.load()
-    fwd = lib.rowsoftmax_fwd
     peak, peak_src = measured_peaks()
 
+    opts = rs._abi._opts(args.options)
     for name in workloads:
         w = W.WORKLOADS[name]
+        if args.rows:
+            w = W.Workload(w.name, w.dtype, min(args.rows, w.M), w.N, w.ld, w.seed, w.kind,
+                           f"first {min(args.rows, w.M)} rows of: {w.description}")
         code = {"f32": rs.RS_F32, "f16": rs.RS_F16, "bf16": rs.RS_BF16}[w.dtype]
         set_bytes = 2 * w.M * w.ld * w.elem_size
         nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
@@ -257,7 +277,7 @@ def run_ours(args, workloads):
 
         def step(i, st=None):
             a, b = args_list[i % nsets]
-            rc = fwd(a, b, w.M, w.N, w.ld, w.ld, code, st if st is not None else s_handle)
+            rc = lib.rowsoftmax_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, code, st if st is not None else s_handle, opts)
             if rc != rs.RS_OK:
                 raise rs.RowSoftmaxError(rc, rs.rowsoftmax_last_cuda_error())
 
@@ -307,15 +327,12 @@ def run_ours(args, workloads):
         # Every step is exactly one launch of the library's kernel, back to
         # back on graph_stream: the average launch duration is total / K.
         kern_ms = total_ms / args.steps
-        t = torch.tensor([total_ms], device=dev)
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
         clocks = sampler.finish() if sampler else None
 
         ms_per_step = total_ms / args.steps
         nbytes = w.algorithmic_bytes
-        value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+        value = job_gbs(world, nbytes, args.steps, total_ms)
         achieved = nbytes / (kern_ms * 1e-3) / 1e9
 
         # End to end through the C ABI with host buffers: every step copies
@@ -342,8 +359,8 @@ def run_ours(args, workloads):
             ev_in[b].record(s_in)
             s_k.wait_event(ev_in[b])
             s_k.wait_event(ev_out[b])
-            rc = fwd(ctypes.c_void_p(d_in[b].data_ptr()), ctypes.c_void_p(d_out[b].data_ptr()), w.M, w.N, w.ld,
-                     w.ld, code, k_handle)
+            rc = lib.rowsoftmax_fwd_ex(ctypes.c_void_p(d_in[b].data_ptr()), ctypes.c_void_p(d_out[b].data_ptr()), w.M,
+                                       w.N, w.ld, w.ld, code, k_handle, opts)
             if rc != rs.RS_OK:
                 raise rs.RowSoftmaxError(rc, rs.rowsoftmax_last_cuda_error())
             ev_k[b].record(s_k)
@@ -367,11 +384,7 @@ def run_ours(args, workloads):
         s_out.wait_stream(s_k)
         e1.record(s_out)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        t = torch.tensor([e2e_ms], device=dev)
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
 
         rc, flags = rs.rowsoftmax_device_status()
         if rc != rs.RS_OK or flags:
@@ -379,7 +392,8 @@ def run_ours(args, workloads):
 
         if rank == 0:
             rc, info = rs.rowsoftmax_device_info()
-            rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code, None, info)
+            rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code,
+                                          args.options, info)
             line = {
                 "metric": "achieved HBM GB/s (row softmax)", "value": round(value, 2), "unit": "GB/s",
                 "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
@@ -387,17 +401,19 @@ def run_ours(args, workloads):
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "rows_per_s": round(world * w.M / (ms_per_step * 1e-3), 1),
                 "hbm_roofline_frac": round(value / world / peak, 4),
-                "config": {"workload": name, "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
+                "config": {"workload": name if not args.rows else f"{name} (first {w.M} rows)",
+                           "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
+                           "options": args.options,
                            "bytes_per_step": nbytes, "parallelism": "replicas",
                            "l2": f"{nsets} rotating input/output sets of {set_bytes / 1e6:.0f} MB; "
                                  f"{reuse_mb:.0f} MB pass between two uses of a set (L2 is 129 MB)",
                            "kernel": rs.PATH_NAMES[plan["path"]], "plan": plan},
                 "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name),
+                             "frac": round(achieved / peak, 4), "traffic": None if (args.options or args.rows) else ncu_traffic(name),
                              "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
                              if peak_src == "measured" else "fallback 6.8 TB/s",
                              "kernel_ms": round(kern_ms, 5)},
-                "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "e2e": {"value": round(job_gbs(world, nbytes, 1, e2e_ms), 2), "unit": "GB/s",
                         "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
                         "d2h_bytes_per_step": h_out[0].numel() * h_out[0].element_size(),
                         "ms_per_step": round(e2e_ms, 4),
@@ -424,7 +440,12 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, help="a workload name, or 'all'")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--options", default=None,
+                    help="JSON object of rs_options fields forcing a kernel configuration (tuning, profiling)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="use only the first ROWS rows of the workload (smaller profiler captures)")
     args = ap.parse_args()
+    args.options = json.loads(args.options) if args.options else None
     if args.warmup < 3:
         args.warmup = 3
     from memory_bound_row_gb300 import workloads as W
