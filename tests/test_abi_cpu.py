@@ -127,6 +127,16 @@ def test_plans_for_the_benchmark_workloads():
     assert p["grid"] <= 512 * p["cluster_size"]  # persistent clusters loop over rows
     p = _plan(1 << 20, 2048, rs.RS_BF16)
     assert p["path"] == rs.RS_PATH_RING and _covers(p, 2048)
+    # a 2048-element bf16 row fits one warp at 64 values a thread: no CTA barrier per row
+    assert (p["threads_per_row"], p["vec_per_thread"]) == (32, 8)
+
+
+def test_few_rows_are_spread_over_the_sms():
+    p = _plan(1024, 1024, rs.RS_F32)
+    assert p["grid"] >= 2 * 152 and p["block_threads"] % 32 == 0
+    assert p["rows_per_cta"] * p["grid"] >= 1024
+    p = _plan(1 << 16, 1024, rs.RS_F32)  # many rows: full 256-thread CTAs
+    assert p["block_threads"] == 256
 
 
 def test_ring_plan_is_persistent_and_fits_shared_memory():
