@@ -108,6 +108,11 @@ typedef struct {
     int ring_values;      /* RS_PATH_RING: rs_ring_values */
     int force_scalar;     /* 1: element-wise accesses even when 16-byte vectors would be legal */
     int64_t grid_limit;   /* >0: cap on CTAs (rows loop inside the kernel); 0: one launch slot per row group */
+    int64_t wait_limit_us;  /* RS_PATH_RING: >0 bounds each mbarrier wait (default 4 s) */
+    int withhold_copies;  /* RS_PATH_RING, failure-path tests only: post the expected bytes of every
+                             stage but never issue the copies, so each wait runs out after
+                             wait_limit_us, bit 0 of the device status word is set and the output
+                             is left unwritten; no fault, trap or unbounded wait is involved */
 } rs_options;
 
 /* What a call would launch (filled by rowsoftmax_plan). */
@@ -125,6 +130,8 @@ typedef struct {
     int64_t chunk_elems;  /* RS_PATH_CLUSTER / RS_PATH_STREAM: row slice per CTA */
     int64_t grid;         /* CTAs launched */
     size_t smem_bytes;    /* dynamic shared memory per CTA */
+    int64_t wait_limit_us;  /* copied from rs_options */
+    int withhold_copies;  /* copied from rs_options */
 } rs_plan;
 
 /* Device facts the planner needs; rowsoftmax_plan takes them explicitly so
@@ -181,9 +188,10 @@ RS_API const char* rowsoftmax_status_string(int status);
 RS_API int rowsoftmax_last_cuda_error(void);
 
 /*
- * Device-side status word of the current device.  The cluster kernels bound
- * every wait on an mbarrier; a wait that runs out sets bit 0 and the CTA
- * abandons its row (the output row is then incomplete).  Reads the word
+ * Device-side status word of the current device.  The ring and cluster
+ * kernels bound every wait on an mbarrier; a wait that runs out sets bit 0
+ * and its CTA abandons the rows it was serving: the output of a call that
+ * reported a timeout is undefined in those rows.  Reads the word
  * (synchronously, with cudaMemcpyFromSymbol) into *flags and clears it when
  * `clear` is nonzero.  Returns RS_OK or RS_ERR_CUDA.
  */

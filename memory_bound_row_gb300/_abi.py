@@ -52,6 +52,8 @@ class rs_options(ctypes.Structure):
         ("ring_values", ctypes.c_int),
         ("force_scalar", ctypes.c_int),
         ("grid_limit", ctypes.c_int64),
+        ("wait_limit_us", ctypes.c_int64),
+        ("withhold_copies", ctypes.c_int),
     ]
 
 
@@ -70,6 +72,8 @@ class rs_plan(ctypes.Structure):
         ("chunk_elems", ctypes.c_int64),
         ("grid", ctypes.c_int64),
         ("smem_bytes", ctypes.c_size_t),
+        ("wait_limit_us", ctypes.c_int64),
+        ("withhold_copies", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -109,12 +109,13 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Waits for the phase of `bar` with the given parity to complete; false if
-// that takes longer than kWaitLimitNs.
-static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// that takes longer than limit_ns (default kWaitLimitNs).
+static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                      uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

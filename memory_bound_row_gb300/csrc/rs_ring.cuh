@@ -18,9 +18,9 @@
 // cp.async pipeline"), applied to rows and carried by the bulk-copy engine.
 //
 // The last partial 16-byte unit of a row (N not a multiple of 16 bytes) is
-// read straight from global memory.  Waits are bounded (rs_async.cuh); a wait
-// that runs out flags the device status word, and the CTA lets its copies in
-// flight land (bounded again) and stops.
+// read straight from global memory.  Waits are bounded (rs_async.cuh); a thread
+// whose wait runs out flags the device status word and writes nothing more;
+// the CTA lets its copies in flight land (bounded again) and stops.
 #pragma once
 
 #include <mutex>
@@ -53,7 +53,8 @@ __device__ __forceinline__ void ring_unit(const unsigned char* srow, const typen
 template <int DT, int VPT, bool HOLD>
 __global__ void __launch_bounds__(HOLD ? rows_block_limit(VPT, Traits<DT>::kVec) : kRingRereadThreads,
                                   HOLD ? 1 : kRingRereadMinCtas)
-ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, int stages) {
+ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, int stages,
+            uint64_t wait_ns, int withhold) {
     using T = Traits<DT>;
     using S = typename T::storage;
     constexpr int VEC = T::kVec;
@@ -86,6 +87,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
             return;
         }
         mbar_arrive_expect_tx(&full[s], slot * (uint32_t)nrows);
+        if (withhold) return;  // failure-path test: the awaited bytes never come
         unsigned char* dst = ring + (size_t)s * stage_bytes;
         for (int k = 0; k < nrows; ++k) bulk_load(dst + (size_t)k * slot, in + (r0 + k) * ldi, slot, &full[s]);
     };
@@ -107,7 +109,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
     uint32_t parity = 0;
     int64_t it = 0;
     for (int64_t g = blockIdx.x; g < groups; g += gridDim.x, ++it) {
-        if (!abort && !mbar_wait_bounded(&full[s], parity)) {
+        if (!abort && !mbar_wait_bounded(&full[s], parity, wait_ns)) {
             abort = true;
             flag_timeout();
         }
@@ -128,7 +130,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
                     ring_unit<DT, VPT, HOLD>(srow, grow, t + k * tpr, units_full, N, active, v[k]);
             }
             const float c = row_exp_and_scale<VPT, VEC>(v, tpr, part[it & 1]);
-            if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v, c);
+            if (active && !abort) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v, c);
         } else {
             float f[VEC];
             float m = kNegInf;
@@ -172,7 +174,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
                 c = rescale(m, mrs) / srow_sum;
             }
 
-            if (active) {
+            if (active && !abort) {
                 S* yr = out + row * ldo;
                 asm volatile("" ::: "memory");
 #pragma unroll 1
@@ -211,7 +213,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         for (int64_t j = it; j < it + stages; ++j) {
             const int64_t gj = blockIdx.x + j * gridDim.x;
             if (gj >= groups) break;
-            (void)mbar_wait_bounded(&full[j % stages], (uint32_t)((j / stages) & 1));
+            (void)mbar_wait_bounded(&full[j % stages], (uint32_t)((j / stages) & 1), wait_ns);
         }
     }
 }
@@ -240,8 +242,9 @@ cudaError_t launch_ring_one(const rs_plan& p, const void* in, void* out, int64_t
             ready[dev] = true;
         }
     }
+    const uint64_t wait_ns = p.wait_limit_us > 0 ? (uint64_t)p.wait_limit_us * 1000ull : kWaitLimitNs;
     kern<<<(unsigned)p.grid, p.block_threads, p.smem_bytes, s>>>(in, out, M, N, ldi, ldo, p.threads_per_row,
-                                                                 p.stages);
+                                                                 p.stages, wait_ns, p.withhold_copies);
     return cudaGetLastError();
 }
 

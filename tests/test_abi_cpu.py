@@ -211,6 +211,18 @@ def test_forced_options():
     assert p["grid"] == 5
 
 
+def test_failure_path_options_are_validated():
+    ok = {"path": rs.RS_PATH_RING, "withhold_copies": 1, "wait_limit_us": 20000}
+    p = _plan(64, 4096, rs.RS_BF16, opts=ok)
+    assert p["withhold_copies"] == 1 and p["wait_limit_us"] == 20000
+    for bad in [{"path": rs.RS_PATH_RING, "withhold_copies": 1},
+                {"path": rs.RS_PATH_ROWS, "withhold_copies": 1, "wait_limit_us": 100},
+                {"withhold_copies": 2, "path": rs.RS_PATH_RING, "wait_limit_us": 100},
+                {"wait_limit_us": -1}]:
+        rc, _ = rs.rowsoftmax_plan(A, A + (1 << 40), 64, 4096, 4096, 4096, rs.RS_BF16, bad, gb300())
+        assert rc == rs.RS_ERR_INVALID_ARG, bad
+
+
 def test_layout_owner_matches_the_pages_worked_example():
     with open(GOLDEN) as f:
         lines = [ln for ln in f if ln.strip() and not ln.startswith("#")]
