@@ -339,3 +339,35 @@ def test_benchmark_launch_configuration_is_the_auto_plan():
     rc, plan = rs.rowsoftmax_plan(x.data_ptr(), x.data_ptr() + (1 << 40), w.M, w.N, w.ld, w.ld, rs.RS_F32, None,
                                   dev)
     assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_ROWS
+
+
+# ---------------------------------------------------------------------------
+# Maximum sizes.
+# ---------------------------------------------------------------------------
+
+def test_more_than_two_to_the_31_rows():
+    # 2^31 + 5 rows of [0, ln 3] in bf16: every row is the same, so every output
+    # row must equal the oracle's result for that one row; row offsets pass 4 GB.
+    M = (1 << 31) + 5
+    x = torch.empty((M, 2), dtype=torch.bfloat16, device="cuda")
+    x[:, 0] = 0.0
+    x[:, 1] = math.log(3.0)
+    y = rs.softmax(x)
+    torch.cuda.synchronize()
+    ref = oracle_rows(x[:1], 2)[0]
+    for col in range(2):
+        got = y[:, col].float()
+        assert float((got.double() - ref[col]).abs().max()) <= 4e-3
+        assert bool((got == got[0]).all())  # every row identical
+    del x, y
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+def test_a_row_of_two_to_the_26_elements(dtype):
+    N = 1 << 26
+    x = _input(2, N, dtype, kind="normal_spike", seed=26)
+    y = _run(x)
+    _check(x, y, what=f"2 x 2^26 {dtype}")
+    del x, y
+    torch.cuda.empty_cache()
