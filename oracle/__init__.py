@@ -58,6 +58,10 @@ def _load():
             lib.orc_decode_array.restype = None
             lib.orc_encode_array.argtypes = [vp, ctypes.c_int, i64, vp]
             lib.orc_encode_array.restype = None
+            lib.orc_rmsnorm_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, ctypes.c_double, vp, i64]
+            lib.orc_rmsnorm_f64.restype = ctypes.c_int
+            lib.orc_layernorm_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp, ctypes.c_double, vp, i64]
+            lib.orc_layernorm_f64.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -116,3 +120,42 @@ def encode(values: np.ndarray, fmt: str) -> np.ndarray:
     out = np.empty(values.shape, dtype=_NP_STORAGE[fmt])
     _load().orc_encode_array(values.ctypes.data, FORMATS[fmt], values.size, out.ctypes.data)
     return out
+
+
+def _vec(v, fmt, n):
+    if v is None:
+        return None
+    v = _as_storage(np.ascontiguousarray(v).reshape(-1), fmt)
+    if v.size != n:
+        raise ValueError(f"expected {n} values, got {v.size}")
+    return v
+
+
+def rmsnorm_f64(x: np.ndarray, fmt: str, weight=None, eps: float = 1e-6, n_cols: int | None = None) -> np.ndarray:
+    """RMSNorm of the rows of x (see softmax_f64 for the layout): y = x / sqrt(mean(x^2) + eps) * w."""
+    x = _as_storage(np.atleast_2d(x), fmt)
+    M, ld = x.shape
+    N = ld if n_cols is None else int(n_cols)
+    w = _vec(weight, fmt, N)
+    y = np.empty((M, N), dtype=np.float64)
+    rc = _load().orc_rmsnorm_f64(x.ctypes.data, FORMATS[fmt], M, N, ld, None if w is None else w.ctypes.data,
+                                 float(eps), y.ctypes.data, N)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the call (status {rc})")
+    return y
+
+
+def layernorm_f64(x: np.ndarray, fmt: str, weight=None, bias=None, eps: float = 1e-5,
+                  n_cols: int | None = None) -> np.ndarray:
+    """LayerNorm of the rows of x: y = (x - mean) / sqrt(var + eps) * w + b (population variance)."""
+    x = _as_storage(np.atleast_2d(x), fmt)
+    M, ld = x.shape
+    N = ld if n_cols is None else int(n_cols)
+    w = _vec(weight, fmt, N)
+    b = _vec(bias, fmt, N)
+    y = np.empty((M, N), dtype=np.float64)
+    rc = _load().orc_layernorm_f64(x.ctypes.data, FORMATS[fmt], M, N, ld, None if w is None else w.ctypes.data,
+                                   None if b is None else b.ctypes.data, float(eps), y.ctypes.data, N)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the call (status {rc})")
+    return y

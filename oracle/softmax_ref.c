@@ -29,7 +29,10 @@
  *  - output encoding to fp16 / bf16 is round-to-nearest, ties-to-even, done
  *    directly from the double result (no intermediate fp32 rounding).
  *
- * Parity pins for this file live in tests/test_oracle_pins.py.
+ * It also holds the plain definitions of RMSNorm and LayerNorm (end of file).
+ *
+ * Parity pins for this file live in tests/test_oracle_pins.py and
+ * tests/test_oracle_norm_pins.py.
  */
 #include <math.h>
 #include <pthread.h>
@@ -247,4 +250,61 @@ int orc_softmax_store(const void* x, void* y, int dtype, int64_t M, int64_t N,
     free(jobs);
     free(th);
     return status;
+}
+
+/* ---------------------------------------------------------------------------
+ * Row normalisations (the next operation on the same row engine).
+ *
+ * RMSNorm, as the "Reference Kernel: RMSNorm" of the Hugging Face
+ * "triton-kernels" skill page computes it:
+ *     r_r = sqrt( (1/N) sum_k x[r][k]^2 + eps ),   y[r][j] = x[r][j] / r_r * w[j]
+ * LayerNorm (the pages name it, next to softmax, as a memory-bound row kernel,
+ * without a formula; the plain definition is taken: population variance,
+ * eps inside the square root, optional elementwise weight and bias):
+ *     mu_r = (1/N) sum_k x[r][k],   var_r = (1/N) sum_k (x[r][k] - mu_r)^2,
+ *     y[r][j] = (x[r][j] - mu_r) / sqrt(var_r + eps) * w[j] + b[j]
+ * w (and b) are N stored values of the same format as x; a NULL w means 1,
+ * a NULL b means 0.  Results are double; sums are plain recursive sums.
+ * ------------------------------------------------------------------------- */
+static double orc_vec(const void* v, int dtype, int64_t j, double dflt)
+{
+    return v ? orc_load(v, dtype, j) : dflt;
+}
+
+int orc_rmsnorm_f64(const void* x, int dtype, int64_t M, int64_t N, int64_t ldx, const void* w, double eps,
+                    double* y, int64_t ldy)
+{
+    if (orc_check(dtype, M, N, ldx, ldy)) return 1;
+    for (int64_t r = 0; r < M; ++r) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double v = orc_load(x, dtype, r * ldx + j);
+            ss += v * v;
+        }
+        const double rms = sqrt(ss / (double)N + eps);
+        for (int64_t j = 0; j < N; ++j)
+            y[r * ldy + j] = orc_load(x, dtype, r * ldx + j) / rms * orc_vec(w, dtype, j, 1.0);
+    }
+    return 0;
+}
+
+int orc_layernorm_f64(const void* x, int dtype, int64_t M, int64_t N, int64_t ldx, const void* w, const void* b,
+                      double eps, double* y, int64_t ldy)
+{
+    if (orc_check(dtype, M, N, ldx, ldy)) return 1;
+    for (int64_t r = 0; r < M; ++r) {
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) s += orc_load(x, dtype, r * ldx + j);
+        const double mu = s / (double)N;
+        double d = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double v = orc_load(x, dtype, r * ldx + j) - mu;
+            d += v * v;
+        }
+        const double sd = sqrt(d / (double)N + eps);
+        for (int64_t j = 0; j < N; ++j)
+            y[r * ldy + j] = (orc_load(x, dtype, r * ldx + j) - mu) / sd * orc_vec(w, dtype, j, 1.0) +
+                             orc_vec(b, dtype, j, 0.0);
+    }
+    return 0;
 }
