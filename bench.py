@@ -1,9 +1,12 @@
 """Benchmark of the fused row softmax on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all] [--impl ours|reference]
+                    [--op softmax|rmsnorm|layernorm]
 
 One step is one rowsoftmax_fwd call (the whole hot path: load, max, exp,
-sum, normalise, store) over one batch of the workload.  The default workload
+sum, normalise, store) over one batch of the workload.  With --op rmsnorm or
+layernorm a step is one rmsnorm_fwd / layernorm_fwd call (with weight, and
+bias for LayerNorm) on the same shapes.  The default workload
 is fp32 8192 x 5000 with row stride 5120.  Rank 0 prints one JSON line per
 workload with achieved HBM GB/s (bytes = M * N * (in + out element size)),
 rows/s, the roofline fraction of the kernel against the measured HBM copy
@@ -149,6 +152,64 @@ def job_gbs(world: int, bytes_per_step: int, steps: int, max_ms: float) -> float
     return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
 
 
+OP_CODES = {"softmax": 0, "rmsnorm": 1, "layernorm": 2}
+OP_EPS = {"softmax": 0.0, "rmsnorm": 1e-6, "layernorm": 1e-5}
+OP_METRIC = {"softmax": "achieved HBM GB/s (row softmax)", "rmsnorm": "achieved HBM GB/s (RMSNorm)",
+             "layernorm": "achieved HBM GB/s (LayerNorm)"}
+
+
+def op_workload(op: str, name: str):
+    from memory_bound_row_gb300 import workloads as W
+
+    return W.WORKLOADS[name] if op == "softmax" else W.norm_workload(name)
+
+
+def op_bytes(op: str, w) -> int:
+    """Algorithmic bytes of one call: every element read once and written
+    once, plus the weight (and bias) vector read once."""
+    vectors = {"softmax": 0, "rmsnorm": 1, "layernorm": 2}[op]
+    return w.algorithmic_bytes + vectors * w.N * w.elem_size
+
+
+def traffic_key(op: str, name: str) -> str:
+    return name if op == "softmax" else f"{op}:{name}"
+
+
+def oracle_op(op: str, x_np, fmt: str, n_cols: int, params, threads: int, out=None):
+    """The oracle's result for the rows of x_np, on `threads` host threads."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import oracle
+
+    if op == "softmax":
+        return oracle.softmax_store(x_np, fmt, n_cols, nthreads=threads, out=out)
+    w, b = params
+    blocks = [blk for blk in np.array_split(np.arange(x_np.shape[0]), threads) if len(blk)]
+
+    def work(blk):
+        part = x_np[blk[0]: blk[-1] + 1]
+        if op == "rmsnorm":
+            return oracle.rmsnorm_f64(part, fmt, w, OP_EPS[op], n_cols)
+        return oracle.layernorm_f64(part, fmt, w, b, OP_EPS[op], n_cols)
+
+    with cf.ThreadPoolExecutor(len(blocks)) as ex:
+        return list(ex.map(work, blocks))
+
+
+def host_params(w):
+    """The weight and bias vectors of workload w in the oracle's storage format."""
+    import numpy as np
+    import torch
+
+    from memory_bound_row_gb300 import workloads as W
+
+    wt, bs = W.norm_params(w.N, w.dtype, w.seed, "cpu")
+    conv = (lambda t: t.view(torch.int16).numpy().view(np.uint16)) if w.dtype == "bf16" else (lambda t: t.numpy())
+    return conv(wt), conv(bs)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -169,35 +230,37 @@ def run_reference(args, workloads):
     if rank != 0:
         return
     cores = os.cpu_count() or 1
+    op = args.op
     for name in workloads:
-        w = W.WORKLOADS[name]
+        w = op_workload(op, name)
         fmt = w.dtype
+        params = host_params(w) if op != "softmax" else None
         probe_rows = min(w.M, max(cores, 8))
         xs = W.generate(w, "cpu", 0, probe_rows)
         store = lambda t: t.view(torch.int16).numpy().view(np.uint16) if fmt == "bf16" else t.numpy()
         x_np = store(xs[:, : w.N].contiguous())
         t = time.perf_counter()
-        oracle.softmax_store(x_np, fmt, w.N, nthreads=cores)
+        oracle_op(op, x_np, fmt, w.N, params, cores)
         per_row = (time.perf_counter() - t) / probe_rows
         budget = 60.0  # seconds for the whole run
         rows_per_step = max(1, min(probe_rows, int(budget / max(1, args.steps + args.warmup) / per_row)))
         sample = x_np[:rows_per_step]
         for _ in range(args.warmup):
-            oracle.softmax_store(sample, fmt, w.N, nthreads=cores)
+            oracle_op(op, sample, fmt, w.N, params, cores)
         t = time.perf_counter()
         for _ in range(args.steps):
-            oracle.softmax_store(sample, fmt, w.N, nthreads=cores)
+            oracle_op(op, sample, fmt, w.N, params, cores)
         dt = (time.perf_counter() - t) / args.steps
         nbytes = rows_per_step * w.N * 2 * w.elem_size
         gbs = nbytes / dt / 1e9
         sample_desc = f"{rows_per_step} of {w.M} rows per step ({w.description}), host oracle, fp64"
         line = {
-            "impl": "reference", "metric": "achieved HBM GB/s (row softmax)", "value": round(gbs, 4),
+            "impl": "reference", "metric": OP_METRIC[op], "value": round(gbs, 4),
             "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "rows_per_s": round(rows_per_step / dt, 2),
-            "config": {"workload": name, "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
+            "config": {"workload": name, "op": op, "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
                        "parallelism": "replicas"},
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample_desc},
@@ -206,16 +269,15 @@ def run_reference(args, workloads):
         print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w, x_dev, seconds: float = 3.0) -> dict:
+def cpu_baseline(w, x_dev, op: str = "softmax", seconds: float = 3.0) -> dict:
     """The oracle, as it stands, on a bounded sample of rows of the workload
     on all host cores, repeated for about `seconds` of wall time."""
     import numpy as np
     import torch
 
-    import oracle
-
     cores = os.cpu_count() or 1
     fmt = w.dtype
+    params = host_params(w) if op != "softmax" else None
 
     def host(rows):
         t = x_dev[:rows, : w.N].cpu().contiguous()
@@ -224,7 +286,7 @@ def cpu_baseline(w, x_dev, seconds: float = 3.0) -> dict:
     probe = min(w.M, max(cores, 16))
     xs = host(probe)
     t = time.perf_counter()
-    oracle.softmax_store(xs, fmt, w.N, nthreads=cores)
+    oracle_op(op, xs, fmt, w.N, params, cores)
     per_row = (time.perf_counter() - t) / probe
     rows = int(min(w.M, max(probe, seconds / 4 / max(per_row, 1e-9))))
     xs = host(rows)
@@ -232,14 +294,15 @@ def cpu_baseline(w, x_dev, seconds: float = 3.0) -> dict:
     passes = 0
     t = time.perf_counter()
     while True:
-        oracle.softmax_store(xs, fmt, w.N, nthreads=cores, out=out)
+        oracle_op(op, xs, fmt, w.N, params, cores, out=out)
         passes += 1
         if time.perf_counter() - t >= seconds:
             break
     dt = (time.perf_counter() - t) / passes
     nbytes = rows * w.N * 2 * w.elem_size
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {rows} of {w.M} rows x {passes} passes, fp64 oracle writing {w.dtype}, "
+            "sample": f"first {rows} of {w.M} rows x {passes} passes, fp64 {op} oracle"
+                      f"{' writing ' + w.dtype if op == 'softmax' else ''}, "
                       f"{dt * passes:.1f} s wall on {cores} threads",
             "rows_per_s": round(rows / dt, 2)}
 
@@ -260,8 +323,9 @@ def run_ours(args, workloads):
     peak, peak_src = measured_peaks()
 
     opts = rs._abi._opts(args.options)
+    op = args.op
     for name in workloads:
-        w = W.WORKLOADS[name]
+        w = op_workload(op, name)
         if args.rows:
             w = W.Workload(w.name, w.dtype, min(args.rows, w.M), w.N, w.ld, w.seed, w.kind,
                            f"first {min(args.rows, w.M)} rows of: {w.description}")
@@ -274,10 +338,20 @@ def run_ours(args, workloads):
         stream = torch.cuda.current_stream(dev)
         s_handle = ctypes.c_void_p(stream.cuda_stream)
         args_list = [(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr())) for x, y in zip(xs, ys)]
+        if op != "softmax":
+            wt, bs = W.norm_params(w.N, w.dtype, w.seed, dev)
+            p_w = ctypes.c_void_p(wt.data_ptr())
+            p_b = ctypes.c_void_p(bs.data_ptr()) if op == "layernorm" else None
+
+        def call(a, b, st):
+            if op == "softmax":
+                return lib.rowsoftmax_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, code, st, opts)
+            return lib.rownorm_fwd_ex(OP_CODES[op], a, b, p_w, p_b, w.M, w.N, w.ld, w.ld, OP_EPS[op], code, st,
+                                      opts)
 
         def step(i, st=None):
             a, b = args_list[i % nsets]
-            rc = lib.rowsoftmax_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, code, st if st is not None else s_handle, opts)
+            rc = call(a, b, st if st is not None else s_handle)
             if rc != rs.RS_OK:
                 raise rs.RowSoftmaxError(rc, rs.rowsoftmax_last_cuda_error())
 
@@ -331,7 +405,7 @@ def run_ours(args, workloads):
         clocks = sampler.finish() if sampler else None
 
         ms_per_step = total_ms / args.steps
-        nbytes = w.algorithmic_bytes
+        nbytes = op_bytes(op, w)
         value = job_gbs(world, nbytes, args.steps, total_ms)
         achieved = nbytes / (kern_ms * 1e-3) / 1e9
 
@@ -359,8 +433,7 @@ def run_ours(args, workloads):
             ev_in[b].record(s_in)
             s_k.wait_event(ev_in[b])
             s_k.wait_event(ev_out[b])
-            rc = lib.rowsoftmax_fwd_ex(ctypes.c_void_p(d_in[b].data_ptr()), ctypes.c_void_p(d_out[b].data_ptr()), w.M,
-                                       w.N, w.ld, w.ld, code, k_handle, opts)
+            rc = call(ctypes.c_void_p(d_in[b].data_ptr()), ctypes.c_void_p(d_out[b].data_ptr()), k_handle)
             if rc != rs.RS_OK:
                 raise rs.RowSoftmaxError(rc, rs.rowsoftmax_last_cuda_error())
             ev_k[b].record(s_k)
@@ -392,16 +465,21 @@ def run_ours(args, workloads):
 
         if rank == 0:
             rc, info = rs.rowsoftmax_device_info()
-            rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code,
-                                          args.options, info)
+            if op == "softmax":
+                rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code,
+                                              args.options, info)
+            else:
+                rc, plan = rs.rownorm_plan(OP_CODES[op], xs[0].data_ptr(), ys[0].data_ptr(), wt.data_ptr(),
+                                           bs.data_ptr() if op == "layernorm" else None, w.M, w.N, w.ld, w.ld,
+                                           OP_EPS[op], code, args.options, info)
             line = {
-                "metric": "achieved HBM GB/s (row softmax)", "value": round(value, 2), "unit": "GB/s",
+                "metric": OP_METRIC[op], "value": round(value, 2), "unit": "GB/s",
                 "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
                 "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "rows_per_s": round(world * w.M / (ms_per_step * 1e-3), 1),
                 "hbm_roofline_frac": round(value / world / peak, 4),
-                "config": {"workload": name if not args.rows else f"{name} (first {w.M} rows)",
+                "config": {"workload": name if not args.rows else f"{name} (first {w.M} rows)", "op": op,
                            "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
                            "options": args.options,
                            "bytes_per_step": nbytes, "parallelism": "replicas",
@@ -409,7 +487,7 @@ def run_ours(args, workloads):
                                  f"{reuse_mb:.0f} MB pass between two uses of a set (L2 is 129 MB)",
                            "kernel": rs.PATH_NAMES[plan["path"]], "plan": plan},
                 "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(achieved / peak, 4), "traffic": None if (args.options or args.rows) else ncu_traffic(name),
+                             "frac": round(achieved / peak, 4), "traffic": None if (args.options or args.rows) else ncu_traffic(traffic_key(op, name)),
                              "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
                              if peak_src == "measured" else "fallback 6.8 TB/s",
                              "kernel_ms": round(kern_ms, 5)},
@@ -417,14 +495,15 @@ def run_ours(args, workloads):
                         "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
                         "d2h_bytes_per_step": h_out[0].numel() * h_out[0].element_size(),
                         "ms_per_step": round(e2e_ms, 4),
-                        "how": "pinned host input copied in, rowsoftmax_fwd, output copied back, every step; "
+                        "how": f"pinned host input copied in, {'rowsoftmax_fwd' if op == 'softmax' else op + '_fwd'}, "
+                               "output copied back, every step; "
                                "two buffer pairs overlap step i+1's copy-in with step i"},
                 "gpu_launches": args.steps,
                 "timing": f"{args.steps // G} replays of a CUDA graph of {G} launches, one event pair",
                 "clocks": clocks,
             }
             if not args.no_cpu_baseline:
-                line["cpu_baseline"] = cpu_baseline(w, xs[0])
+                line["cpu_baseline"] = cpu_baseline(w, xs[0], op)
             print(json.dumps(line), flush=True)
         del xs, ys, h_in, h_out, d_in, d_out, graph
         torch.cuda.empty_cache()
@@ -439,6 +518,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, help="a workload name, or 'all'")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=sorted(OP_CODES), default="softmax",
+                    help="the row operation timed (softmax: the fused row softmax; rmsnorm, layernorm: the "
+                         "normalisations on the same row engine)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--options", default=None,
                     help="JSON object of rs_options fields forcing a kernel configuration (tuning, profiling)")

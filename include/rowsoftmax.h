@@ -72,6 +72,13 @@ typedef enum {
     RS_ERR_NO_PATH = 6             /* the forced options cannot serve this shape */
 } rs_status;
 
+/* Row operations served by the same row engine (rs_plan.op). */
+typedef enum {
+    RS_OP_SOFTMAX = 0,   /* rowsoftmax_fwd */
+    RS_OP_RMSNORM = 1,   /* rmsnorm_fwd */
+    RS_OP_LAYERNORM = 2  /* layernorm_fwd */
+} rs_op;
+
 /* Kernel families (see rs_plan). */
 typedef enum {
     RS_PATH_AUTO = 0,     /* let the library choose (the default) */
@@ -80,7 +87,9 @@ typedef enum {
                              shared memory with bulk asynchronous copies (TMA engine), online (m, l),
                              partial pairs merged over distributed shared memory; reads HBM once */
     RS_PATH_STREAM = 3,   /* any row: a cluster per row streams its slice twice from global memory
-                             (online (m, l) on the first read, normalise on the second); reads 2x */
+                             (online (m, l) on the first read, normalise on the second); reads 2x.
+                             Normalisations: one CTA per row, reading it once per moment and
+                             once to write (RMSNorm 2x, LayerNorm 3x) */
     RS_PATH_RING = 4      /* single pass as RS_PATH_ROWS, but a persistent grid whose CTAs stage the
                              next row groups in a ring of shared-memory stages filled by bulk
                              asynchronous copies (TMA engine); 16-byte aligned data only */
@@ -132,6 +141,7 @@ typedef struct {
     size_t smem_bytes;    /* dynamic shared memory per CTA */
     int64_t wait_limit_us;  /* copied from rs_options */
     int withhold_copies;  /* copied from rs_options */
+    int op;               /* rs_op the plan serves */
 } rs_plan;
 
 /* Device facts the planner needs; rowsoftmax_plan takes them explicitly so
@@ -175,6 +185,58 @@ RS_API int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N,
 RS_API int rowsoftmax_plan(const void* in, const void* out, int64_t M, int64_t N,
                     int64_t in_row_stride, int64_t out_row_stride, int dtype,
                     const rs_options* opts, const rs_device_info* dev, rs_plan* plan);
+
+/*
+ * Row normalisations on the same engine (one read of x, one write of y for
+ * every row that the register and ring kernels hold; RS_PATH_STREAM re-reads
+ * wider rows).  Data model, ownership, in-place rule, asynchrony and error
+ * behaviour are those of rowsoftmax_fwd; `weight` and `bias` are further
+ * DEVICE pointers to N values of the same storage type `dtype` (contiguous,
+ * read only, element-aligned; 16-byte alignment of both, as of x and y, lets
+ * the vector kernels run), and may be NULL (weight 1, bias 0).  They must not
+ * overlap `out` (RS_ERR_OVERLAP).  `eps` must be finite and >= 0
+ * (RS_ERR_INVALID_ARG otherwise); the kernels compute in fp32 and round the
+ * result to `dtype` with round-to-nearest-even.
+ *
+ * RMSNorm, after the "Reference Kernel: RMSNorm" of the Hugging Face
+ * "triton-kernels" skill page (fp32 accumulation, masked lanes read as 0):
+ *
+ *     y[r][j] = x[r][j] / sqrt(sum_k x[r][k]^2 / N + eps) * w[j].
+ */
+RS_API int rmsnorm_fwd(const void* in, void* out, const void* weight, int64_t M, int64_t N,
+                       int64_t in_row_stride, int64_t out_row_stride, double eps, int dtype,
+                       cudaStream_t stream);
+
+/*
+ * LayerNorm, which the nano-triton post ("Rebuilding Triton and Helion from
+ * Scratch", the opening and "deuteron: the autotuning layer") names beside
+ * softmax as a memory-bound row kernel, without a formula; the plain
+ * definition is taken, population variance and eps inside the square root:
+ *
+ *     mu_r  = sum_k x[r][k] / N,   var_r = sum_k (x[r][k] - mu_r)^2 / N,
+ *     y[r][j] = (x[r][j] - mu_r) / sqrt(var_r + eps) * w[j] + b[j].
+ *
+ * Arguments as rmsnorm_fwd, plus `bias`.
+ */
+RS_API int layernorm_fwd(const void* in, void* out, const void* weight, const void* bias, int64_t M,
+                         int64_t N, int64_t in_row_stride, int64_t out_row_stride, double eps,
+                         int dtype, cudaStream_t stream);
+
+/* rmsnorm_fwd (op RS_OP_RMSNORM, bias must be NULL) or layernorm_fwd (op
+ * RS_OP_LAYERNORM) with forcing options.  Paths RS_PATH_ROWS, RS_PATH_RING
+ * and RS_PATH_STREAM serve the normalisations; RS_PATH_CLUSTER and
+ * RS_RING_REREAD return RS_ERR_NO_PATH.  An op that is not RS_OP_RMSNORM or
+ * RS_OP_LAYERNORM is RS_ERR_INVALID_ARG. */
+RS_API int rownorm_fwd_ex(int op, const void* in, void* out, const void* weight, const void* bias,
+                          int64_t M, int64_t N, int64_t in_row_stride, int64_t out_row_stride,
+                          double eps, int dtype, cudaStream_t stream, const rs_options* opts);
+
+/* Host-only planner of rownorm_fwd_ex, as rowsoftmax_plan is of
+ * rowsoftmax_fwd_ex. */
+RS_API int rownorm_plan(int op, const void* in, const void* out, const void* weight, const void* bias,
+                        int64_t M, int64_t N, int64_t in_row_stride, int64_t out_row_stride,
+                        double eps, int dtype, const rs_options* opts, const rs_device_info* dev,
+                        rs_plan* plan);
 
 /* Host-only: fill `dev` for the current CUDA device.  Returns RS_OK or
  * RS_ERR_CUDA. */

@@ -26,6 +26,8 @@ RS_ERR_NO_PATH = 6
 # rs_path
 RS_PATH_AUTO, RS_PATH_ROWS, RS_PATH_CLUSTER, RS_PATH_STREAM, RS_PATH_RING = 0, 1, 2, 3, 4
 RS_RING_AUTO, RS_RING_REGISTERS, RS_RING_REREAD = 0, 1, 2
+# rs_op
+RS_OP_SOFTMAX, RS_OP_RMSNORM, RS_OP_LAYERNORM = 0, 1, 2
 PATH_NAMES = {RS_PATH_AUTO: "auto", RS_PATH_ROWS: "rows", RS_PATH_CLUSTER: "cluster", RS_PATH_STREAM: "stream",
               RS_PATH_RING: "ring"}
 
@@ -38,6 +40,10 @@ EXPORTED = (
     "rowsoftmax_last_cuda_error",
     "rowsoftmax_device_status",
     "rowsoftmax_layout_owner",
+    "rmsnorm_fwd",
+    "layernorm_fwd",
+    "rownorm_fwd_ex",
+    "rownorm_plan",
 )
 
 
@@ -74,6 +80,7 @@ class rs_plan(ctypes.Structure):
         ("smem_bytes", ctypes.c_size_t),
         ("wait_limit_us", ctypes.c_int64),
         ("withhold_copies", ctypes.c_int),
+        ("op", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -125,6 +132,17 @@ def load() -> ctypes.CDLL:
         lib.rowsoftmax_device_status.restype = ci
         lib.rowsoftmax_layout_owner.argtypes = [i64, ci, ci, ctypes.POINTER(ci), ctypes.POINTER(i64)]
         lib.rowsoftmax_layout_owner.restype = ci
+        f64 = ctypes.c_double
+        lib.rmsnorm_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, f64, ci, vp]
+        lib.rmsnorm_fwd.restype = ci
+        lib.layernorm_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f64, ci, vp]
+        lib.layernorm_fwd.restype = ci
+        lib.rownorm_fwd_ex.argtypes = [ci, vp, vp, vp, vp, i64, i64, i64, i64, f64, ci, vp,
+                                       ctypes.POINTER(rs_options)]
+        lib.rownorm_fwd_ex.restype = ci
+        lib.rownorm_plan.argtypes = [ci, vp, vp, vp, vp, i64, i64, i64, i64, f64, ci, ctypes.POINTER(rs_options),
+                                     ctypes.POINTER(rs_device_info), ctypes.POINTER(rs_plan)]
+        lib.rownorm_plan.restype = ci
         _lib = lib
         return lib
 
@@ -187,3 +205,31 @@ def rowsoftmax_layout_owner(j: int, threads: int, vec: int) -> tuple[int, int, i
     s = ctypes.c_int64(0)
     rc = load().rowsoftmax_layout_owner(j, threads, vec, ctypes.byref(t), ctypes.byref(s))
     return rc, t.value, s.value
+
+
+def rmsnorm_fwd(in_ptr: int, out_ptr: int, weight_ptr: int | None, M: int, N: int, in_row_stride: int,
+                out_row_stride: int, eps: float, dtype: int, stream: int = 0) -> int:
+    return load().rmsnorm_fwd(in_ptr, out_ptr, weight_ptr, M, N, in_row_stride, out_row_stride, eps, dtype, stream)
+
+
+def layernorm_fwd(in_ptr: int, out_ptr: int, weight_ptr: int | None, bias_ptr: int | None, M: int, N: int,
+                  in_row_stride: int, out_row_stride: int, eps: float, dtype: int, stream: int = 0) -> int:
+    return load().layernorm_fwd(in_ptr, out_ptr, weight_ptr, bias_ptr, M, N, in_row_stride, out_row_stride, eps,
+                                dtype, stream)
+
+
+def rownorm_fwd_ex(op: int, in_ptr: int, out_ptr: int, weight_ptr: int | None, bias_ptr: int | None, M: int,
+                   N: int, in_row_stride: int, out_row_stride: int, eps: float, dtype: int, stream: int = 0,
+                   options=None) -> int:
+    return load().rownorm_fwd_ex(op, in_ptr, out_ptr, weight_ptr, bias_ptr, M, N, in_row_stride, out_row_stride,
+                                 eps, dtype, stream, _opts(options))
+
+
+def rownorm_plan(op: int, in_ptr: int, out_ptr: int, weight_ptr: int | None, bias_ptr: int | None, M: int, N: int,
+                 in_row_stride: int, out_row_stride: int, eps: float, dtype: int, options=None,
+                 device: rs_device_info | None = None) -> tuple[int, dict]:
+    plan = rs_plan()
+    dev = ctypes.pointer(device) if device is not None else None
+    rc = load().rownorm_plan(op, in_ptr, out_ptr, weight_ptr, bias_ptr, M, N, in_row_stride, out_row_stride, eps,
+                             dtype, _opts(options), dev, ctypes.byref(plan))
+    return rc, plan.as_dict()

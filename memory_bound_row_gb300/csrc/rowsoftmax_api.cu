@@ -45,8 +45,16 @@ bool valid_tpr(int tpr) {
     return tpr > 32 && tpr <= rs::kRowsMaxThreads && tpr % 32 == 0;
 }
 
-// The per-thread unit counts instantiated for (dtype, vec) and their number.
-const int* vpt_table(int dtype, int vec, int* n) {
+// The per-thread unit counts instantiated for (op, dtype, vec) and their number.
+const int* vpt_table(int op, int dtype, int vec, int* n) {
+    if (op != RS_OP_SOFTMAX) {
+        if (vec == 1) {
+            *n = (int)(sizeof(rs::kVptNormScalar) / sizeof(int));
+            return rs::kVptNormScalar;
+        }
+        *n = (int)(sizeof(rs::kVptNormVec) / sizeof(int));
+        return rs::kVptNormVec;
+    }
     if (vec == 1) {
         *n = (int)(sizeof(rs::kVptScalar) / sizeof(int));
         return rs::kVptScalar;
@@ -59,18 +67,18 @@ const int* vpt_table(int dtype, int vec, int* n) {
     return rs::kVptVec16;
 }
 
-bool vpt_instantiated(int dtype, int vec, int vpt) {
+bool vpt_instantiated(int op, int dtype, int vec, int vpt) {
     int n = 0;
-    const int* t = vpt_table(dtype, vec, &n);
+    const int* t = vpt_table(op, dtype, vec, &n);
     for (int i = 0; i < n; ++i)
         if (t[i] == vpt) return true;
     return false;
 }
 
 // Smallest instantiated count >= want, or 0.
-int vpt_at_least(int dtype, int vec, int64_t want) {
+int vpt_at_least(int op, int dtype, int vec, int64_t want) {
     int n = 0;
-    const int* t = vpt_table(dtype, vec, &n);
+    const int* t = vpt_table(op, dtype, vec, &n);
     for (int i = 0; i < n; ++i)
         if (t[i] >= want) return t[i];
     return 0;
@@ -81,7 +89,7 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
     int tpr = o.threads_per_row;
     int vpt = o.vec_per_thread;
     if (tpr && !valid_tpr(tpr)) return RS_ERR_INVALID_ARG;
-    if (vpt && !vpt_instantiated(dtype, vec, vpt)) return RS_ERR_NO_PATH;
+    if (vpt && !vpt_instantiated(p->op, dtype, vec, vpt)) return RS_ERR_NO_PATH;
     if (!tpr) {
         if (vpt) {
             const int64_t need = ceil_div(units, vpt);
@@ -93,7 +101,7 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
             }
         } else {
             int n_inst = 0;
-            const int* inst = vpt_table(dtype, vec, &n_inst);
+            const int* inst = vpt_table(p->op, dtype, vec, &n_inst);
             int vt = kRowsTargetValues / vec > 0 ? kRowsTargetValues / vec : 1;
             if (vt > inst[n_inst - 1]) vt = inst[n_inst - 1];
             // 16-bit rows that one warp can hold at up to 64 values a thread
@@ -111,7 +119,7 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
         if (tpr > rs::kRowsMaxThreads) return RS_ERR_NO_PATH;
     }
     if (!vpt) {
-        vpt = vpt_at_least(dtype, vec, ceil_div(units, tpr));
+        vpt = vpt_at_least(p->op, dtype, vec, ceil_div(units, tpr));
         if (!vpt) return RS_ERR_NO_PATH;
     }
     if ((int64_t)tpr * vpt < units) return RS_ERR_NO_PATH;
@@ -171,6 +179,7 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     if (o.stages && (o.stages < 2 || o.stages > rs::kRingMaxStages)) return RS_ERR_INVALID_ARG;
     if (o.ring_values < RS_RING_AUTO || o.ring_values > RS_RING_REREAD) return RS_ERR_INVALID_ARG;
     const int values = o.ring_values == RS_RING_AUTO ? RS_RING_REGISTERS : o.ring_values;
+    if (values == RS_RING_REREAD && p->op != RS_OP_SOFTMAX) return RS_ERR_NO_PATH;
     rs_options ro = o;
     ro.grid_limit = 0;
     int rc = plan_rows(dtype, vec, M, units, ro, p, values == RS_RING_REGISTERS);
@@ -317,13 +326,42 @@ int plan_wide(int dtype, int path, int vec, int64_t M, int64_t N, const rs_optio
     return RS_OK;
 }
 
-int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t ldi,
-                      int64_t ldo, int dtype, const rs_options* opts, const rs_device_info* dev,
-                      rs_plan* p) {
+// RS_PATH_STREAM for the normalisations: one CTA per row, a grid of a few
+// CTAs per SM looping over the rows.
+int plan_norm_stream(int vec, int64_t M, const rs_options& o, const rs_device_info& dev, rs_plan* p) {
+    if (o.cluster_size > 1 || o.threads_per_row || o.vec_per_thread) return RS_ERR_NO_PATH;
+    if (o.block_threads && o.block_threads != rs::kNormStreamThreads) return RS_ERR_NO_PATH;
+    int64_t grid = (int64_t)dev.sm_count * rs::kNormStreamCtasPerSm;
+    if (grid > M) grid = M;
+    if (o.grid_limit > 0 && grid > o.grid_limit) grid = o.grid_limit;
+    p->path = RS_PATH_STREAM;
+    p->vec_elems = vec;
+    p->threads_per_row = rs::kNormStreamThreads;
+    p->rows_per_cta = 1;
+    p->block_threads = rs::kNormStreamThreads;
+    p->cluster_size = 1;
+    p->grid = grid;
+    return RS_OK;
+}
+
+// Byte range [lo, lo + bytes) of `q` overlaps [r, r + rbytes)?
+bool ranges_overlap(uintptr_t q, uint64_t bytes, uintptr_t r, uint64_t rbytes) {
+    return q < r + rbytes && r < q + bytes;
+}
+
+int validate_and_plan_op(int op, const void* in, const void* out, const void* w, const void* b, int64_t M,
+                         int64_t N, int64_t ldi, int64_t ldo, double eps, int dtype, const rs_options* opts,
+                         const rs_device_info* dev, rs_plan* p) {
     memset(p, 0, sizeof(*p));
     p->dtype = dtype;
+    p->op = op;
+    if (op != RS_OP_SOFTMAX && op != RS_OP_RMSNORM && op != RS_OP_LAYERNORM) return RS_ERR_INVALID_ARG;
     if (dtype != RS_F32 && dtype != RS_F16 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED_DTYPE;
     if (M < 0 || N < 0) return RS_ERR_INVALID_ARG;
+    if (op == RS_OP_SOFTMAX && (w || b)) return RS_ERR_INVALID_ARG;
+    if (op == RS_OP_RMSNORM && b) return RS_ERR_INVALID_ARG;
+    // eps enters the kernels as a float: finite, >= 0, representable.
+    if (op != RS_OP_SOFTMAX && !(eps >= 0.0 && eps <= (double)3.402823466e38f)) return RS_ERR_INVALID_ARG;
     rs_options o;
     memset(&o, 0, sizeof(o));
     if (opts) o = *opts;
@@ -341,23 +379,28 @@ int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int
     if (!in || !out) return RS_ERR_INVALID_ARG;
     if (ldi < N || ldo < N) return RS_ERR_INVALID_ARG;
     const int es = elem_size(dtype);
-    const uintptr_t ai = (uintptr_t)in, ao = (uintptr_t)out;
-    if (ai % es || ao % es) return RS_ERR_INVALID_ARG;
+    const uintptr_t ai = (uintptr_t)in, ao = (uintptr_t)out, aw = (uintptr_t)w, ab = (uintptr_t)b;
+    if (ai % es || ao % es || aw % es || ab % es) return RS_ERR_INVALID_ARG;
     // Byte extent of each tensor: ((M-1)*ld + N) * es, checked for overflow.
     if ((M - 1) > (INT64_MAX / es - N) / ldi || (M - 1) > (INT64_MAX / es - N) / ldo)
         return RS_ERR_INVALID_ARG;
     const uint64_t ext_i = (uint64_t)(((M - 1) * ldi + N) * es);
     const uint64_t ext_o = (uint64_t)(((M - 1) * ldo + N) * es);
+    const uint64_t ext_v = (uint64_t)(N * es);  // a weight or bias vector
     if (ai > UINTPTR_MAX - ext_i || ao > UINTPTR_MAX - ext_o) return RS_ERR_INVALID_ARG;
-    const bool overlap = ai < ao + ext_o && ao < ai + ext_i;
-    if (overlap && !(ai == ao && ldi == ldo)) return RS_ERR_OVERLAP;
+    if ((w && aw > UINTPTR_MAX - ext_v) || (b && ab > UINTPTR_MAX - ext_v)) return RS_ERR_INVALID_ARG;
+    if (ranges_overlap(ai, ext_i, ao, ext_o) && !(ai == ao && ldi == ldo)) return RS_ERR_OVERLAP;
+    if ((w && ranges_overlap(aw, ext_v, ao, ext_o)) || (b && ranges_overlap(ab, ext_v, ao, ext_o)))
+        return RS_ERR_OVERLAP;
     if (!dev || dev->sm_count <= 0 || dev->max_smem_per_block_optin <= 0) return RS_ERR_INVALID_ARG;
 
     const int kvec = 16 / es;
     const bool strides_ok = M == 1 || (((ldi * es) % 16) == 0 && ((ldo * es) % 16) == 0);
-    const bool vec_ok = !o.force_scalar && ai % 16 == 0 && ao % 16 == 0 && strides_ok;
+    const bool vec_ok = !o.force_scalar && ai % 16 == 0 && ao % 16 == 0 && aw % 16 == 0 && ab % 16 == 0 &&
+                        strides_ok;
     const int vec = vec_ok ? kvec : 1;
     const int64_t units = ceil_div(N, vec);
+    const bool norm = op != RS_OP_SOFTMAX;
 
     int path = o.path;
     if (path == RS_PATH_AUTO) {
@@ -372,6 +415,7 @@ int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int
         if (N * es <= kRowsMaxRowBytes) rc = plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
+        if (norm) return plan_norm_stream(vec, M, o, *dev, p);
         if (vec_ok) {
             rc = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, p);
             if (rc == RS_OK) return RS_OK;
@@ -381,7 +425,14 @@ int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int
     }
     if (path == RS_PATH_ROWS) return plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
     if (path == RS_PATH_RING) return plan_ring(dtype, vec, M, N, units, o, *dev, p);
+    if (norm) return path == RS_PATH_STREAM ? plan_norm_stream(vec, M, o, *dev, p) : RS_ERR_NO_PATH;
     return plan_wide(dtype, path, vec, M, N, o, *dev, p);
+}
+
+int validate_and_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t ldi, int64_t ldo,
+                      int dtype, const rs_options* opts, const rs_device_info* dev, rs_plan* p) {
+    return validate_and_plan_op(RS_OP_SOFTMAX, in, out, nullptr, nullptr, M, N, ldi, ldo, 0.0, dtype, opts, dev,
+                                p);
 }
 
 std::mutex g_dev_mu;
@@ -492,15 +543,32 @@ int rowsoftmax_plan(const void* in, const void* out, int64_t M, int64_t N, int64
     return validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, opts, dev, plan);
 }
 
-int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
-                      int64_t out_row_stride, int dtype, cudaStream_t stream, const rs_options* opts) {
+int rownorm_plan(int op, const void* in, const void* out, const void* weight, const void* bias, int64_t M,
+                 int64_t N, int64_t in_row_stride, int64_t out_row_stride, double eps, int dtype,
+                 const rs_options* opts, const rs_device_info* dev, rs_plan* plan) {
+    if (!plan) return RS_ERR_INVALID_ARG;
+    if (op != RS_OP_RMSNORM && op != RS_OP_LAYERNORM) {
+        memset(plan, 0, sizeof(*plan));
+        return RS_ERR_INVALID_ARG;
+    }
+    return validate_and_plan_op(op, in, out, weight, bias, M, N, in_row_stride, out_row_stride, eps, dtype, opts,
+                                dev, plan);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validate, plan on the current device and launch one row operation.
+int run_op(int op, const void* in, void* out, const void* w, const void* b, int64_t M, int64_t N, int64_t ldi,
+           int64_t ldo, double eps, int dtype, cudaStream_t stream, const rs_options* opts) {
     // Shape and argument errors first: they need no device.
     rs_device_info probe;
     memset(&probe, 0, sizeof(probe));
     probe.sm_count = 1;
     probe.max_smem_per_block_optin = 1;
     rs_plan plan;
-    int rc = validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, nullptr, &probe, &plan);
+    int rc = validate_and_plan_op(op, in, out, w, b, M, N, ldi, ldo, eps, dtype, nullptr, &probe, &plan);
     if (rc != RS_OK && rc != RS_ERR_NO_PATH) return rc;
     if (M == 0 || N == 0) return RS_OK;
 
@@ -510,11 +578,13 @@ int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t i
     if (rc != RS_OK) return rc;
     if ((rc = check_device_pointer(in, dev)) != RS_OK) return rc;
     if ((rc = check_device_pointer(out, dev)) != RS_OK) return rc;
-    rc = validate_and_plan(in, out, M, N, in_row_stride, out_row_stride, dtype, opts, &info, &plan);
+    if (w && (rc = check_device_pointer(w, dev)) != RS_OK) return rc;
+    if (b && (rc = check_device_pointer(b, dev)) != RS_OK) return rc;
+    rc = validate_and_plan_op(op, in, out, w, b, M, N, ldi, ldo, eps, dtype, opts, &info, &plan);
     if (rc != RS_OK) return rc;
 
     const bool persistent_cluster = plan.path == RS_PATH_CLUSTER && plan.ring_values == RS_RING_REGISTERS;
-    if ((plan.path == RS_PATH_CLUSTER || plan.path == RS_PATH_STREAM) &&
+    if (op == RS_OP_SOFTMAX && (plan.path == RS_PATH_CLUSTER || plan.path == RS_PATH_STREAM) &&
         (plan.cluster_size > rs::kMaxClusterPortable || persistent_cluster)) {
         int n = 0;
         cudaError_t e = max_active_clusters_cached(dev, plan, &n);
@@ -530,23 +600,59 @@ int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t i
 
     cudaError_t e = cudaSuccess;
     const int n = (int)N;
-    if (plan.path == RS_PATH_ROWS) {
+    if (op != RS_OP_SOFTMAX) {
+        const rs::RowArgs a{w, b, (float)eps};
         switch (dtype) {
-            case RS_F32: e = rs::launch_rows_f32(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
-            case RS_F16: e = rs::launch_rows_f16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
-            default: e = rs::launch_rows_bf16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+            case RS_F32: e = rs::launch_norm_f32(plan, in, out, M, n, ldi, ldo, stream, a); break;
+            case RS_F16: e = rs::launch_norm_f16(plan, in, out, M, n, ldi, ldo, stream, a); break;
+            default: e = rs::launch_norm_bf16(plan, in, out, M, n, ldi, ldo, stream, a); break;
+        }
+    } else if (plan.path == RS_PATH_ROWS) {
+        switch (dtype) {
+            case RS_F32: e = rs::launch_rows_f32(plan, in, out, M, n, ldi, ldo, stream); break;
+            case RS_F16: e = rs::launch_rows_f16(plan, in, out, M, n, ldi, ldo, stream); break;
+            default: e = rs::launch_rows_bf16(plan, in, out, M, n, ldi, ldo, stream); break;
         }
     } else if (plan.path == RS_PATH_RING) {
         switch (dtype) {
-            case RS_F32: e = rs::launch_ring_f32(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
-            case RS_F16: e = rs::launch_ring_f16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
-            default: e = rs::launch_ring_bf16(plan, in, out, M, n, in_row_stride, out_row_stride, stream); break;
+            case RS_F32: e = rs::launch_ring_f32(plan, in, out, M, n, ldi, ldo, stream); break;
+            case RS_F16: e = rs::launch_ring_f16(plan, in, out, M, n, ldi, ldo, stream); break;
+            default: e = rs::launch_ring_bf16(plan, in, out, M, n, ldi, ldo, stream); break;
         }
     } else {
-        e = rs::launch_wide(plan, in, out, M, n, in_row_stride, out_row_stride, stream);
+        e = rs::launch_wide(plan, in, out, M, n, ldi, ldo, stream);
     }
     if (e != cudaSuccess) return fail_cuda(e);
     return RS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                      int64_t out_row_stride, int dtype, cudaStream_t stream, const rs_options* opts) {
+    return run_op(RS_OP_SOFTMAX, in, out, nullptr, nullptr, M, N, in_row_stride, out_row_stride, 0.0, dtype,
+                  stream, opts);
+}
+
+int rownorm_fwd_ex(int op, const void* in, void* out, const void* weight, const void* bias, int64_t M,
+                   int64_t N, int64_t in_row_stride, int64_t out_row_stride, double eps, int dtype,
+                   cudaStream_t stream, const rs_options* opts) {
+    if (op != RS_OP_RMSNORM && op != RS_OP_LAYERNORM) return RS_ERR_INVALID_ARG;
+    return run_op(op, in, out, weight, bias, M, N, in_row_stride, out_row_stride, eps, dtype, stream, opts);
+}
+
+int rmsnorm_fwd(const void* in, void* out, const void* weight, int64_t M, int64_t N, int64_t in_row_stride,
+                int64_t out_row_stride, double eps, int dtype, cudaStream_t stream) {
+    return rownorm_fwd_ex(RS_OP_RMSNORM, in, out, weight, nullptr, M, N, in_row_stride, out_row_stride, eps,
+                          dtype, stream, nullptr);
+}
+
+int layernorm_fwd(const void* in, void* out, const void* weight, const void* bias, int64_t M, int64_t N,
+                  int64_t in_row_stride, int64_t out_row_stride, double eps, int dtype, cudaStream_t stream) {
+    return rownorm_fwd_ex(RS_OP_LAYERNORM, in, out, weight, bias, M, N, in_row_stride, out_row_stride, eps,
+                          dtype, stream, nullptr);
 }
 
 int rowsoftmax_fwd(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
@@ -586,6 +692,9 @@ int rowsoftmax_device_status(unsigned int* flags, int clear) {
     if (e == cudaSuccess) e = rs::read_status_f32(flags, clear != 0);
     if (e == cudaSuccess) e = rs::read_status_f16(flags, clear != 0);
     if (e == cudaSuccess) e = rs::read_status_bf16(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_norm_f32(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_norm_f16(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_norm_bf16(flags, clear != 0);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return fail_cuda(e);

@@ -97,18 +97,53 @@ template <> struct Traits<RS_F16> {
 // ---------------------------------------------------------------------------
 // Access of one "unit" of VEC elements starting at element `base` of a row:
 // VEC == Traits::kVec is one 16-byte access (the caller guarantees alignment),
-// VEC == 1 is one element.  Units that run past n are filled with -inf on
-// load and clipped on store, element by element (masked tail).
+// VEC == 1 is one element.  Units that run past n are filled with `fill`
+// (-inf for the softmax max, 0 for sums) on load and clipped on store,
+// element by element (masked tail).
 // ---------------------------------------------------------------------------
 template <int DT, int VEC>
 __device__ __forceinline__ void load_unit(const typename Traits<DT>::storage* row, int base, int n,
-                                          float* v) {
+                                          float* v, float fill = kNegInf) {
     using T = Traits<DT>;
     if (VEC == T::kVec && base + VEC <= n) {
         T::unpack(__ldcs(reinterpret_cast<const uint4*>(row + base)), v);
     } else {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) v[e] = (base + e < n) ? T::load1(row + base + e) : kNegInf;
+        for (int e = 0; e < VEC; ++e) v[e] = (base + e < n) ? T::load1(row + base + e) : fill;
+    }
+}
+
+// One element of a read-only parameter vector (a weight or a bias), kept in
+// the caches: every row reads the same vector.
+template <int DT>
+__device__ __forceinline__ float load_param1(const typename Traits<DT>::storage* p) {
+    if constexpr (DT == RS_F32) {
+        return __ldg(p);
+    } else if constexpr (DT == RS_BF16) {
+        return __uint_as_float(((unsigned int)__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+    } else {
+        unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p));
+        return __half2float(*reinterpret_cast<__half*>(&b));
+    }
+}
+
+// The unit [base, base + VEC) of a parameter vector of n values; `dflt` for
+// a null vector and past n.
+template <int DT, int VEC>
+__device__ __forceinline__ void load_param_unit(const void* vec, int base, int n, float* f, float dflt) {
+    using T = Traits<DT>;
+    using S = typename T::storage;
+    if (!vec) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = dflt;
+        return;
+    }
+    const S* q = static_cast<const S*>(vec);
+    if (VEC == T::kVec && base + VEC <= n) {
+        T::unpack(__ldg(reinterpret_cast<const uint4*>(q + base)), f);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = (base + e < n) ? load_param1<DT>(q + base + e) : dflt;
     }
 }
 

@@ -21,6 +21,17 @@ constexpr int kVptVecF32[] = {RS_VPT_VEC_F32};
 constexpr int kVptVec16[] = {RS_VPT_VEC_16};
 constexpr int kVptScalar[] = {RS_VPT_SCALAR};
 
+// The normalisations (RMSNorm, LayerNorm) are instantiated for fewer counts.
+#define RS_VPT_NORM_VEC 1, 2, 3, 4, 6, 8
+#define RS_VPT_NORM_SCALAR 1, 2, 4, 8, 16
+constexpr int kVptNormVec[] = {RS_VPT_NORM_VEC};
+constexpr int kVptNormScalar[] = {RS_VPT_NORM_SCALAR};
+
+// The one-CTA-per-row streaming normalisation kernel: threads per CTA, and
+// CTAs per SM in the grid (few, so that the rows being re-read stay in L2).
+constexpr int kNormStreamThreads = 512;
+constexpr int kNormStreamCtasPerSm = 2;
+
 // Upper bound on fp32 values a thread holds in RS_PATH_ROWS (register budget).
 constexpr int kRowsMaxValuesPerThread = 64;
 constexpr int kRowsMaxThreads = 1024;
@@ -52,8 +63,24 @@ constexpr size_t kWideStaticSmem = 1024;  // upper bound of the kernel's static 
 constexpr int kWideHoldThreads = 512;     // max threads per CTA of the register-holding cluster kernel
 constexpr int kWideHoldMaxVpt = 8;        // units per thread it is instantiated for: 1, 2, 4, 8 (8: 256 threads)
 
+// Per-call parameters of a row operation: the normalisations' weight and
+// bias vectors (N stored values each, or null) and eps; zero for the softmax.
+struct RowArgs {
+    const void* w;
+    const void* b;
+    float eps;
+};
+
 // Launchers.  Each returns the CUDA error of the launch (cudaSuccess if it
 // was enqueued).  Arguments were validated and planned by the caller.
+// Normalisations: plan.op selects RMSNorm or LayerNorm; plan.path RS_PATH_ROWS,
+// RS_PATH_RING or RS_PATH_STREAM (one CTA per row, reads the row 2 or 3 times).
+cudaError_t launch_norm_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                            int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t launch_norm_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                            int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t launch_norm_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                             int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_rows_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
                             int64_t ldi, int64_t ldo, cudaStream_t s);
 cudaError_t launch_rows_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
@@ -79,5 +106,8 @@ cudaError_t read_status_f32(unsigned int* flags, bool clear);
 cudaError_t read_status_f16(unsigned int* flags, bool clear);
 cudaError_t read_status_bf16(unsigned int* flags, bool clear);
 cudaError_t read_status_wide(unsigned int* flags, bool clear);
+cudaError_t read_status_norm_f32(unsigned int* flags, bool clear);
+cudaError_t read_status_norm_f16(unsigned int* flags, bool clear);
+cudaError_t read_status_norm_bf16(unsigned int* flags, bool clear);
 
 }  // namespace rs

@@ -1,5 +1,6 @@
-// RS_PATH_RING: persistent single-pass row softmax whose input rows are
-// staged through a ring of shared-memory stages by bulk asynchronous copies.
+// RS_PATH_RING: persistent single-pass row operation (softmax, RMSNorm,
+// LayerNorm) whose input rows are staged through a ring of shared-memory
+// stages by bulk asynchronous copies.
 //
 // The arithmetic is that of RS_PATH_ROWS (rs_rows.cuh): one group of `tpr`
 // threads per row, the row in registers as 16-byte group-cyclic units, a
@@ -38,23 +39,25 @@ namespace rs {
 // exp twice per element: fewer registers, so more CTAs and warps per SM.
 template <int DT, int VPT, bool HOLD>
 __device__ __forceinline__ void ring_unit(const unsigned char* srow, const typename Traits<DT>::storage* grow,
-                                          int u, int units_full, int N, bool active, float* f) {
+                                          int u, int units_full, int N, bool active, float* f,
+                                          float fill = kNegInf) {
     constexpr int VEC = Traits<DT>::kVec;
     if (active && u < units_full) {
         Traits<DT>::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)u * 16), f);
     } else if (active && u * VEC < N) {
-        load_unit<DT, VEC>(grow, u * VEC, N, f);
+        load_unit<DT, VEC>(grow, u * VEC, N, f, fill);
     } else {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) f[e] = kNegInf;
+        for (int e = 0; e < VEC; ++e) f[e] = fill;
     }
 }
 
-template <int DT, int VPT, bool HOLD>
+template <int DT, int VPT, bool HOLD, typename OP>
 __global__ void __launch_bounds__(HOLD ? rows_block_limit(VPT, Traits<DT>::kVec) : kRingRereadThreads,
                                   HOLD ? 1 : kRingRereadMinCtas)
 ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, int stages,
-            uint64_t wait_ns, int withhold) {
+            uint64_t wait_ns, int withhold, RowArgs args) {
+    static_assert(HOLD || OP::kOp == RS_OP_SOFTMAX, "the re-read variant is the softmax's only");
     using T = Traits<DT>;
     using S = typename T::storage;
     constexpr int VEC = T::kVec;
@@ -118,7 +121,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         const unsigned char* srow = ring + (size_t)s * stage_bytes + (size_t)grp * slot;
         const S* grow = in + (active ? row : 0) * ldi;
 
-        if (HOLD) {
+        if constexpr (HOLD) {
             float v[VPT][VEC];
             if (active && (t + (VPT - 1) * tpr) < units_full) {
 #pragma unroll
@@ -127,10 +130,11 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
             } else {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k)
-                    ring_unit<DT, VPT, HOLD>(srow, grow, t + k * tpr, units_full, N, active, v[k]);
+                    ring_unit<DT, VPT, HOLD>(srow, grow, t + k * tpr, units_full, N, active, v[k], OP::kFill);
             }
-            const float c = row_exp_and_scale<VPT, VEC>(v, tpr, part[it & 1]);
-            if (active && !abort) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v, c);
+            const bool whole = (t + (VPT - 1) * tpr + 1) * VEC <= N;
+            OP::template apply<DT, VEC, VPT>(v, t, tpr, N, whole, args, part[it & 1]);
+            if (active && !abort) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v);
         } else {
             float f[VEC];
             float m = kNegInf;
@@ -218,10 +222,10 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
     }
 }
 
-template <int DT, int VPT, bool HOLD>
+template <int DT, int VPT, bool HOLD, typename OP>
 cudaError_t launch_ring_one(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
-                            int64_t ldo, cudaStream_t s) {
-    auto kern = ring_kernel<DT, VPT, HOLD>;
+                            int64_t ldo, cudaStream_t s, const RowArgs& a) {
+    auto kern = ring_kernel<DT, VPT, HOLD, OP>;
     // The dynamic shared-memory ceiling is a per-device attribute: raise it to
     // the device maximum once per device for this instance.
     static std::mutex mu;
@@ -244,29 +248,33 @@ cudaError_t launch_ring_one(const rs_plan& p, const void* in, void* out, int64_t
     }
     const uint64_t wait_ns = p.wait_limit_us > 0 ? (uint64_t)p.wait_limit_us * 1000ull : kWaitLimitNs;
     kern<<<(unsigned)p.grid, p.block_threads, p.smem_bytes, s>>>(in, out, M, N, ldi, ldo, p.threads_per_row,
-                                                                 p.stages, wait_ns, p.withhold_copies);
+                                                                 p.stages, wait_ns, p.withhold_copies, a);
     return cudaGetLastError();
 }
 
-template <int DT, int... Vs>
+template <int DT, typename OP, int... Vs>
 struct RingDispatch;
 
-template <int DT>
-struct RingDispatch<DT> {
-    static cudaError_t go(const rs_plan&, const void*, void*, int64_t, int, int64_t, int64_t, cudaStream_t) {
+template <int DT, typename OP>
+struct RingDispatch<DT, OP> {
+    static cudaError_t go(const rs_plan&, const void*, void*, int64_t, int, int64_t, int64_t, cudaStream_t,
+                          const RowArgs&) {
         return cudaErrorInvalidConfiguration;
     }
 };
 
-template <int DT, int V0, int... Vs>
-struct RingDispatch<DT, V0, Vs...> {
+template <int DT, typename OP, int V0, int... Vs>
+struct RingDispatch<DT, OP, V0, Vs...> {
     static cudaError_t go(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
-                          int64_t ldo, cudaStream_t s) {
+                          int64_t ldo, cudaStream_t s, const RowArgs& a) {
         if (p.vec_per_thread == V0) {
-            if (p.ring_values == RS_RING_REREAD) return launch_ring_one<DT, V0, false>(p, in, out, M, N, ldi, ldo, s);
-            return launch_ring_one<DT, V0, true>(p, in, out, M, N, ldi, ldo, s);
+            if constexpr (OP::kOp == RS_OP_SOFTMAX) {
+                if (p.ring_values == RS_RING_REREAD)
+                    return launch_ring_one<DT, V0, false, OP>(p, in, out, M, N, ldi, ldo, s, a);
+            }
+            return launch_ring_one<DT, V0, true, OP>(p, in, out, M, N, ldi, ldo, s, a);
         }
-        return RingDispatch<DT, Vs...>::go(p, in, out, M, N, ldi, ldo, s);
+        return RingDispatch<DT, OP, Vs...>::go(p, in, out, M, N, ldi, ldo, s, a);
     }
 };
 

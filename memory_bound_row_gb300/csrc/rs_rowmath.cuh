@@ -1,6 +1,8 @@
 // The per-row arithmetic shared by RS_PATH_ROWS and RS_PATH_RING: a row is
 // held in registers by the `tpr` threads of a row group, as VPT units of
-// VEC fp32 values per thread (-inf where the row has no element).
+// VEC fp32 values per thread (a fill value where the row has no element).
+// The softmax below; RMSNorm and LayerNorm at the end, as row operations of
+// the same engine.
 //
 // Three-level reduction as in the nano-triton post ("Reductions and
 // broadcasting"): registers, then __shfl_xor_sync butterflies inside the
@@ -13,6 +15,7 @@
 #pragma once
 
 #include "rs_common.cuh"
+#include "rs_internal.h"
 
 namespace rs {
 
@@ -62,10 +65,10 @@ __device__ __forceinline__ float row_exp_and_scale(float (&v)[VPT][VEC], int tpr
 
 // Loads the thread's units t, t + tpr, ... of a row from global memory
 // (16-byte units when VEC is the 16-byte width, else single elements);
-// whole units take the branch-free path.
+// whole units take the branch-free path; `fill` stands for absent elements.
 template <int DT, int VEC, int VPT>
 __device__ __forceinline__ void load_row_units(const typename Traits<DT>::storage* row, int t, int tpr, int n,
-                                               bool active, float (&v)[VPT][VEC]) {
+                                               bool active, float (&v)[VPT][VEC], float fill = kNegInf) {
     if (active && (t + (VPT - 1) * tpr + 1) * VEC <= n) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -77,23 +80,19 @@ __device__ __forceinline__ void load_row_units(const typename Traits<DT>::storag
         }
     } else if (active) {
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) load_unit<DT, VEC>(row, (t + k * tpr) * VEC, n, v[k]);
+        for (int k = 0; k < VPT; ++k) load_unit<DT, VEC>(row, (t + k * tpr) * VEC, n, v[k], fill);
     } else {
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] = kNegInf;
+            for (int e = 0; e < VEC; ++e) v[k][e] = fill;
     }
 }
 
-// Stores v * c to the thread's units of a row.
+// Stores v to the thread's units of a row (rounded to the storage type).
 template <int DT, int VEC, int VPT>
 __device__ __forceinline__ void store_row_units(typename Traits<DT>::storage* row, int t, int tpr, int n,
-                                                float (&v)[VPT][VEC], float c) {
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+                                                const float (&v)[VPT][VEC]) {
     if ((t + (VPT - 1) * tpr + 1) * VEC <= n) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -108,5 +107,125 @@ __device__ __forceinline__ void store_row_units(typename Traits<DT>::storage* ro
         for (int k = 0; k < VPT; ++k) store_unit<DT, VEC>(row, (t + k * tpr) * VEC, n, v[k]);
     }
 }
+
+// Stores v * c (the softmax's scaled values).
+template <int DT, int VEC, int VPT>
+__device__ __forceinline__ void store_row_units(typename Traits<DT>::storage* row, int t, int tpr, int n,
+                                                float (&v)[VPT][VEC], float c) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+    store_row_units<DT, VEC, VPT>(row, t, tpr, n, v);
+}
+
+// ---------------------------------------------------------------------------
+// Row operations.  Each turns the thread's loaded units v (with kFill where the
+// row has no element) into the values to store, cooperating with the other
+// threads of the row through warp butterflies and, for rows wider than a warp,
+// the per-warp pairs `part` (one CTA barrier per reduction).
+// ---------------------------------------------------------------------------
+// Sum over the threads of a row; SLOT picks the half of the per-warp pair.
+template <int SLOT>
+__device__ __forceinline__ float row_sum(float s, int tpr, float2* part) {
+    const int width = tpr < 32 ? tpr : 32;
+    s = group_sum(s, width);
+    if (tpr <= 32) return s;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int wpr = tpr >> 5;
+    if (lane == 0) {
+        if (SLOT == 0) part[warp].x = s; else part[warp].y = s;
+    }
+    __syncthreads();
+    const int w0 = (warp / wpr) * wpr;
+    float p = 0.0f;
+    if (lane < wpr) p = SLOT == 0 ? part[w0 + lane].x : part[w0 + lane].y;
+    return __shfl_sync(0xffffffffu, group_sum(p, pow2_ceil(wpr)), 0);
+}
+
+struct OpSoftmax {
+    static constexpr int kOp = RS_OP_SOFTMAX;
+    static constexpr float kFill = kNegInf;
+    template <int DT, int VEC, int VPT>
+    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int, int tpr, int, bool, const RowArgs&,
+                                                 float2* part) {
+        const float c = row_exp_and_scale<VPT, VEC>(v, tpr, part);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+    }
+};
+
+// RMSNorm ("Reference Kernel: RMSNorm", Hugging Face "triton-kernels" skill
+// page): y = x * rsqrt(sum(x^2)/N + eps) * w, accumulated in fp32.
+struct OpRmsNorm {
+    static constexpr int kOp = RS_OP_RMSNORM;
+    static constexpr float kFill = 0.0f;  // absent elements add nothing to the sum of squares
+    template <int DT, int VEC, int VPT>
+    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool,
+                                                 const RowArgs& a, float2* part) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) s = fmaf(v[k][e], v[k][e], s);
+        s = row_sum<0>(s, tpr, part);
+        const float r = 1.0f / sqrtf(s / (float)n + a.eps);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            float w[VEC];
+            load_param_unit<DT, VEC>(a.w, (t + k * tpr) * VEC, n, w, 1.0f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[k][e] = v[k][e] * r * w[e];
+        }
+    }
+};
+
+// LayerNorm: y = (x - mean) * rsqrt(var + eps) * w + b, population variance,
+// the two moments reduced one after the other (two passes over registers).
+struct OpLayerNorm {
+    static constexpr int kOp = RS_OP_LAYERNORM;
+    static constexpr float kFill = 0.0f;
+    template <int DT, int VEC, int VPT>
+    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool whole,
+                                                 const RowArgs& a, float2* part) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) s += v[k][e];
+        const float mean = row_sum<0>(s, tpr, part) / (float)n;
+        float d = 0.0f;
+        if (whole) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float x = v[k][e] - mean;
+                    d = fmaf(x, x, d);
+                }
+        } else {  // absent elements hold 0, not the mean: leave them out
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float x = v[k][e] - mean;
+                    if ((t + k * tpr) * VEC + e < n) d = fmaf(x, x, d);
+                }
+        }
+        const float var = row_sum<1>(d, tpr, part) / (float)n;
+        const float r = 1.0f / sqrtf(var + a.eps);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            float w[VEC], b[VEC];
+            load_param_unit<DT, VEC>(a.w, (t + k * tpr) * VEC, n, w, 1.0f);
+            load_param_unit<DT, VEC>(a.b, (t + k * tpr) * VEC, n, b, 0.0f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[k][e] = fmaf((v[k][e] - mean) * r, w[e], b[e]);
+        }
+    }
+};
 
 }  // namespace rs

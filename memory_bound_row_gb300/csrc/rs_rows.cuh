@@ -1,4 +1,5 @@
-// RS_PATH_ROWS: single-pass row softmax with the whole row in registers.
+// RS_PATH_ROWS: single-pass row operation (softmax, RMSNorm, LayerNorm) with
+// the whole row in registers.
 //
 // This is the fused kernel of "stanleyjacob.dev: Triton", Part II, "Worked
 // example: fused softmax" (one pass: load the row with -inf in masked lanes,
@@ -23,54 +24,55 @@
 
 namespace rs {
 
-template <int DT, int VEC, int VPT>
+template <int DT, int VEC, int VPT, typename OP>
 __global__ void __launch_bounds__(rows_block_limit(VPT, VEC))
-rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr) {
+rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, RowArgs args) {
     using S = typename Traits<DT>::storage;
     const S* in = static_cast<const S*>(in_);
     S* out = static_cast<S*>(out_);
-    __shared__ float2 part[2][32];  // per-warp (m, l), double-buffered over row iterations
+    __shared__ float2 part[2][32];  // per-warp partials, double-buffered over row iterations
 
     const int rows_per_cta = blockDim.x / tpr;
     const int grp = threadIdx.x / tpr;
     const int t = threadIdx.x - grp * tpr;
+    const bool whole = (t + (VPT - 1) * tpr + 1) * VEC <= N;  // all of this thread's units lie in the row
 
     int it = 0;
     for (int64_t rb = blockIdx.x; rb * rows_per_cta < M; rb += gridDim.x, ++it) {
         const int64_t row = rb * rows_per_cta + grp;
         const bool active = row < M;
         float v[VPT][VEC];
-        load_row_units<DT, VEC, VPT>(in + (active ? row : 0) * ldi, t, tpr, N, active, v);
-        const float c = row_exp_and_scale<VPT, VEC>(v, tpr, part[it & 1]);
-        if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v, c);
+        load_row_units<DT, VEC, VPT>(in + (active ? row : 0) * ldi, t, tpr, N, active, v, OP::kFill);
+        OP::template apply<DT, VEC, VPT>(v, t, tpr, N, whole, args, part[it & 1]);
+        if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v);
     }
 }
 
-template <int DT, int VEC, int VPT>
+template <int DT, int VEC, int VPT, typename OP>
 cudaError_t launch_rows_one(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                            int64_t ldi, int64_t ldo, cudaStream_t s) {
-    rows_kernel<DT, VEC, VPT><<<(unsigned)p.grid, p.block_threads, 0, s>>>(in, out, M, N, ldi, ldo,
-                                                                         p.threads_per_row);
+                            int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a) {
+    rows_kernel<DT, VEC, VPT, OP><<<(unsigned)p.grid, p.block_threads, 0, s>>>(in, out, M, N, ldi, ldo,
+                                                                             p.threads_per_row, a);
     return cudaGetLastError();
 }
 
-template <int DT, int VEC, int... Vs>
+template <int DT, int VEC, typename OP, int... Vs>
 struct RowsDispatch;
 
-template <int DT, int VEC>
-struct RowsDispatch<DT, VEC> {
-    static cudaError_t go(const rs_plan&, const void*, void*, int64_t, int, int64_t, int64_t,
-                          cudaStream_t) {
+template <int DT, int VEC, typename OP>
+struct RowsDispatch<DT, VEC, OP> {
+    static cudaError_t go(const rs_plan&, const void*, void*, int64_t, int, int64_t, int64_t, cudaStream_t,
+                          const RowArgs&) {
         return cudaErrorInvalidConfiguration;
     }
 };
 
-template <int DT, int VEC, int V0, int... Vs>
-struct RowsDispatch<DT, VEC, V0, Vs...> {
-    static cudaError_t go(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                          int64_t ldi, int64_t ldo, cudaStream_t s) {
-        if (p.vec_per_thread == V0) return launch_rows_one<DT, VEC, V0>(p, in, out, M, N, ldi, ldo, s);
-        return RowsDispatch<DT, VEC, Vs...>::go(p, in, out, M, N, ldi, ldo, s);
+template <int DT, int VEC, typename OP, int V0, int... Vs>
+struct RowsDispatch<DT, VEC, OP, V0, Vs...> {
+    static cudaError_t go(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                          int64_t ldo, cudaStream_t s, const RowArgs& a) {
+        if (p.vec_per_thread == V0) return launch_rows_one<DT, VEC, V0, OP>(p, in, out, M, N, ldi, ldo, s, a);
+        return RowsDispatch<DT, VEC, OP, Vs...>::go(p, in, out, M, N, ldi, ldo, s, a);
     }
 };
 

@@ -7,16 +7,16 @@ namespace rs {
 cudaError_t launch_rows_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
                             int64_t ldi, int64_t ldo, cudaStream_t s) {
     if (p.vec_elems == Traits<RS_F32>::kVec)
-        return RowsDispatch<RS_F32, Traits<RS_F32>::kVec, RS_VPT_VEC_F32>::go(p, in, out, M, N, ldi, ldo, s);
+        return RowsDispatch<RS_F32, Traits<RS_F32>::kVec, OpSoftmax, RS_VPT_VEC_F32>::go(p, in, out, M, N, ldi, ldo, s, RowArgs{});
     if (p.vec_elems == 1)
-        return RowsDispatch<RS_F32, 1, RS_VPT_SCALAR>::go(p, in, out, M, N, ldi, ldo, s);
+        return RowsDispatch<RS_F32, 1, OpSoftmax, RS_VPT_SCALAR>::go(p, in, out, M, N, ldi, ldo, s, RowArgs{});
     return cudaErrorInvalidConfiguration;
 }
 
 cudaError_t launch_ring_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
                             int64_t ldi, int64_t ldo, cudaStream_t s) {
     if (p.vec_elems != Traits<RS_F32>::kVec) return cudaErrorInvalidConfiguration;
-    return RingDispatch<RS_F32, RS_VPT_VEC_F32>::go(p, in, out, M, N, ldi, ldo, s);
+    return RingDispatch<RS_F32, OpSoftmax, RS_VPT_VEC_F32>::go(p, in, out, M, N, ldi, ldo, s, RowArgs{});
 }
 
 cudaError_t read_status_f32(unsigned int* flags, bool clear) { return read_unit_status(flags, clear); }

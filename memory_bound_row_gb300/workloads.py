@@ -1,8 +1,9 @@
-"""Seeded synthetic inputs for the row softmax: the five benchmark workloads
-and the extra shapes used by the tests.
+"""Seeded synthetic inputs for the row softmax and the row normalisations:
+the five benchmark workloads, the extra shapes used by the tests and the
+normalisations' weight and bias vectors.
 
-This module only makes input data; it contains none of the softmax
-arithmetic.  Values are a pure function of (seed, stream, flat index): a
+This module only makes input data; it contains none of the softmax or
+normalisation arithmetic.  Values are a pure function of (seed, stream, flat index): a
 SplitMix64 hash of the counter gives uniforms on (0, 1), and the Box-Muller
 transform (cosine branch) turns two uniforms into one standard normal.  Any
 subset of rows can therefore be generated on its own and equals the same rows
@@ -18,6 +19,11 @@ Workloads (rows x cols, storage type, distribution):
   fp16_512x131072     fp16 512 x 131072, N(0, var 2), one +15 spike per row
   bf16_causal_16x32x2048  bf16 [16, 32, 2048, 2048] attention scores viewed as
                       1048576 x 2048, N(0, 1)/sqrt(128), -inf where col > row mod 2048
+
+The normalisations run on the same shapes and recipes, except that the causal
+scores' -inf entries (which make every normalised row NaN) are left out: that
+workload becomes N(0, 1)/sqrt(128) everywhere (norm_workload).  Weight
+vectors are 1 + N(0, 1)/4 and bias vectors N(0, 1)/2 (norm_params).
 """
 from __future__ import annotations
 
@@ -150,6 +156,10 @@ def _values(w: Workload, rows: torch.Tensor, cols: torch.Tensor) -> torch.Tensor
     if w.kind == "causal_scores":
         v = normal(flat, w.seed, 0) / math.sqrt(128.0)
         return torch.where(c > (r % 2048), -math.inf, v)
+    if w.kind == "scores_unmasked":
+        return normal(flat, w.seed, 0) / math.sqrt(128.0)
+    if w.kind == "offset50":  # a large common offset: N(50, 1)
+        return 50.0 + normal(flat, w.seed, 0)
     raise ValueError(f"unknown recipe {w.kind}")
 
 
@@ -176,3 +186,24 @@ def generate_rows(w: Workload, rows: torch.Tensor, device="cpu") -> torch.Tensor
     rows = rows.to(device=device, dtype=torch.int64)
     cols = torch.arange(w.N, dtype=torch.int64, device=device)
     return _values(w, rows, cols).to(torch.float32).to(w.torch_dtype)
+
+
+def norm_workload(name: str) -> Workload:
+    """Benchmark workload `name` as the normalisations use it (the causal
+    scores without their -inf mask)."""
+    w = WORKLOADS[name]
+    if w.kind == "causal_scores":
+        return Workload(w.name, w.dtype, w.M, w.N, w.ld, w.seed, "scores_unmasked",
+                        w.description.replace(", -inf above the diagonal", "").replace(
+                            ", -inf where col > row mod 2048", "") + ", unmasked")
+    return w
+
+
+def norm_params(N: int, dtype: str, seed: int = 0, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+    """Weight (1 + N(0,1)/4) and bias (N(0,1)/2) vectors of N values in the
+    storage type `dtype`, seeded."""
+    td = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    idx = torch.arange(N, dtype=torch.int64, device=device)
+    w = 1.0 + 0.25 * normal(idx, seed, 10)
+    b = 0.5 * normal(idx, seed, 11)
+    return w.to(torch.float32).to(td), b.to(torch.float32).to(td)

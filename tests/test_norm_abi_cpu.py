@@ -1,0 +1,146 @@
+"""CPU checks of the row normalisations' C entry points (rmsnorm_fwd,
+layernorm_fwd, rownorm_fwd_ex, rownorm_plan): argument validation before any
+device call, and the launches the planner picks.  No kernel runs."""
+import pytest
+
+import memory_bound_row_gb300 as rs
+from memory_bound_row_gb300 import build
+
+from test_abi_cpu import gb300
+
+A = 1 << 20            # 16-byte aligned fake addresses; validation fails before they are used
+OUT = A + (1 << 40)
+W = A + (1 << 41)
+B = A + (1 << 42)
+NORM_VPT_VEC = {1, 2, 3, 4, 6, 8}
+NORM_VPT_SCALAR = {1, 2, 4, 8, 16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _plan(op, M, N, dtype, ld=None, opts=None, a=A, o=OUT, w=W, b=None, eps=1e-5):
+    rc, plan = rs.rownorm_plan(op, a, o, w, b, M, N, ld or N, ld or N, eps, dtype, opts, gb300())
+    assert rc == rs.RS_OK, rs.rowsoftmax_status_string(rc)
+    return plan
+
+
+def _covers(plan, N):
+    units = -(-N // plan["vec_elems"])
+    if plan["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING):
+        return plan["threads_per_row"] * plan["vec_per_thread"] >= units
+    return plan["path"] == rs.RS_PATH_STREAM and plan["cluster_size"] == 1
+
+
+@pytest.mark.parametrize(
+    "op,b,eps,status",
+    [
+        (rs.RS_OP_SOFTMAX, None, 1e-5, rs.RS_ERR_INVALID_ARG),      # not a normalisation
+        (7, None, 1e-5, rs.RS_ERR_INVALID_ARG),
+        (rs.RS_OP_RMSNORM, B, 1e-5, rs.RS_ERR_INVALID_ARG),         # RMSNorm has no bias
+        (rs.RS_OP_RMSNORM, None, -1e-6, rs.RS_ERR_INVALID_ARG),
+        (rs.RS_OP_LAYERNORM, None, float("nan"), rs.RS_ERR_INVALID_ARG),
+        (rs.RS_OP_LAYERNORM, B, float("inf"), rs.RS_ERR_INVALID_ARG),
+        (rs.RS_OP_LAYERNORM, B, 1e39, rs.RS_ERR_INVALID_ARG),       # not a finite float
+        (rs.RS_OP_LAYERNORM, B, 0.0, rs.RS_OK),
+        (rs.RS_OP_RMSNORM, None, 1e-6, rs.RS_OK),
+    ],
+)
+def test_op_bias_and_eps_are_validated(op, b, eps, status):
+    rc, plan = rs.rownorm_plan(op, A, OUT, W, b, 64, 1024, 1024, 1024, eps, rs.RS_F32, None, gb300())
+    assert rc == status
+    assert rs.rownorm_fwd_ex(op, A, OUT, W, b, 64, 1024, 1024, 1024, eps, rs.RS_F32, 0, None) == (
+        status if status != rs.RS_OK else rs.rownorm_fwd_ex(op, A, OUT, W, b, 64, 1024, 1024, 1024, eps,
+                                                            rs.RS_F32, 0, None))
+    if status == rs.RS_OK:
+        assert plan["op"] == op
+
+
+@pytest.mark.parametrize(
+    "w,b,status",
+    [
+        (OUT + 64, None, rs.RS_ERR_OVERLAP),          # weight inside the output
+        (None, OUT + 4096 * 4 - 8, rs.RS_ERR_OVERLAP),  # bias straddles the output's end
+        (OUT - 1024 * 4 + 4, None, rs.RS_ERR_OVERLAP),  # weight's last value is the output's first
+        (OUT - 1024 * 4, None, rs.RS_OK),             # ends where the output starts
+        (A + 64, None, rs.RS_OK),                     # inside the input: read-only, allowed
+        (W + 2, None, rs.RS_ERR_INVALID_ARG),         # not element-aligned
+        (None, B + 1, rs.RS_ERR_INVALID_ARG),
+    ],
+)
+def test_weight_and_bias_pointers_are_validated(w, b, status):
+    rc, _ = rs.rownorm_plan(rs.RS_OP_LAYERNORM, A, OUT, w, b, 4, 1024, 1024, 1024, 1e-5, rs.RS_F32, None,
+                            gb300())
+    assert rc == status
+    if status != rs.RS_OK:  # rejected before any device call
+        assert rs.layernorm_fwd(A, OUT, w, b, 4, 1024, 1024, 1024, 1e-5, rs.RS_F32, 0) == status
+
+
+def test_shape_errors_match_the_softmax():
+    for args, status in [((A, OUT, -1, 8, 8, 8), rs.RS_ERR_INVALID_ARG),
+                         ((A, OUT, 4, 8, 7, 8), rs.RS_ERR_INVALID_ARG),
+                         ((A, A + 64, 4, 8, 8, 8), rs.RS_ERR_OVERLAP),
+                         ((0, OUT, 4, 8, 8, 8), rs.RS_ERR_INVALID_ARG)]:
+        assert rs.rmsnorm_fwd(args[0], args[1], None, *args[2:], 1e-6, rs.RS_F32, 0) == status
+        assert rs.rmsnorm_fwd(args[0], args[1], None, *args[2:], 1e-6, 9, 0) == rs.RS_ERR_UNSUPPORTED_DTYPE
+    assert rs.rmsnorm_fwd(0, 0, None, 0, 8, 8, 8, 1e-6, rs.RS_F32, 0) == rs.RS_OK  # empty: no-op
+    assert rs.layernorm_fwd(0, 0, None, None, 8, 0, 0, 0, 1e-5, rs.RS_BF16, 0) == rs.RS_OK
+
+
+def test_plans_for_typical_hidden_sizes():
+    # 16-bit rows between 512 B and 32 KB: the bulk-copy ring, holding the row in registers
+    for op in (rs.RS_OP_RMSNORM, rs.RS_OP_LAYERNORM):
+        p = _plan(op, 32768, 8192, rs.RS_BF16)
+        assert p["path"] == rs.RS_PATH_RING and p["ring_values"] == rs.RS_RING_REGISTERS and _covers(p, 8192)
+        assert p["vec_per_thread"] in NORM_VPT_VEC
+        p = _plan(op, 8192, 5000, rs.RS_F32, ld=5120)   # fp32: register rows
+        assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 4 and _covers(p, 5000)
+        p = _plan(op, 512, 131072, rs.RS_F16)          # wide rows: one streaming CTA per row
+        assert p["path"] == rs.RS_PATH_STREAM and p["grid"] == 2 * 152 and p["vec_elems"] == 8
+        p = _plan(op, 100, 131072, rs.RS_F16)
+        assert p["grid"] == 100
+
+
+def test_misaligned_parameter_vectors_select_element_wise_kernels():
+    p = _plan(rs.RS_OP_RMSNORM, 64, 4096, rs.RS_BF16, w=W + 2)
+    assert p["vec_elems"] == 1 and p["path"] == rs.RS_PATH_ROWS and p["vec_per_thread"] in NORM_VPT_SCALAR
+    p = _plan(rs.RS_OP_LAYERNORM, 64, 4096, rs.RS_F32, w=W, b=B + 4)
+    assert p["vec_elems"] == 1
+    p = _plan(rs.RS_OP_LAYERNORM, 64, 4096, rs.RS_F32, w=None, b=None)
+    assert p["vec_elems"] == 4
+
+
+def test_paths_without_a_normalisation_kernel():
+    for opts in [{"path": rs.RS_PATH_CLUSTER},
+                 {"path": rs.RS_PATH_RING, "ring_values": rs.RS_RING_REREAD},
+                 {"path": rs.RS_PATH_STREAM, "cluster_size": 2}]:
+        rc, _ = rs.rownorm_plan(rs.RS_OP_RMSNORM, A, OUT, W, None, 64, 4096, 4096, 4096, 1e-6, rs.RS_BF16,
+                                opts, gb300())
+        assert rc == rs.RS_ERR_NO_PATH, opts
+    p = _plan(rs.RS_OP_RMSNORM, 64, 4096, rs.RS_BF16, opts={"path": rs.RS_PATH_STREAM})
+    assert p["path"] == rs.RS_PATH_STREAM
+    p = _plan(rs.RS_OP_LAYERNORM, 64, 4096, rs.RS_F32, opts={"path": rs.RS_PATH_ROWS, "threads_per_row": 128,
+                                                              "vec_per_thread": 8})
+    assert (p["threads_per_row"], p["vec_per_thread"]) == (128, 8)
+    rc, _ = rs.rownorm_plan(rs.RS_OP_LAYERNORM, A, OUT, W, None, 64, 4096, 4096, 4096, 1e-6, rs.RS_F32,
+                            {"path": rs.RS_PATH_ROWS, "threads_per_row": 128, "vec_per_thread": 10}, gb300())
+    assert rc == rs.RS_ERR_NO_PATH  # 10 units a thread is a softmax-only instance
+
+
+@pytest.mark.parametrize("op", [rs.RS_OP_RMSNORM, rs.RS_OP_LAYERNORM])
+@pytest.mark.parametrize("dtype", [rs.RS_F32, rs.RS_F16, rs.RS_BF16])
+@pytest.mark.parametrize("N", [1, 2, 7, 8, 9, 33, 255, 1000, 1500, 4096, 5000, 8192, 8193, 16384, 65536,
+                               1 << 20])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_auto_plan_uses_instantiated_kernels_and_covers_the_row(op, dtype, N, aligned):
+    a = A if aligned else A + 2 * (1 if dtype else 2)
+    p = _plan(op, 3, N, dtype, a=a)
+    assert _covers(p, N)
+    if p["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING):
+        table = NORM_VPT_VEC if p["vec_elems"] > 1 else NORM_VPT_SCALAR
+        assert p["vec_per_thread"] in table
+        assert p["block_threads"] % p["threads_per_row"] == 0 and p["block_threads"] <= 1024
+    if N <= 4096 or (p["vec_elems"] > 1 and N * (4 if dtype == rs.RS_F32 else 2) <= 32 * 1024):
+        assert p["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING)  # single pass over HBM

@@ -1,0 +1,385 @@
+"""GPU parity of the row normalisations (RMSNorm, LayerNorm) against the CPU
+oracle, through the C ABI.
+
+Each case makes seeded inputs, weight and bias vectors on the GPU, runs the
+normalisation through the ctypes binding of librowsoftmax.so and compares
+every output element with the oracle under the bound of tests/_parity.py.
+Covered: the register-row, ring and streaming kernels of every storage type,
+forced thread shapes, persistent grids that loop over rows, ragged tails,
+element-wise access (misaligned pointers, odd strides), padded rows with
+guard bands, in-place calls, optional weight and bias, special values, rows
+with a large common offset, eps = 0, the benchmark shapes at full size
+(sampled rows) in the launch configuration the benchmark times, and the
+maximum sizes.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_row_gb300 as rs
+from memory_bound_row_gb300 import build
+from memory_bound_row_gb300 import workloads as W
+
+from _parity import compare_norm, oracle_norm_rows
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+OPS = ["rms", "ln"]
+EPS = {"rms": 1e-6, "ln": 1e-5}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    rc, flags = rs.rowsoftmax_device_status(clear=True)
+    assert rc == rs.RS_OK
+    yield
+    rc, flags = rs.rowsoftmax_device_status(clear=False)
+    assert rc == rs.RS_OK and flags == 0, f"device status word {flags:#x}"
+
+
+def _params(N, dtype, seed=0, weight=True, bias=True):
+    w, b = W.norm_params(N, dtype, seed, "cuda")
+    return (w if weight else None), (b if bias else None)
+
+
+def _run(op, x, w=None, b=None, eps=None, out=None, options=None):
+    eps = EPS[op] if eps is None else eps
+    if op == "rms":
+        y = rs.rmsnorm(x, w, eps=eps, out=out, options=options)
+    else:
+        y = rs.layernorm(x, w, b, eps=eps, out=out, options=options)
+    torch.cuda.synchronize()
+    return y
+
+
+def _check(op, x, y, w=None, b=None, eps=None, what=""):
+    eps = EPS[op] if eps is None else eps
+    N = x.shape[1]
+    ref = oracle_norm_rows(op, x, N, w, b if op == "ln" else None, eps)
+    return compare_norm(y[:, :N], ref, x, op, w, b if op == "ln" else None, eps, what)
+
+
+def _servable(op, x, w, b, options):
+    rc, dev = rs.rowsoftmax_device_info()
+    assert rc == rs.RS_OK
+    M, N = x.shape
+    code = rs.RS_OP_RMSNORM if op == "rms" else rs.RS_OP_LAYERNORM
+    rc, plan = rs.rownorm_plan(code, x.data_ptr(), x.data_ptr() + (1 << 44), None if w is None else w.data_ptr(),
+                               None if (b is None or op == "rms") else b.data_ptr(), M, N,
+                               x.stride(0) if M > 1 else N, x.stride(0) if M > 1 else N, EPS[op],
+                               rs.dtype_code(x.dtype), options, dev)
+    assert rc in (rs.RS_OK, rs.RS_ERR_NO_PATH)
+    return rc == rs.RS_OK, plan
+
+
+def _input(M, N, dtype, ld=None, kind="normal1", seed=0):
+    return W.generate(W.custom(M, N, dtype, ld=ld, seed=seed, kind=kind), "cuda")
+
+
+def _aligned(M, N, dtype, kind="normal1", seed=0):
+    vec = 4 if dtype == "f32" else 8
+    ld = -(-N // vec) * vec
+    x = _input(M, N, dtype, ld=ld, kind=kind, seed=seed)[:, :N]
+    out = torch.empty((M, ld), dtype=DT[dtype], device="cuda")[:, :N]
+    return x, out
+
+
+SHAPES = [(1, 1), (3, 2), (5, 3), (37, 7), (64, 8), (33, 33), (300, 100), (17, 255), (129, 781), (64, 1000),
+          (40, 1500), (24, 4096), (16, 5000), (8, 8192), (5, 12288), (3, 16384)]
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_auto_path_small_shapes(op, dtype, M, N):
+    x, out = _aligned(M, N, dtype, seed=M * 7 + N)
+    w, b = _params(N, dtype, seed=N)
+    y = _run(op, x, w, b, out=out)
+    _check(op, x, y, w, b, what=f"{op} {dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("weight,bias", [(False, False), (True, False), (False, True)])
+@pytest.mark.parametrize("N", [100, 4096])
+def test_optional_weight_and_bias(op, dtype, weight, bias, N):
+    x, out = _aligned(50, N, dtype, seed=3)
+    w, b = _params(N, dtype, seed=5, weight=weight, bias=bias)
+    y = _run(op, x, w, b, out=out)
+    _check(op, x, y, w, b, what=f"{op} w={weight} b={bias}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("tpr,vpt", [(1, 1), (2, 2), (4, 3), (8, 6), (16, 8), (32, 1), (32, 6), (64, 4), (96, 2),
+                                     (128, 8), (256, 3), (1024, 1)])
+@pytest.mark.parametrize("grid_limit", [0, 3])
+def test_rows_path_thread_shapes(op, dtype, tpr, vpt, grid_limit):
+    vec = 4 if dtype == "f32" else 8
+    N = max(1, tpr * vpt * vec - 3)  # a ragged last unit
+    M = 70
+    x, out = _aligned(M, N, dtype, seed=tpr + vpt)
+    w, b = _params(N, dtype, seed=tpr)
+    opts = {"path": rs.RS_PATH_ROWS, "threads_per_row": tpr, "vec_per_thread": vpt, "grid_limit": grid_limit}
+    ok, _ = _servable(op, x, w, b, opts)
+    if not ok:
+        pytest.skip("register budget of this shape")
+    y = _run(op, x, w, b, out=out, options=opts)
+    _check(op, x, y, w, b, what=f"{op} rows tpr={tpr} vpt={vpt}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [1, 5, 31, 100, 777, 4096])
+def test_rows_path_element_wise(op, dtype, N):
+    x = _input(45, N, dtype, seed=N)
+    w, b = _params(N, dtype, seed=1)
+    y = _run(op, x, w, b, options={"force_scalar": 1})
+    _check(op, x, y, w, b, what=f"{op} scalar {dtype} N={N}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [8, 100, 1001, 2048, 5000, 8192, 12345])
+@pytest.mark.parametrize("stages", [2, 3, 8])
+@pytest.mark.parametrize("grid_limit", [0, 2])
+def test_ring_path(op, dtype, N, stages, grid_limit):
+    x, out = _aligned(97, N, dtype, seed=N + stages)
+    w, b = _params(N, dtype, seed=stages)
+    opts = {"path": rs.RS_PATH_RING, "stages": stages, "grid_limit": grid_limit}
+    ok, _ = _servable(op, x, w, b, opts)
+    if not ok:
+        pytest.skip("ring stages do not fit shared memory")
+    y = _run(op, x, w, b, out=out, options=opts)
+    _check(op, x, y, w, b, what=f"{op} ring {dtype} N={N} stages={stages}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("tpr,vpt", [(1, 1), (4, 2), (32, 8), (64, 4), (160, 6), (256, 4), (512, 2), (1024, 1)])
+@pytest.mark.parametrize("grid_limit", [0, 3])
+def test_ring_thread_shapes_and_wraparound(op, dtype, tpr, vpt, grid_limit):
+    vec = 4 if dtype == "f32" else 8
+    N = tpr * vpt * vec - 5 if tpr * vpt * vec > 5 else tpr * vpt * vec
+    x, out = _aligned(41, N, dtype, seed=tpr * vpt)
+    w, b = _params(N, dtype, seed=vpt)
+    opts = {"path": rs.RS_PATH_RING, "threads_per_row": tpr, "vec_per_thread": vpt, "grid_limit": grid_limit}
+    ok, _ = _servable(op, x, w, b, opts)
+    if not ok:
+        pytest.skip("no ring plan for this shape")
+    y = _run(op, x, w, b, out=out, options=opts)
+    _check(op, x, y, w, b, what=f"{op} ring tpr={tpr} vpt={vpt} grid_limit={grid_limit}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("scalar", [0, 1])
+@pytest.mark.parametrize("N", [1, 3, 1000, 70001, 131075])
+@pytest.mark.parametrize("grid_limit", [0, 2])
+def test_stream_path(op, dtype, scalar, N, grid_limit):
+    x, out = _aligned(9, N, dtype, seed=N, kind="normal_spike")
+    w, b = _params(N, dtype, seed=2)
+    opts = {"path": rs.RS_PATH_STREAM, "force_scalar": scalar, "grid_limit": grid_limit}
+    y = _run(op, x, w, b, out=out, options=opts)
+    _check(op, x, y, w, b, what=f"{op} stream {dtype} N={N} scalar={scalar}")
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_paths_agree_on_the_same_input(op):
+    x, _ = _aligned(64, 3000, "bf16", seed=11)
+    w, b = _params(3000, "bf16", seed=11)
+    ys = [_run(op, x, w, b, options={"path": p}) for p in (rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_STREAM)]
+    for y in ys:
+        _check(op, x, y, w, b, what=f"{op} paths")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_padded_strides_and_guard_bands(op, dtype):
+    M, N, ld = 33, 1000, 1040
+    x = _input(M, N, dtype, ld=ld, seed=4)  # padding columns hold NaN
+    buf = torch.full((M + 2, ld), float("nan"), dtype=DT[dtype], device="cuda")
+    before = buf.clone()
+    out = buf[1: M + 1, :N]
+    w, b = _params(N, dtype, seed=4)
+    y = _run(op, x[:, :N], w, b, out=out)
+    _check(op, x[:, :N], y, w, b, what=f"{op} padded")
+    bits = torch.int32 if dtype == "f32" else torch.int16
+    assert torch.equal(buf[0].view(bits), before[0].view(bits))
+    assert torch.equal(buf[M + 1].view(bits), before[M + 1].view(bits))
+    assert torch.equal(buf[1: M + 1, N:].view(bits), before[1: M + 1, N:].view(bits))
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shift", [1, 3])
+def test_misaligned_pointers_use_element_wise_access(op, dtype, shift):
+    M, N = 20, 3001
+    base = _input(M, N + 8, dtype, seed=shift)
+    x = base[:, shift: shift + N]
+    wbuf, bbuf = _params(N + 8, dtype, seed=shift)
+    w, b = wbuf[shift: shift + N], bbuf[1: 1 + N]
+    ok, plan = _servable(op, x, w, b, None)
+    assert ok and plan["vec_elems"] == 1
+    y = _run(op, x, w, b)
+    _check(op, x, y, w, b, what=f"{op} misaligned shift={shift}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [100, 8192, 70000])
+@pytest.mark.parametrize("path", [rs.RS_PATH_AUTO, rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_STREAM])
+def test_in_place(op, dtype, N, path):
+    x, _ = _aligned(12, N, dtype, seed=N)
+    w, b = _params(N, dtype, seed=N)
+    opts = {"path": path}
+    ok, _ = _servable(op, x, w, b, opts)
+    if not ok:
+        pytest.skip("path does not serve this shape")
+    x0 = x.clone()
+    y = _run(op, x, w, b, out=x, options=opts)
+    assert y.data_ptr() == x.data_ptr()
+    _check(op, x0, y, w, b, what=f"{op} in place")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_STREAM])
+def test_special_values(op, dtype, path):
+    M, N = 8, 1000
+    x, out = _aligned(M, N, dtype, seed=9)
+    x[0, 5] = float("inf")
+    x[1, 7] = float("-inf")
+    x[2, 0] = float("nan")
+    x[3, :] = 0.0                        # RMSNorm gives 0, LayerNorm the bias
+    x[4, :] = 2.5                        # constant row: LayerNorm gives the bias
+    x[5, 3] = float("inf")
+    x[5, 4] = float("-inf")
+    w, b = _params(N, dtype, seed=9)
+    ok, _ = _servable(op, x, w, b, {"path": path})
+    if not ok:
+        pytest.skip("path does not serve this shape")
+    y = _run(op, x, w, b, out=out, options={"path": path})
+    _check(op, x, y, w, b, what=f"{op} special values")
+    if op == "rms":
+        assert bool((y[3] == 0).all())
+    else:
+        assert torch.equal(y[3], b)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [1500, 8192, 100000])
+def test_layernorm_of_rows_with_a_large_offset(dtype, N):
+    # N(50, 1) rows: the two-pass variance keeps its accuracy where
+    # E[x^2] - E[x]^2 would cancel.
+    x, out = _aligned(16, N, dtype, kind="offset50", seed=N)
+    w, b = _params(N, dtype, seed=1)
+    y = _run("ln", x, w, b, out=out)
+    _check("ln", x, y, w, b, what=f"ln offset {dtype} N={N}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("N", [1, 2, 1000])
+def test_eps_zero(op, N):
+    x, out = _aligned(30, N, "f32", seed=N)
+    w, b = _params(N, "f32", seed=N)
+    if N == 1 and op == "ln":
+        pytest.skip("one-element rows have zero variance: 0/0 at eps = 0")
+    y = _run(op, x, w, b, eps=0.0, out=out)
+    _check(op, x, y, w, b, eps=0.0, what=f"{op} eps=0")
+
+
+def test_rejections_on_device_memory():
+    x = torch.randn(8, 64, device="cuda")
+    out = torch.empty_like(x)
+    w = out[0]  # the weight inside the output
+    with pytest.raises(rs.RowSoftmaxError) as e:
+        rs.rmsnorm(x, w, out=out)
+    assert e.value.status == rs.RS_ERR_OVERLAP
+    host_w = torch.ones(64)
+    rc = rs.rmsnorm_fwd(x.data_ptr(), out.data_ptr(), host_w.data_ptr(), 8, 64, 64, 64, 1e-6, rs.RS_F32, 0)
+    assert rc == rs.RS_ERR_NOT_DEVICE_MEMORY
+
+
+def test_nonzero_stream():
+    x, out = _aligned(256, 4096, "bf16", seed=1)
+    w, b = _params(4096, "bf16", seed=1)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = rs.layernorm(x, w, b, out=out)
+    s.synchronize()
+    _check("ln", x, y, w, b, what="side stream")
+
+
+# ---------------------------------------------------------------------------
+# The benchmark shapes at full size, in the launch configuration the
+# benchmark times (auto plan, weight and bias present).
+# ---------------------------------------------------------------------------
+
+def _sample_rows(M, extra=()):
+    rng = np.random.default_rng(M + 1)
+    rows = set(rng.choice(M, size=min(M, 64), replace=False).tolist())
+    rows.update([0, 1, M // 2, M - 2, M - 1])
+    rows.update(int(r) for r in extra)
+    return sorted(r for r in rows if 0 <= r < M)
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("name", W.ORDER)
+def test_benchmark_shapes_full_size(op, name):
+    w = W.norm_workload(name)
+    x = W.generate(w, "cuda")
+    out = torch.full_like(x, float("nan")) if w.ld > w.N else torch.empty_like(x)
+    if w.ld > w.N:
+        pad_before = out[:, w.N:].clone()
+    wt, bs = W.norm_params(w.N, w.dtype, w.seed, "cuda")
+    y = _run(op, x[:, : w.N], wt, bs, out=out[:, : w.N])
+
+    extra = []
+    if w.kind == "normal2_const":
+        extra = W.pick_rows(w.M, round(0.01 * w.M), w.seed, 1, "cpu").tolist()[:8]
+    if w.kind == "uniform20_offset":
+        extra = W.pick_rows(w.M, round(0.10 * w.M), w.seed, 1, "cpu").tolist()[:8]
+    rows = torch.tensor(_sample_rows(w.M, extra), device="cuda")
+    _check(op, x[rows, : w.N], y[rows], wt, bs, what=f"{op} {name}")
+    assert bool(torch.isfinite(y).all())
+    if w.ld > w.N:
+        assert torch.equal(out[:, w.N:].view(torch.int32), pad_before.view(torch.int32))
+
+
+# ---------------------------------------------------------------------------
+# Maximum sizes.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("op", OPS)
+def test_more_than_two_to_the_31_rows(op):
+    M = (1 << 31) + 5
+    x = torch.empty((M, 2), dtype=torch.bfloat16, device="cuda")
+    x[:, 0] = 0.5
+    x[:, 1] = -1.75
+    w, b = _params(2, "bf16", seed=31)
+    y = _run(op, x, w, b)
+    _check(op, x[:1], y[:1], w, b, what=f"{op} 2^31+5 rows")
+    last = y[-1:].clone()
+    _check(op, x[:1], last, w, b, what=f"{op} 2^31+5 rows, last row")
+    for col in range(2):
+        assert bool((y[:, col] == y[0, col]).all())
+    del x, y
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_a_row_of_two_to_the_26_elements(op):
+    N = 1 << 26
+    x = _input(2, N, "f32", kind="normal_spike", seed=26)
+    w, b = _params(N, "f32", seed=26)
+    y = _run(op, x, w, b)
+    _check(op, x, y, w, b, what=f"{op} 2 x 2^26")
+    del x, y
+    torch.cuda.empty_cache()
