@@ -69,30 +69,43 @@ norm_stream_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, i
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
         const S* xr = in + row * ldi;
         S* yr = out + row * ldo;
-        float shift = 0.0f, r;
+        float nmr = 0.0f, r;  // y = (x * r + nmr) * w + b, nmr = -mean * r (0 for RMSNorm)
+        float acc[VEC];
+        auto reset = [&]() {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+        };
+        auto total = [&]() {
+#pragma unroll
+            for (int h = VEC / 2; h > 0; h /= 2)
+#pragma unroll
+                for (int e = 0; e < h; ++e) acc[e] += acc[e + h];
+            return acc[0];
+        };
         if constexpr (OP::kOp == RS_OP_RMSNORM) {
-            float s = 0.0f;
+            reset();
             for_units<DT, VEC, true>(xr, N, units, [&](int, const float* v) {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) s = fmaf(v[e], v[e], s);
+                for (int e = 0; e < VEC; ++e) acc[e] = fmaf(v[e], v[e], acc[e]);
             });
-            r = 1.0f / sqrtf(block_sum(s, red) / (float)N + a.eps);
+            r = 1.0f / sqrtf(block_sum(total(), red) / (float)N + a.eps);
         } else {
-            float s = 0.0f;
+            reset();
             for_units<DT, VEC, true>(xr, N, units, [&](int, const float* v) {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) s += v[e];
+                for (int e = 0; e < VEC; ++e) acc[e] += v[e];
             });
-            shift = block_sum(s, red) / (float)N;
-            float d = 0.0f;
+            const float mean = block_sum(total(), red) / (float)N;
+            reset();
             for_units<DT, VEC, true>(xr, N, units, [&](int u, const float* v) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    const float x = v[e] - shift;
-                    if (u * VEC + e < N) d = fmaf(x, x, d);
+                    const float x = v[e] - mean;
+                    if (u * VEC + e < N) acc[e] = fmaf(x, x, acc[e]);
                 }
             });
-            r = 1.0f / sqrtf(block_sum(d, red) / (float)N + a.eps);
+            r = 1.0f / sqrtf(block_sum(total(), red) / (float)N + a.eps);
+            nmr = -mean * r;
         }
         // The writing pass holds weight and bias units too: fewer in flight
         // for 16-byte units of 16-bit values (no spills at 128 registers).
@@ -101,7 +114,7 @@ norm_stream_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, i
             load_param_unit<DT, VEC>(a.w, u * VEC, N, w, 1.0f);
             load_param_unit<DT, VEC>(a.b, u * VEC, N, b, 0.0f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) y[e] = fmaf((v[e] - shift) * r, w[e], b[e]);
+            for (int e = 0; e < VEC; ++e) y[e] = fmaf(fmaf(v[e], r, nmr), w[e], b[e]);
             store_unit<DT, VEC>(yr, u * VEC, N, y);
         });
     }

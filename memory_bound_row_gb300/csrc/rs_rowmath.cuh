@@ -144,6 +144,25 @@ __device__ __forceinline__ float row_sum(float s, int tpr, float2* part) {
     return __shfl_sync(0xffffffffu, group_sum(p, pow2_ceil(wpr)), 0);
 }
 
+// Sum over the thread's values of acc' = f(acc, x, k, e), spread over up to
+// eight independent accumulators (short dependency chains: the additions of
+// different accumulators overlap in the pipeline), then added as a tree.
+template <int VPT, int VEC, typename F>
+__device__ __forceinline__ float thread_sum(const float (&v)[VPT][VEC], F f) {
+    constexpr int n = VPT * VEC;
+    constexpr int A = n >= 8 ? 8 : n >= 4 ? 4 : n >= 2 ? 2 : 1;
+    float acc[A];
+#pragma unroll
+    for (int i = 0; i < A; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < n; ++i) acc[i % A] = f(acc[i % A], v[i / VEC][i % VEC], i / VEC, i % VEC);
+#pragma unroll
+    for (int h = A / 2; h > 0; h /= 2)
+#pragma unroll
+        for (int i = 0; i < h; ++i) acc[i] += acc[i + h];
+    return acc[0];
+}
+
 struct OpSoftmax {
     static constexpr int kOp = RS_OP_SOFTMAX;
     static constexpr float kFill = kNegInf;
@@ -166,11 +185,7 @@ struct OpRmsNorm {
     template <int DT, int VEC, int VPT>
     __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool,
                                                  const RowArgs& a, float2* part) {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) s = fmaf(v[k][e], v[k][e], s);
+        float s = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return fmaf(x, x, acc); });
         s = row_sum<0>(s, tpr, part);
         const float r = 1.0f / sqrtf(s / (float)n + a.eps);
 #pragma unroll
@@ -184,46 +199,38 @@ struct OpRmsNorm {
 };
 
 // LayerNorm: y = (x - mean) * rsqrt(var + eps) * w + b, population variance,
-// the two moments reduced one after the other (two passes over registers).
+// the two moments reduced one after the other (two passes over registers);
+// the output is formed as ((x * r) - mean * r) * w + b with two FMAs.
 struct OpLayerNorm {
     static constexpr int kOp = RS_OP_LAYERNORM;
     static constexpr float kFill = 0.0f;
     template <int DT, int VEC, int VPT>
     __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool whole,
                                                  const RowArgs& a, float2* part) {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) s += v[k][e];
+        float s = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return acc + x; });
         const float mean = row_sum<0>(s, tpr, part) / (float)n;
-        float d = 0.0f;
+        float d;
         if (whole) {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float x = v[k][e] - mean;
-                    d = fmaf(x, x, d);
-                }
+            d = thread_sum<VPT, VEC>(v, [mean](float acc, float x, int, int) {
+                const float c = x - mean;
+                return fmaf(c, c, acc);
+            });
         } else {  // absent elements hold 0, not the mean: leave them out
-#pragma unroll
-            for (int k = 0; k < VPT; ++k)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float x = v[k][e] - mean;
-                    if ((t + k * tpr) * VEC + e < n) d = fmaf(x, x, d);
-                }
+            d = thread_sum<VPT, VEC>(v, [mean, t, tpr, n](float acc, float x, int k, int e) {
+                const float c = x - mean;
+                return (t + k * tpr) * VEC + e < n ? fmaf(c, c, acc) : acc;
+            });
         }
         const float var = row_sum<1>(d, tpr, part) / (float)n;
         const float r = 1.0f / sqrtf(var + a.eps);
+        const float nmr = -mean * r;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             float w[VEC], b[VEC];
             load_param_unit<DT, VEC>(a.w, (t + k * tpr) * VEC, n, w, 1.0f);
             load_param_unit<DT, VEC>(a.b, (t + k * tpr) * VEC, n, b, 0.0f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] = fmaf((v[k][e] - mean) * r, w[e], b[e]);
+            for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
         }
     }
 };
