@@ -39,7 +39,13 @@
  * Execution: every call is asynchronous on `stream` (0 = legacy default
  * stream), allocates no device memory, and never synchronises.  Errors in
  * the arguments are reported before anything is launched.  Calls are safe
- * from several host threads.
+ * from several host threads.  The kernels that are not cluster launches
+ * (RS_PATH_ROWS, RS_PATH_RING, and RS_PATH_STREAM of the normalisations) use
+ * programmatic dependent launch: such a kernel may be scheduled and set up
+ * while the previous kernel of the stream finishes, but reads and writes no
+ * global memory before that kernel has completed, so stream order is kept;
+ * back-to-back calls overlap their launch latency.  rs_options.strict_order
+ * turns this off.
  */
 #ifndef ROWSOFTMAX_H
 #define ROWSOFTMAX_H
@@ -122,6 +128,7 @@ typedef struct {
                              stage but never issue the copies, so each wait runs out after
                              wait_limit_us, bit 0 of the device status word is set and the output
                              is left unwritten; no fault, trap or unbounded wait is involved */
+    int strict_order;     /* 1: launch without programmatic dependent launch (see "Execution") */
 } rs_options;
 
 /* What a call would launch (filled by rowsoftmax_plan). */
@@ -142,6 +149,7 @@ typedef struct {
     int64_t wait_limit_us;  /* copied from rs_options */
     int withhold_copies;  /* copied from rs_options */
     int op;               /* rs_op the plan serves */
+    int strict_order;     /* copied from rs_options */
 } rs_plan;
 
 /* Device facts the planner needs; rowsoftmax_plan takes them explicitly so

@@ -60,6 +60,7 @@ class rs_options(ctypes.Structure):
         ("grid_limit", ctypes.c_int64),
         ("wait_limit_us", ctypes.c_int64),
         ("withhold_copies", ctypes.c_int),
+        ("strict_order", ctypes.c_int),
     ]
 
 
@@ -81,6 +82,7 @@ class rs_plan(ctypes.Structure):
         ("wait_limit_us", ctypes.c_int64),
         ("withhold_copies", ctypes.c_int),
         ("op", ctypes.c_int),
+        ("strict_order", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -367,13 +367,15 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
     if (opts) o = *opts;
     if (o.path < RS_PATH_AUTO || o.path > RS_PATH_RING || o.grid_limit < 0 || o.vec_per_thread < 0 ||
         o.threads_per_row < 0 || o.block_threads < 0 || o.cluster_size < 0 || o.stages < 0 ||
-        o.wait_limit_us < 0 || o.withhold_copies < 0 || o.withhold_copies > 1)
+        o.wait_limit_us < 0 || o.withhold_copies < 0 || o.withhold_copies > 1 || o.strict_order < 0 ||
+        o.strict_order > 1)
         return RS_ERR_INVALID_ARG;
     // Withholding copies is only defined for the ring, and needs a short wait limit.
     if (o.withhold_copies && (o.path != RS_PATH_RING || o.wait_limit_us <= 0 || o.wait_limit_us > 1000000))
         return RS_ERR_INVALID_ARG;
     p->wait_limit_us = o.wait_limit_us;
     p->withhold_copies = o.withhold_copies;
+    p->strict_order = o.strict_order;
     if (M == 0 || N == 0) return RS_OK;  // nothing to do, nothing launched
     if (N > kMaxN) return RS_ERR_INVALID_ARG;
     if (!in || !out) return RS_ERR_INVALID_ARG;

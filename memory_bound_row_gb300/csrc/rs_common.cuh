@@ -161,6 +161,19 @@ __device__ __forceinline__ void store_unit(typename Traits<DT>::storage* row, in
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of this library is launched so
+// that it may begin (be scheduled, set up shared memory and barriers) while
+// the previous kernel of its stream is still finishing.  Before its first
+// access to global memory it waits for that kernel to complete and for its
+// writes to be visible, which keeps the stream's order; it then allows the
+// next programmatically launched kernel of the stream to begin its own setup.
+// Kernels launched without the attribute, or first in their stream, pass the
+// wait at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // exp(x - m) is always taken against safe(m): a max of -inf (a row, or part
 // of one, with no finite entry) is replaced by 0 so that -inf entries give
 // exp(-inf) = 0 instead of (-inf) - (-inf) = NaN.  Partial sums that belong

@@ -2,7 +2,7 @@
 // planner and the kernel translation units.  Not part of the public ABI.
 #pragma once
 
-#include <cuda_runtime_api.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "rowsoftmax.h"
@@ -70,6 +70,42 @@ struct RowArgs {
     const void* b;
     float eps;
 };
+
+// Launch of `kern` with the programmatic-dependent-launch attribute (unless
+// `strict`), and a cluster dimension when cluster > 0.  The kernels wait for
+// the previous grid of the stream before touching global memory (see
+// wait_prior_grid), so the attribute only overlaps launch and setup.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                          int cluster, bool strict, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (!strict) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return err;
+    }
+    return cudaGetLastError();
+}
 
 // Launchers.  Each returns the CUDA error of the launch (cudaSuccess if it
 // was enqueued).  Arguments were validated and planned by the caller.

@@ -66,6 +66,7 @@ norm_stream_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, i
     S* out = static_cast<S*>(out_);
     __shared__ float red[33];
     const int units = (N + VEC - 1) / VEC;
+    wait_prior_grid();
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
         const S* xr = in + row * ldi;
         S* yr = out + row * ldo;
@@ -118,13 +119,14 @@ norm_stream_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, i
             store_unit<DT, VEC>(yr, u * VEC, N, y);
         });
     }
+    allow_next_grid();  // a grid that loops over rows: the next kernel may begin once this CTA is done
 }
 
 template <int DT, int VEC, typename OP>
 cudaError_t launch_norm_stream(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                                int64_t ldo, cudaStream_t s, const RowArgs& a) {
-    norm_stream_kernel<DT, VEC, OP><<<(unsigned)p.grid, kNormStreamThreads, 0, s>>>(in, out, M, N, ldi, ldo, a);
-    return cudaGetLastError();
+    return launch_kernel(norm_stream_kernel<DT, VEC, OP>, (unsigned)p.grid, (unsigned)kNormStreamThreads, 0, s, 0,
+                         p.strict_order != 0, in, out, M, N, ldi, ldo, a);
 }
 
 }  // namespace rs

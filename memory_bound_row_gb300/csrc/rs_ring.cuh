@@ -100,6 +100,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         fence_mbar_init();
     }
     __syncthreads();
+    wait_prior_grid();
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             const int64_t g = blockIdx.x + (int64_t)s * gridDim.x;
@@ -210,6 +211,10 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         }
     }
 
+    // Persistent grid: the next kernel of the stream may begin its launch once
+    // this CTA has no more rows (earlier, its waiting CTAs would share the SMs
+    // with this grid's work).
+    allow_next_grid();
     if (abort && threadIdx.x == 0) {
         // Let the copies of iterations it .. it + stages - 1 land before the
         // shared memory is released (iteration j used stage j % stages with
@@ -247,9 +252,8 @@ cudaError_t launch_ring_one(const rs_plan& p, const void* in, void* out, int64_t
         }
     }
     const uint64_t wait_ns = p.wait_limit_us > 0 ? (uint64_t)p.wait_limit_us * 1000ull : kWaitLimitNs;
-    kern<<<(unsigned)p.grid, p.block_threads, p.smem_bytes, s>>>(in, out, M, N, ldi, ldo, p.threads_per_row,
-                                                                 p.stages, wait_ns, p.withhold_copies, a);
-    return cudaGetLastError();
+    return launch_kernel(kern, (unsigned)p.grid, (unsigned)p.block_threads, p.smem_bytes, s, 0, p.strict_order != 0,
+                         in, out, M, N, ldi, ldo, p.threads_per_row, p.stages, wait_ns, p.withhold_copies, a);
 }
 
 template <int DT, typename OP, int... Vs>

@@ -36,6 +36,8 @@ rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
     const int grp = threadIdx.x / tpr;
     const int t = threadIdx.x - grp * tpr;
     const bool whole = (t + (VPT - 1) * tpr + 1) * VEC <= N;  // all of this thread's units lie in the row
+    wait_prior_grid();
+    allow_next_grid();
 
     int it = 0;
     for (int64_t rb = blockIdx.x; rb * rows_per_cta < M; rb += gridDim.x, ++it) {
@@ -51,9 +53,8 @@ rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
 template <int DT, int VEC, int VPT, typename OP>
 cudaError_t launch_rows_one(const rs_plan& p, const void* in, void* out, int64_t M, int N,
                             int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a) {
-    rows_kernel<DT, VEC, VPT, OP><<<(unsigned)p.grid, p.block_threads, 0, s>>>(in, out, M, N, ldi, ldo,
-                                                                             p.threads_per_row, a);
-    return cudaGetLastError();
+    return launch_kernel(rows_kernel<DT, VEC, VPT, OP>, (unsigned)p.grid, (unsigned)p.block_threads, 0, s, 0,
+                         p.strict_order != 0, in, out, M, N, ldi, ldo, p.threads_per_row, a);
 }
 
 template <int DT, int VEC, typename OP, int... Vs>

@@ -91,6 +91,7 @@ wide_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         }
     };
 
+    wait_prior_grid();
     if (STAGED) {
         if (tid == 0) {
             for (int s = 0; s < kWideMaxStages; ++s) {
@@ -224,6 +225,7 @@ wide_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
                 (void)mbar_wait_bounded(&bars[j % nslots][s], (uint32_t)((j / nslots) & 1));
         }
     }
+    allow_next_grid();  // persistent grid: the next kernel may begin once this CTA is done
     cluster.sync();  // peers may still be reading cta_part
 }
 
@@ -293,6 +295,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
         fence_mbar_init();
     }
     __syncthreads();
+    wait_prior_grid();
     if (tid == 0) {
         for (int j = 0; j < nslots; ++j)
             if (cluster_id + j * n_clusters < M) issue(cluster_id + j * n_clusters, j);
@@ -394,6 +397,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
         if (!abort) store_row_units<DT, VEC, VPT>(out + row * ldo + c0, tid, tpr, len, v, c);
     }
 
+    allow_next_grid();  // persistent grid: the next kernel may begin once this CTA is done
     if (abort && tid == 0 && abort_it >= 0) {
         for (int64_t j = abort_it; j < abort_it + nslots; ++j) {
             if (cluster_id + j * n_clusters >= M) break;
@@ -440,35 +444,15 @@ static cudaError_t ensure_hold_attributes() {
     return set_wide_attributes(wide_hold_kernel<DT, VPT>, mu, done);
 }
 
-template <typename Kern, typename... Args>
-static cudaError_t launch_cluster(Kern kern, const rs_plan& p, size_t smem, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-    cfg.blockDim = dim3((unsigned)p.block_threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.cluster_size;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, args...);
-    if (err != cudaSuccess) {
-        (void)cudaGetLastError();
-        return err;
-    }
-    return cudaGetLastError();
-}
-
 template <int DT, int VPT>
 static cudaError_t launch_hold_one(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                                    int64_t ldo, cudaStream_t s) {
     cudaError_t err = ensure_hold_attributes<DT, VPT>();
     if (err != cudaSuccess) return err;
-    return launch_cluster(wide_hold_kernel<DT, VPT>, p, p.smem_bytes, s, in, out, M, N, ldi, ldo,
-                          (int)p.chunk_elems, p.stages);
+    // Cluster grids are launched in strict stream order: with programmatic
+    // dependent launch the persistent clusters measured about 10 % slower.
+    return launch_kernel(wide_hold_kernel<DT, VPT>, (unsigned)p.grid, (unsigned)p.block_threads, p.smem_bytes, s,
+                         p.cluster_size, true, in, out, M, N, ldi, ldo, (int)p.chunk_elems, p.stages);
 }
 
 template <int DT, int VEC, bool STAGED>
@@ -477,25 +461,9 @@ static cudaError_t launch_wide_one(const rs_plan& p, const void* in, void* out, 
     auto kern = wide_kernel<DT, VEC, STAGED>;
     cudaError_t err = ensure_wide_attributes<DT, VEC, STAGED>();
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-    cfg.blockDim = dim3(kWideThreads, 1, 1);
-    cfg.dynamicSmemBytes = STAGED ? p.smem_bytes : 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.cluster_size;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const int nslots = (STAGED && p.grid / p.cluster_size < M) ? 2 : 1;
-    err = cudaLaunchKernelEx(&cfg, kern, in, out, M, N, ldi, ldo, (int)p.chunk_elems, nslots);
-    if (err != cudaSuccess) {
-        (void)cudaGetLastError();
-        return err;
-    }
-    return cudaGetLastError();
+    return launch_kernel(kern, (unsigned)p.grid, (unsigned)kWideThreads, STAGED ? p.smem_bytes : 0, s,
+                         p.cluster_size, true, in, out, M, N, ldi, ldo, (int)p.chunk_elems, nslots);
 }
 
 template <int DT>

@@ -223,6 +223,17 @@ def test_failure_path_options_are_validated():
         assert rc == rs.RS_ERR_INVALID_ARG, bad
 
 
+def test_strict_order_option():
+    p = _plan(64, 4096, rs.RS_BF16)
+    assert p["strict_order"] == 0  # programmatic dependent launch by default
+    p = _plan(64, 4096, rs.RS_BF16, opts={"strict_order": 1})
+    assert p["strict_order"] == 1
+    for bad in (-1, 2):
+        rc, _ = rs.rowsoftmax_plan(A, A + (1 << 40), 64, 4096, 4096, 4096, rs.RS_BF16, {"strict_order": bad},
+                                   gb300())
+        assert rc == rs.RS_ERR_INVALID_ARG
+
+
 def test_layout_owner_matches_the_pages_worked_example():
     with open(GOLDEN) as f:
         lines = [ln for ln in f if ln.strip() and not ln.startswith("#")]
