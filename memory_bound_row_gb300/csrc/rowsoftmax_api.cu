@@ -417,7 +417,14 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         if (N * es <= kRowsMaxRowBytes) rc = plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
-        if (norm) return plan_norm_stream(vec, M, o, *dev, p);
+        if (norm) {
+            if (vec_ok) {
+                rc = plan_cluster_hold(dtype, vec, M, N, o, *dev, p);
+                if (rc == RS_OK) return RS_OK;
+                if (rc != RS_ERR_NO_PATH) return rc;
+            }
+            return plan_norm_stream(vec, M, o, *dev, p);
+        }
         if (vec_ok) {
             rc = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, p);
             if (rc == RS_OK) return RS_OK;
@@ -427,7 +434,12 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
     }
     if (path == RS_PATH_ROWS) return plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
     if (path == RS_PATH_RING) return plan_ring(dtype, vec, M, N, units, o, *dev, p);
-    if (norm) return path == RS_PATH_STREAM ? plan_norm_stream(vec, M, o, *dev, p) : RS_ERR_NO_PATH;
+    if (norm) {
+        if (path == RS_PATH_STREAM) return plan_norm_stream(vec, M, o, *dev, p);
+        // Clusters serve the normalisations with the slice in registers only.
+        if (vec == 1 || o.ring_values == RS_RING_REREAD) return RS_ERR_NO_PATH;
+        return plan_cluster_hold(dtype, vec, M, N, o, *dev, p);
+    }
     return plan_wide(dtype, path, vec, M, N, o, *dev, p);
 }
 
@@ -479,11 +491,11 @@ int current_device(int* dev, rs_device_info* info) {
 // cudaOccupancyMaxActiveClusters for a planned cluster launch, cached by
 // device and launch shape (the query costs far more than a launch).
 struct ClusterKey {
-    int dev, dtype, path, values, vec, vpt, block, cs;
+    int dev, op, dtype, path, values, vec, vpt, block, cs;
     size_t smem;
     bool operator==(const ClusterKey& o) const {
-        return dev == o.dev && dtype == o.dtype && path == o.path && values == o.values && vec == o.vec &&
-               vpt == o.vpt && block == o.block && cs == o.cs && smem == o.smem;
+        return dev == o.dev && op == o.op && dtype == o.dtype && path == o.path && values == o.values &&
+               vec == o.vec && vpt == o.vpt && block == o.block && cs == o.cs && smem == o.smem;
     }
 };
 std::mutex g_cluster_mu;
@@ -492,7 +504,7 @@ int g_cluster_vals[64];
 int g_cluster_n = 0;
 
 cudaError_t max_active_clusters_cached(int dev, const rs_plan& p, int* n) {
-    const ClusterKey k{dev, p.dtype, p.path, p.ring_values, p.vec_elems, p.vec_per_thread, p.block_threads,
+    const ClusterKey k{dev, p.op, p.dtype, p.path, p.ring_values, p.vec_elems, p.vec_per_thread, p.block_threads,
                        p.cluster_size, p.smem_bytes};
     {
         std::lock_guard<std::mutex> lock(g_cluster_mu);
@@ -502,7 +514,11 @@ cudaError_t max_active_clusters_cached(int dev, const rs_plan& p, int* n) {
                 return cudaSuccess;
             }
     }
-    cudaError_t e = rs::wide_max_active_clusters(p, n);
+    cudaError_t e;
+    if (p.op == RS_OP_SOFTMAX) e = rs::wide_max_active_clusters(p, n);
+    else if (p.dtype == RS_F32) e = rs::norm_max_clusters_f32(p, n);
+    else if (p.dtype == RS_F16) e = rs::norm_max_clusters_f16(p, n);
+    else e = rs::norm_max_clusters_bf16(p, n);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_cluster_mu);
     const int slot = g_cluster_n < 64 ? g_cluster_n++ : (int)(k.smem % 64);
@@ -586,7 +602,8 @@ int run_op(int op, const void* in, void* out, const void* w, const void* b, int6
     if (rc != RS_OK) return rc;
 
     const bool persistent_cluster = plan.path == RS_PATH_CLUSTER && plan.ring_values == RS_RING_REGISTERS;
-    if (op == RS_OP_SOFTMAX && (plan.path == RS_PATH_CLUSTER || plan.path == RS_PATH_STREAM) &&
+    if ((op == RS_OP_SOFTMAX || plan.path == RS_PATH_CLUSTER) &&
+        (plan.path == RS_PATH_CLUSTER || plan.path == RS_PATH_STREAM) &&
         (plan.cluster_size > rs::kMaxClusterPortable || persistent_cluster)) {
         int n = 0;
         cudaError_t e = max_active_clusters_cached(dev, plan, &n);

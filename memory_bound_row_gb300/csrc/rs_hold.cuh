@@ -1,0 +1,374 @@
+// RS_PATH_CLUSTER with the slice held in registers (RS_RING_REGISTERS), for
+// every row operation of the engine (softmax, RMSNorm, LayerNorm).
+//
+// Persistent clusters; CTA `rank` of a cluster serves slice
+// [rank * chunk, rank * chunk + len) of rows cluster_id, cluster_id +
+// n_clusters, ...  Each CTA has `nslots` shared-memory slots filled by bulk
+// copies.  A slot is only a landing buffer: the CTA copies its slice from the
+// slot into registers (VPT 16-byte units per thread, fp32), releases the slot
+// at once -- thread 0 immediately issues the copy of a later row into it --
+// and then reduces and writes from registers, so the next rows' bytes stream
+// in while this row is reduced and stored.  Each input byte crosses HBM once
+// and each output byte once.
+//
+// Merges go warps -> CTA through shared memory and CTAs -> cluster through
+// distributed shared memory: every CTA pushes one pair of floats into a slot
+// of every CTA of its cluster (st.async, counted on the receivers' mbarrier)
+// and combines the cluster's pairs itself.  The pair of a slice is
+//   softmax    (m, l): its max and its sum of exp(x - m); pairs merge with the
+//              online normaliser of the mohakchugh.is-a.dev post ("How Flash
+//              Attention Uses Triton"): m = max m_c, l = sum l_c exp(m_c - m);
+//   RMSNorm    (sum of x^2, 0): sums add;
+//   LayerNorm  (S_c, Q_c): the slice's sum and its sum of squared deviations
+//              from the slice's own mean mu_c = S_c / n_c; slices combine with
+//              the textbook parallel-variance identity (Chan, Golub and
+//              LeVeque): mu = sum S_c / N,
+//              sum (x - mu)^2 = sum_c [Q_c + n_c (mu_c - mu)^2],
+//              so the variance is exact algebra of two-pass slice moments and
+//              no global E[x^2] - mu^2 cancellation occurs.
+//
+// Waits are bounded by %globaltimer (a wait that runs out sets bit 0 of the
+// device status word, the CTA stops issuing copies, waits a second bounded
+// time for its copies in flight and leaves its rows unwritten).
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include <mutex>
+
+#include "rs_async.cuh"
+#include "rs_common.cuh"
+#include "rs_internal.h"
+#include "rs_rowmath.cuh"
+
+namespace rs {
+
+namespace hold_cg = cooperative_groups;
+
+// Length of the slice of CTA `rank` (0 past the row).
+__device__ __forceinline__ int hold_slice_len(int rank, int chunk, int N) {
+    const int64_t c0 = (int64_t)rank * chunk;
+    if (c0 >= N) return 0;
+    return (int)(c0 + chunk < N ? chunk : N - c0);
+}
+
+template <int DT, int VPT, typename OP>
+__global__ void __launch_bounds__(VPT <= 4 ? kWideHoldThreads : kWideHoldThreads / 2, 2)
+wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int chunk, int nslots,
+                 RowArgs args) {
+    using T = Traits<DT>;
+    using S = typename T::storage;
+    constexpr int VEC = T::kVec;
+    constexpr bool kSoftmax = OP::kOp == RS_OP_SOFTMAX;
+    const S* in = static_cast<const S*>(in_);
+    S* out = static_cast<S*>(out_);
+    hold_cg::cluster_group cluster = hold_cg::this_cluster();
+    const int cs = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+
+    extern __shared__ __align__(128) unsigned char slots[];
+    __shared__ __align__(8) uint64_t bars[2];      // slot filled
+    __shared__ __align__(8) uint64_t recv_bar[2];  // all CTAs' pairs of a row received
+    __shared__ __align__(8) float2 recv[2][kMaxCluster];
+    __shared__ float2 warp_part[2][kWideHoldThreads / 32];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int tpr = blockDim.x;
+
+    const int64_t c0l = (int64_t)rank * chunk < N ? (int64_t)rank * chunk : (int64_t)N;
+    const int c0 = (int)c0l;
+    const int len = (int)((c0l + chunk < N ? c0l + chunk : (int64_t)N) - c0l);
+    const int full = len / VEC;                        // whole units, bulk-copied
+    const uint32_t slice_bytes = (uint32_t)full * 16u;
+    const size_t slot_stride = ((size_t)chunk * sizeof(S) + 15) & ~(size_t)15;
+    const uint32_t pair_bytes = (uint32_t)cs * (uint32_t)sizeof(float2);
+    const bool whole = (tid + (VPT - 1) * tpr + 1) * VEC <= len;  // all of this thread's units in the slice
+
+    const int64_t cluster_id = blockIdx.x / cs;
+    const int64_t n_clusters = gridDim.x / cs;
+
+    auto issue = [&](int64_t row, int slot) {
+        if (slice_bytes == 0) {
+            mbar_arrive(&bars[slot]);
+            return;
+        }
+        mbar_arrive_expect_tx(&bars[slot], slice_bytes);
+        bulk_load(slots + (size_t)slot * slot_stride, in + row * ldi + c0, slice_bytes, &bars[slot]);
+    };
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&recv_bar[0], 1);
+        mbar_init(&recv_bar[1], 1);
+        mbar_arrive_expect_tx(&recv_bar[0], pair_bytes);  // armed for rows 0 and 1 of this cluster
+        mbar_arrive_expect_tx(&recv_bar[1], pair_bytes);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    wait_prior_grid();
+    if (tid == 0) {
+        for (int j = 0; j < nslots; ++j)
+            if (cluster_id + j * n_clusters < M) issue(cluster_id + j * n_clusters, j);
+    }
+    cluster.sync();  // every CTA's receive barriers are armed before any pair is sent
+
+    bool abort = false;
+    int64_t abort_it = -1;
+    int64_t it = 0;
+    for (int64_t row = cluster_id; row < M; row += n_clusters, ++it) {
+        const int slot = (int)(it % nslots);
+        const uint32_t parity = (uint32_t)((it / nslots) & 1);
+        if (!abort && !mbar_wait_bounded(&bars[slot], parity)) {
+            abort = true;
+            flag_timeout();
+        }
+        const unsigned char* buf = slots + (size_t)slot * slot_stride;
+        const S* xr = in + row * ldi + c0;
+
+        float v[VPT][VEC];
+        if ((tid + (VPT - 1) * tpr) < full) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+                T::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)(tid + k * tpr) * 16), v[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int u = tid + k * tpr;
+                if (u < full) {
+                    T::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)u * 16), v[k]);
+                } else {
+                    load_unit<DT, VEC>(xr, u * VEC, len, v[k], OP::kFill);  // ragged tail, or fill past the slice
+                }
+            }
+        }
+
+        // This thread's contribution, reduced over the warp.
+        float m = kNegInf;  // softmax: the warp's max
+        float a0 = 0.0f;    // softmax: l; norms: sum of x^2 or sum of x
+        if constexpr (kSoftmax) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+            m = group_max(m, 32);
+            const float ms = safe_max(m);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    v[k][e] = exp_diff(v[k][e], ms);
+                    a0 += v[k][e];
+                }
+        } else if constexpr (OP::kOp == RS_OP_RMSNORM) {
+            a0 = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return fmaf(x, x, acc); });
+        } else {
+            a0 = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return acc + x; });
+        }
+        a0 = group_sum(a0, 32);
+
+        // CTA merge of the warps' partials.  The barrier also ends every read
+        // of the slot, which is then handed to the copy of a later row.
+        if (lane == 0) warp_part[it & 1][warp] = make_float2(m, a0);
+        abort = __syncthreads_or(abort) != 0;
+        if (abort && abort_it < 0) abort_it = it;
+        if (tid == 0 && !abort && row + nslots * n_clusters < M) {
+            fence_proxy_async_smem();
+            issue(row + nslots * n_clusters, slot);
+        }
+        float pm = kNegInf, pl = 0.0f;
+        if (lane < nwarps) {
+            const float2 q = warp_part[it & 1][lane];
+            pm = q.x;
+            pl = q.y;
+        }
+        if constexpr (kSoftmax) {
+            group_merge(pm, pl, pow2_ceil(nwarps));  // lanes 0..nwarps-1 hold the CTA's pair
+            pm = __shfl_sync(0xffffffffu, pm, 0);
+            pl = __shfl_sync(0xffffffffu, pl, 0);
+        } else if constexpr (OP::kOp == RS_OP_RMSNORM) {
+            pm = __shfl_sync(0xffffffffu, group_sum(pl, pow2_ceil(nwarps)), 0);  // the slice's sum of squares
+            pl = 0.0f;
+        } else {
+            // The slice's sum, then its squared deviations from its own mean
+            // (a second CTA reduction through the other half of the pairs).
+            const float sc = __shfl_sync(0xffffffffu, group_sum(pl, pow2_ceil(nwarps)), 0);
+            const float mu_c = len > 0 ? sc / (float)len : 0.0f;
+            float d;
+            if (whole) {
+                d = thread_sum<VPT, VEC>(v, [mu_c](float acc, float x, int, int) {
+                    const float dx = x - mu_c;
+                    return fmaf(dx, dx, acc);
+                });
+            } else {
+                d = thread_sum<VPT, VEC>(v, [mu_c, tid, tpr, len](float acc, float x, int k, int e) {
+                    const float dx = x - mu_c;
+                    return (tid + k * tpr) * VEC + e < len ? fmaf(dx, dx, acc) : acc;
+                });
+            }
+            d = group_sum(d, 32);
+            if (lane == 0) warp_part[it & 1][warp].x = d;
+            __syncthreads();
+            float q = lane < nwarps ? warp_part[it & 1][lane].x : 0.0f;
+            pm = sc;
+            pl = __shfl_sync(0xffffffffu, group_sum(q, pow2_ceil(nwarps)), 0);
+        }
+
+        // Cluster merge: warp 0 pushes this CTA's pair into slot `rank` of
+        // every CTA's receive buffer (st.async, counted on their barrier); all
+        // threads wait for the cs pairs of this row on their own barrier.
+        const int rb = (int)(it & 1);
+        if (warp == 0 && lane < cs) {
+            const uint32_t dst = map_to_rank(smem_addr(&recv[rb][rank]), (uint32_t)lane);
+            const uint32_t dbar = map_to_rank(smem_addr(&recv_bar[rb]), (uint32_t)lane);
+            st_async_pair(dst, pm, pl, dbar);
+        }
+        if (!abort && !mbar_wait_cluster_bounded(&recv_bar[rb], (uint32_t)((it >> 1) & 1))) {
+            abort = true;
+            flag_timeout();
+        }
+        float qa = kSoftmax ? kNegInf : 0.0f, qb = 0.0f;
+        if (lane < cs) {
+            const float2 q = recv[rb][lane];
+            qa = q.x;
+            qb = q.y;
+        }
+        if constexpr (kSoftmax) {
+            group_merge(qa, qb, pow2_ceil(cs));
+            qa = __shfl_sync(0xffffffffu, qa, 0);
+            qb = __shfl_sync(0xffffffffu, qb, 0);
+            const float c = rescale(m, safe_max(qa)) / qb;
+            __syncwarp();
+            if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+        } else {
+            float r, nmr = 0.0f;
+            if constexpr (OP::kOp == RS_OP_RMSNORM) {
+                const float ss = __shfl_sync(0xffffffffu, group_sum(qa, pow2_ceil(cs)), 0);
+                r = 1.0f / sqrtf(ss / (float)N + args.eps);
+            } else {
+                const float mean = __shfl_sync(0xffffffffu, group_sum(qa, pow2_ceil(cs)), 0) / (float)N;
+                const int nl = lane < cs ? hold_slice_len(lane, chunk, N) : 0;
+                float term = 0.0f;
+                if (nl > 0) {
+                    const float dm = qa / (float)nl - mean;
+                    term = fmaf((float)nl * dm, dm, qb);
+                }
+                const float m2 = __shfl_sync(0xffffffffu, group_sum(term, pow2_ceil(cs)), 0);
+                r = 1.0f / sqrtf(m2 / (float)N + args.eps);
+                nmr = -mean * r;
+            }
+            __syncwarp();
+            if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int base = c0 + (tid + k * tpr) * VEC;
+                float w[VEC], b[VEC];
+                load_param_unit<DT, VEC>(args.w, base, N, w, 1.0f);
+                if constexpr (OP::kOp == RS_OP_LAYERNORM) load_param_unit<DT, VEC>(args.b, base, N, b, 0.0f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    if constexpr (OP::kOp == RS_OP_RMSNORM) v[k][e] = v[k][e] * r * w[e];
+                    else v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
+                }
+            }
+        }
+
+        if (!abort) store_row_units<DT, VEC, VPT>(out + row * ldo + c0, tid, tpr, len, v);
+    }
+
+    allow_next_grid();  // persistent grid: the next kernel may begin once this CTA is done
+    if (abort && tid == 0 && abort_it >= 0) {
+        for (int64_t j = abort_it; j < abort_it + nslots; ++j) {
+            if (cluster_id + j * n_clusters >= M) break;
+            (void)mbar_wait_bounded(&bars[j % nslots], (uint32_t)((j / nslots) & 1));
+        }
+    }
+    cluster.sync();  // no CTA leaves while a peer's pair may still be in flight to it
+}
+
+// The dynamic shared-memory ceiling is raised to the device maximum and the
+// non-portable cluster sizes are allowed, once per device and instance.
+template <int DT, int VPT, typename OP>
+cudaError_t ensure_hold_attributes() {
+    static std::mutex mu;
+    static bool done[64] = {};
+    auto kern = wide_hold_kernel<DT, VPT, OP>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (done[dev]) return cudaSuccess;
+    int optin = 0;
+    err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (err != cudaSuccess) return err;
+    const int dyn = optin - (int)kWideStaticSmem;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn > 0 ? dyn : 0);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
+    done[dev] = true;
+    return cudaSuccess;
+}
+
+template <int DT, int VPT, typename OP>
+cudaError_t launch_hold_one(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                            int64_t ldo, cudaStream_t s, const RowArgs& a) {
+    cudaError_t err = ensure_hold_attributes<DT, VPT, OP>();
+    if (err != cudaSuccess) return err;
+    // Cluster grids are launched in strict stream order: with programmatic
+    // dependent launch the persistent clusters measured about 10 % slower.
+    return launch_kernel(wide_hold_kernel<DT, VPT, OP>, (unsigned)p.grid, (unsigned)p.block_threads, p.smem_bytes,
+                         s, p.cluster_size, true, in, out, M, N, ldi, ldo, (int)p.chunk_elems, p.stages, a);
+}
+
+template <int DT, typename OP>
+cudaError_t launch_hold(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi, int64_t ldo,
+                        cudaStream_t s, const RowArgs& a) {
+    if (p.vec_elems != Traits<DT>::kVec) return cudaErrorInvalidConfiguration;
+    switch (p.vec_per_thread) {
+        case 1: return launch_hold_one<DT, 1, OP>(p, in, out, M, N, ldi, ldo, s, a);
+        case 2: return launch_hold_one<DT, 2, OP>(p, in, out, M, N, ldi, ldo, s, a);
+        case 4: return launch_hold_one<DT, 4, OP>(p, in, out, M, N, ldi, ldo, s, a);
+        case 8: return launch_hold_one<DT, 8, OP>(p, in, out, M, N, ldi, ldo, s, a);
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
+template <int DT, int VPT, typename OP>
+cudaError_t max_clusters_hold_one(const rs_plan& p, int* n) {
+    cudaError_t err = ensure_hold_attributes<DT, VPT, OP>();
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.cluster_size, 1, 1);
+    cfg.blockDim = dim3((unsigned)p.block_threads, 1, 1);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cluster_size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(n, wide_hold_kernel<DT, VPT, OP>, &cfg);
+}
+
+template <int DT, typename OP>
+cudaError_t max_clusters_hold(const rs_plan& p, int* n) {
+    switch (p.vec_per_thread) {
+        case 1: return max_clusters_hold_one<DT, 1, OP>(p, n);
+        case 2: return max_clusters_hold_one<DT, 2, OP>(p, n);
+        case 4: return max_clusters_hold_one<DT, 4, OP>(p, n);
+        case 8: return max_clusters_hold_one<DT, 8, OP>(p, n);
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
+}  // namespace rs

@@ -110,7 +110,8 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), unsigned grid, unsigned block,
 // Launchers.  Each returns the CUDA error of the launch (cudaSuccess if it
 // was enqueued).  Arguments were validated and planned by the caller.
 // Normalisations: plan.op selects RMSNorm or LayerNorm; plan.path RS_PATH_ROWS,
-// RS_PATH_RING or RS_PATH_STREAM (one CTA per row, reads the row 2 or 3 times).
+// RS_PATH_RING, RS_PATH_CLUSTER (register-holding clusters) or RS_PATH_STREAM
+// (one CTA per row, reads the row 2 or 3 times).
 cudaError_t launch_norm_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                             int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_norm_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
@@ -142,6 +143,11 @@ cudaError_t read_status_f32(unsigned int* flags, bool clear);
 cudaError_t read_status_f16(unsigned int* flags, bool clear);
 cudaError_t read_status_bf16(unsigned int* flags, bool clear);
 cudaError_t read_status_wide(unsigned int* flags, bool clear);
+// cudaOccupancyMaxActiveClusters of a planned register-holding cluster launch
+// of a normalisation (plan.op).
+cudaError_t norm_max_clusters_f32(const rs_plan& p, int* n);
+cudaError_t norm_max_clusters_f16(const rs_plan& p, int* n);
+cudaError_t norm_max_clusters_bf16(const rs_plan& p, int* n);
 cudaError_t read_status_norm_f32(unsigned int* flags, bool clear);
 cudaError_t read_status_norm_f16(unsigned int* flags, bool clear);
 cudaError_t read_status_norm_bf16(unsigned int* flags, bool clear);

@@ -1,5 +1,7 @@
-// RMSNorm and LayerNorm instances for bf16 storage: RS_PATH_ROWS,
+// RMSNorm and LayerNorm instances (register rows, ring, register-holding
+// clusters, one-CTA-per-row streaming) for bf16 storage: RS_PATH_ROWS,
 // RS_PATH_RING and the one-CTA-per-row streaming kernel (rs_norm.cuh).
+#include "rs_hold.cuh"
 #include "rs_norm.cuh"
 #include "rs_ring.cuh"
 #include "rs_rows.cuh"
@@ -20,6 +22,8 @@ static cudaError_t launch_norm_op(const rs_plan& p, const void* in, void* out, i
         case RS_PATH_RING:
             if (p.vec_elems != KV) return cudaErrorInvalidConfiguration;
             return RingDispatch<RS_BF16, OP, RS_VPT_NORM_VEC>::go(p, in, out, M, N, ldi, ldo, s, a);
+        case RS_PATH_CLUSTER:
+            return launch_hold<RS_BF16, OP>(p, in, out, M, N, ldi, ldo, s, a);
         case RS_PATH_STREAM:
             if (p.vec_elems == KV) return launch_norm_stream<RS_BF16, KV, OP>(p, in, out, M, N, ldi, ldo, s, a);
             if (p.vec_elems == 1) return launch_norm_stream<RS_BF16, 1, OP>(p, in, out, M, N, ldi, ldo, s, a);
@@ -33,6 +37,12 @@ cudaError_t launch_norm_bf16(const rs_plan& p, const void* in, void* out, int64_
                             int64_t ldo, cudaStream_t s, const RowArgs& a) {
     if (p.op == RS_OP_RMSNORM) return launch_norm_op<OpRmsNorm>(p, in, out, M, N, ldi, ldo, s, a);
     if (p.op == RS_OP_LAYERNORM) return launch_norm_op<OpLayerNorm>(p, in, out, M, N, ldi, ldo, s, a);
+    return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t norm_max_clusters_bf16(const rs_plan& p, int* n) {
+    if (p.op == RS_OP_RMSNORM) return max_clusters_hold<RS_BF16, OpRmsNorm>(p, n);
+    if (p.op == RS_OP_LAYERNORM) return max_clusters_hold<RS_BF16, OpLayerNorm>(p, n);
     return cudaErrorInvalidConfiguration;
 }
 

@@ -15,6 +15,9 @@
 // ("Reference Kernel: Softmax": one DRAM read, one DRAM write per row), for
 // rows far wider than one SM can hold.
 //
+// The register-holding variant of RS_PATH_CLUSTER (RS_RING_REGISTERS, the
+// default for slices that fit a CTA's registers) is in rs_hold.cuh.
+//
 // RS_PATH_STREAM (STAGED = false).  Same cluster split and merge, but the
 // slice is read from global memory twice (once for (m, l), once to
 // normalise).  It serves rows wider than the clusters' shared memory and rows
@@ -31,6 +34,7 @@
 
 #include "rs_async.cuh"
 #include "rs_common.cuh"
+#include "rs_hold.cuh"
 #include "rs_internal.h"
 #include "rs_rowmath.cuh"
 
@@ -229,184 +233,6 @@ wide_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
     cluster.sync();  // peers may still be reading cta_part
 }
 
-// RS_PATH_CLUSTER with the slice held in registers (RS_RING_REGISTERS).
-//
-// Persistent clusters; CTA `rank` of a cluster serves slice
-// [rank * chunk, rank * chunk + len) of rows cluster_id, cluster_id +
-// n_clusters, ...  Each CTA has `nslots` shared-memory slots filled by bulk
-// copies.  A slot is only a landing buffer: the CTA copies its slice from the
-// slot into registers (VPT 16-byte units per thread, fp32), releases the slot
-// at once -- thread 0 immediately issues the copy of a later row into it --
-// and then reduces and normalises from registers with one exp per element, so
-// the next rows' bytes stream in while this row is reduced and stored.
-// Merges: warps -> CTA through shared memory, CTAs -> cluster through
-// distributed shared memory, all with the (m, l) operator.
-template <int DT, int VPT>
-__global__ void __launch_bounds__(VPT <= 4 ? kWideHoldThreads : kWideHoldThreads / 2, 2)
-wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int chunk, int nslots) {
-    using T = Traits<DT>;
-    using S = typename T::storage;
-    constexpr int VEC = T::kVec;
-    const S* in = static_cast<const S*>(in_);
-    S* out = static_cast<S*>(out_);
-    cg::cluster_group cluster = cg::this_cluster();
-    const int cs = (int)cluster.num_blocks();
-    const int rank = (int)cluster.block_rank();
-
-    extern __shared__ __align__(128) unsigned char slots[];
-    __shared__ __align__(8) uint64_t bars[2];      // slot filled
-    __shared__ __align__(8) uint64_t recv_bar[2];  // all CTAs' pairs of a row received
-    __shared__ __align__(8) float2 recv[2][kMaxCluster];
-    __shared__ float2 warp_part[2][kWideHoldThreads / 32];
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const int tpr = blockDim.x;
-
-    const int64_t c0l = (int64_t)rank * chunk < N ? (int64_t)rank * chunk : (int64_t)N;
-    const int c0 = (int)c0l;
-    const int len = (int)((c0l + chunk < N ? c0l + chunk : (int64_t)N) - c0l);
-    const int full = len / VEC;                        // whole units, bulk-copied
-    const uint32_t slice_bytes = (uint32_t)full * 16u;
-    const size_t slot_stride = ((size_t)chunk * sizeof(S) + 15) & ~(size_t)15;
-    const uint32_t pair_bytes = (uint32_t)cs * (uint32_t)sizeof(float2);
-
-    const int64_t cluster_id = blockIdx.x / cs;
-    const int64_t n_clusters = gridDim.x / cs;
-
-    auto issue = [&](int64_t row, int slot) {
-        if (slice_bytes == 0) {
-            mbar_arrive(&bars[slot]);
-            return;
-        }
-        mbar_arrive_expect_tx(&bars[slot], slice_bytes);
-        bulk_load(slots + (size_t)slot * slot_stride, in + row * ldi + c0, slice_bytes, &bars[slot]);
-    };
-
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&recv_bar[0], 1);
-        mbar_init(&recv_bar[1], 1);
-        mbar_arrive_expect_tx(&recv_bar[0], pair_bytes);  // armed for rows 0 and 1 of this cluster
-        mbar_arrive_expect_tx(&recv_bar[1], pair_bytes);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    wait_prior_grid();
-    if (tid == 0) {
-        for (int j = 0; j < nslots; ++j)
-            if (cluster_id + j * n_clusters < M) issue(cluster_id + j * n_clusters, j);
-    }
-    cluster.sync();  // every CTA's receive barriers are armed before any pair is sent
-
-    bool abort = false;
-    int64_t abort_it = -1;
-    int64_t it = 0;
-    for (int64_t row = cluster_id; row < M; row += n_clusters, ++it) {
-        const int slot = (int)(it % nslots);
-        const uint32_t parity = (uint32_t)((it / nslots) & 1);
-        if (!abort && !mbar_wait_bounded(&bars[slot], parity)) {
-            abort = true;
-            flag_timeout();
-        }
-        const unsigned char* buf = slots + (size_t)slot * slot_stride;
-        const S* xr = in + row * ldi + c0;
-
-        float v[VPT][VEC];
-        if ((tid + (VPT - 1) * tpr) < full) {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k)
-                T::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)(tid + k * tpr) * 16), v[k]);
-        } else {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int u = tid + k * tpr;
-                if (u < full) {
-                    T::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)u * 16), v[k]);
-                } else {
-                    load_unit<DT, VEC>(xr, u * VEC, len, v[k]);  // ragged tail, or -inf past the slice
-                }
-            }
-        }
-
-        float m = kNegInf;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
-        m = group_max(m, 32);
-        const float ms = safe_max(m);
-        float l = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                v[k][e] = exp_diff(v[k][e], ms);
-                l += v[k][e];
-            }
-        l = group_sum(l, 32);
-
-        // CTA merge of the warps' pairs.  The barrier also ends every read of
-        // the slot, which is then handed to the copy of a later row.
-        if (lane == 0) warp_part[it & 1][warp] = make_float2(m, l);
-        abort = __syncthreads_or(abort) != 0;
-        if (abort && abort_it < 0) abort_it = it;
-        if (tid == 0 && !abort && row + nslots * n_clusters < M) {
-            fence_proxy_async_smem();
-            issue(row + nslots * n_clusters, slot);
-        }
-        float pm = kNegInf, pl = 0.0f;
-        if (lane < nwarps) {
-            const float2 q = warp_part[it & 1][lane];
-            pm = q.x;
-            pl = q.y;
-        }
-        group_merge(pm, pl, pow2_ceil(nwarps));  // lanes 0..nwarps-1 hold the CTA's pair
-        pm = __shfl_sync(0xffffffffu, pm, 0);
-        pl = __shfl_sync(0xffffffffu, pl, 0);
-
-        // Cluster merge: warp 0 pushes this CTA's pair into slot `rank` of
-        // every CTA's receive buffer (st.async, counted on their barrier); all
-        // threads wait for the cs pairs of this row on their own barrier.
-        const int rb = (int)(it & 1);
-        if (warp == 0 && lane < cs) {
-            const uint32_t dst = map_to_rank(smem_addr(&recv[rb][rank]), (uint32_t)lane);
-            const uint32_t dbar = map_to_rank(smem_addr(&recv_bar[rb]), (uint32_t)lane);
-            st_async_pair(dst, pm, pl, dbar);
-        }
-        if (!abort && !mbar_wait_cluster_bounded(&recv_bar[rb], (uint32_t)((it >> 1) & 1))) {
-            abort = true;
-            flag_timeout();
-        }
-        float qm = kNegInf, ql = 0.0f;
-        if (lane < cs) {
-            const float2 q = recv[rb][lane];
-            qm = q.x;
-            ql = q.y;
-        }
-        group_merge(qm, ql, pow2_ceil(cs));
-        qm = __shfl_sync(0xffffffffu, qm, 0);
-        ql = __shfl_sync(0xffffffffu, ql, 0);
-        const float c = rescale(m, safe_max(qm)) / ql;
-        __syncwarp();
-        if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
-
-        if (!abort) store_row_units<DT, VEC, VPT>(out + row * ldo + c0, tid, tpr, len, v, c);
-    }
-
-    allow_next_grid();  // persistent grid: the next kernel may begin once this CTA is done
-    if (abort && tid == 0 && abort_it >= 0) {
-        for (int64_t j = abort_it; j < abort_it + nslots; ++j) {
-            if (cluster_id + j * n_clusters >= M) break;
-            (void)mbar_wait_bounded(&bars[j % nslots], (uint32_t)((j / nslots) & 1));
-        }
-    }
-    cluster.sync();  // no CTA leaves while a peer's pair may still be in flight to it
-}
-
 // Kernel attributes are per device: the dynamic shared-memory ceiling is
 // raised to the device maximum and the non-portable cluster sizes are
 // allowed, once per device and kernel instance.  Nothing ever lowers them.
@@ -437,23 +263,6 @@ static cudaError_t ensure_wide_attributes() {
     return set_wide_attributes(wide_kernel<DT, VEC, STAGED>, mu, done);
 }
 
-template <int DT, int VPT>
-static cudaError_t ensure_hold_attributes() {
-    static std::mutex mu;
-    static bool done[64] = {};
-    return set_wide_attributes(wide_hold_kernel<DT, VPT>, mu, done);
-}
-
-template <int DT, int VPT>
-static cudaError_t launch_hold_one(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
-                                   int64_t ldo, cudaStream_t s) {
-    cudaError_t err = ensure_hold_attributes<DT, VPT>();
-    if (err != cudaSuccess) return err;
-    // Cluster grids are launched in strict stream order: with programmatic
-    // dependent launch the persistent clusters measured about 10 % slower.
-    return launch_kernel(wide_hold_kernel<DT, VPT>, (unsigned)p.grid, (unsigned)p.block_threads, p.smem_bytes, s,
-                         p.cluster_size, true, in, out, M, N, ldi, ldo, (int)p.chunk_elems, p.stages);
-}
 
 template <int DT, int VEC, bool STAGED>
 static cudaError_t launch_wide_one(const rs_plan& p, const void* in, void* out, int64_t M, int N,
@@ -471,13 +280,7 @@ static cudaError_t launch_wide_dt(const rs_plan& p, const void* in, void* out, i
                                   int64_t ldi, int64_t ldo, cudaStream_t s) {
     constexpr int KV = Traits<DT>::kVec;
     if (p.path == RS_PATH_CLUSTER && p.vec_elems == KV && p.ring_values == RS_RING_REGISTERS) {
-        switch (p.vec_per_thread) {
-            case 1: return launch_hold_one<DT, 1>(p, in, out, M, N, ldi, ldo, s);
-            case 2: return launch_hold_one<DT, 2>(p, in, out, M, N, ldi, ldo, s);
-            case 4: return launch_hold_one<DT, 4>(p, in, out, M, N, ldi, ldo, s);
-            case 8: return launch_hold_one<DT, 8>(p, in, out, M, N, ldi, ldo, s);
-            default: return cudaErrorInvalidConfiguration;
-        }
+        return launch_hold<DT, OpSoftmax>(p, in, out, M, N, ldi, ldo, s, RowArgs{});
     }
     if (p.path == RS_PATH_CLUSTER && p.vec_elems == KV)
         return launch_wide_one<DT, KV, true>(p, in, out, M, N, ldi, ldo, s);
@@ -517,35 +320,11 @@ static cudaError_t max_clusters_one(const rs_plan& p, int* n) {
     return cudaOccupancyMaxActiveClusters(n, kern, &cfg);
 }
 
-template <int DT, int VPT>
-static cudaError_t max_clusters_hold(const rs_plan& p, int* n) {
-    cudaError_t err = ensure_hold_attributes<DT, VPT>();
-    if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.cluster_size, 1, 1);
-    cfg.blockDim = dim3((unsigned)p.block_threads, 1, 1);
-    cfg.dynamicSmemBytes = p.smem_bytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.cluster_size;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(n, wide_hold_kernel<DT, VPT>, &cfg);
-}
-
 template <int DT>
 static cudaError_t max_clusters_dt(const rs_plan& p, int* n) {
     constexpr int KV = Traits<DT>::kVec;
     if (p.path == RS_PATH_CLUSTER && p.ring_values == RS_RING_REGISTERS) {
-        switch (p.vec_per_thread) {
-            case 1: return max_clusters_hold<DT, 1>(p, n);
-            case 2: return max_clusters_hold<DT, 2>(p, n);
-            case 4: return max_clusters_hold<DT, 4>(p, n);
-            case 8: return max_clusters_hold<DT, 8>(p, n);
-            default: return cudaErrorInvalidConfiguration;
-        }
+        return max_clusters_hold<DT, OpSoftmax>(p, n);
     }
     if (p.path == RS_PATH_CLUSTER) return max_clusters_one<DT, KV, true>(p, n);
     if (p.vec_elems == KV) return max_clusters_one<DT, KV, false>(p, n);

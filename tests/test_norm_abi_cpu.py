@@ -31,6 +31,9 @@ def _covers(plan, N):
     units = -(-N // plan["vec_elems"])
     if plan["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING):
         return plan["threads_per_row"] * plan["vec_per_thread"] >= units
+    if plan["path"] == rs.RS_PATH_CLUSTER:  # register-holding clusters: every slice fits its CTA
+        return (plan["ring_values"] == rs.RS_RING_REGISTERS and plan["cluster_size"] * plan["chunk_elems"] >= N
+                and plan["block_threads"] * plan["vec_per_thread"] * plan["vec_elems"] >= plan["chunk_elems"])
     return plan["path"] == rs.RS_PATH_STREAM and plan["cluster_size"] == 1
 
 
@@ -97,10 +100,13 @@ def test_plans_for_typical_hidden_sizes():
         assert p["vec_per_thread"] in NORM_VPT_VEC
         p = _plan(op, 8192, 5000, rs.RS_F32, ld=5120)   # fp32: register rows
         assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 4 and _covers(p, 5000)
-        p = _plan(op, 512, 131072, rs.RS_F16)          # wide rows: one streaming CTA per row
-        assert p["path"] == rs.RS_PATH_STREAM and p["grid"] == 2 * 152 and p["vec_elems"] == 8
-        p = _plan(op, 100, 131072, rs.RS_F16)
-        assert p["grid"] == 100
+        p = _plan(op, 512, 131072, rs.RS_F16)          # wide rows: a cluster per row, slices in registers
+        assert p["path"] == rs.RS_PATH_CLUSTER and p["ring_values"] == rs.RS_RING_REGISTERS
+        assert p["cluster_size"] >= 2 and p["grid"] % p["cluster_size"] == 0 and _covers(p, 131072)
+        p = _plan(op, 512, 131072, rs.RS_F16, a=A + 2)  # misaligned wide rows: one streaming CTA per row
+        assert p["path"] == rs.RS_PATH_STREAM and p["grid"] == 2 * 152 and p["vec_elems"] == 1
+        p = _plan(op, 100, 1 << 22, rs.RS_F32)          # beyond the clusters' registers
+        assert p["path"] == rs.RS_PATH_STREAM and p["grid"] == 100
 
 
 def test_misaligned_parameter_vectors_select_element_wise_kernels():
@@ -113,7 +119,8 @@ def test_misaligned_parameter_vectors_select_element_wise_kernels():
 
 
 def test_paths_without_a_normalisation_kernel():
-    for opts in [{"path": rs.RS_PATH_CLUSTER},
+    for opts in [{"path": rs.RS_PATH_CLUSTER, "ring_values": rs.RS_RING_REREAD},
+                 {"path": rs.RS_PATH_CLUSTER, "force_scalar": 1},
                  {"path": rs.RS_PATH_RING, "ring_values": rs.RS_RING_REREAD},
                  {"path": rs.RS_PATH_STREAM, "cluster_size": 2}]:
         rc, _ = rs.rownorm_plan(rs.RS_OP_RMSNORM, A, OUT, W, None, 64, 4096, 4096, 4096, 1e-6, rs.RS_BF16,
@@ -121,6 +128,8 @@ def test_paths_without_a_normalisation_kernel():
         assert rc == rs.RS_ERR_NO_PATH, opts
     p = _plan(rs.RS_OP_RMSNORM, 64, 4096, rs.RS_BF16, opts={"path": rs.RS_PATH_STREAM})
     assert p["path"] == rs.RS_PATH_STREAM
+    p = _plan(rs.RS_OP_LAYERNORM, 64, 4096, rs.RS_BF16, opts={"path": rs.RS_PATH_CLUSTER, "cluster_size": 4})
+    assert p["path"] == rs.RS_PATH_CLUSTER and p["cluster_size"] == 4 and _covers(p, 4096)
     p = _plan(rs.RS_OP_LAYERNORM, 64, 4096, rs.RS_F32, opts={"path": rs.RS_PATH_ROWS, "threads_per_row": 128,
                                                               "vec_per_thread": 8})
     assert (p["threads_per_row"], p["vec_per_thread"]) == (128, 8)

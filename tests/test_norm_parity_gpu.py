@@ -4,7 +4,8 @@ oracle, through the C ABI.
 Each case makes seeded inputs, weight and bias vectors on the GPU, runs the
 normalisation through the ctypes binding of librowsoftmax.so and compares
 every output element with the oracle under the bound of tests/_parity.py.
-Covered: the register-row, ring and streaming kernels of every storage type,
+Covered: the register-row, ring, register-holding cluster and streaming
+kernels of every storage type,
 forced thread shapes, persistent grids that loop over rows, ragged tails,
 element-wise access (misaligned pointers, odd strides), padded rows with
 guard bands, in-place calls, optional weight and bias, special values, rows
@@ -191,10 +192,31 @@ def test_stream_path(op, dtype, scalar, N, grid_limit):
 
 
 @pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("cs", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("N", [8, 1000, 4104, 65536, 100003])
+@pytest.mark.parametrize("grid_limit", [0, 2])
+def test_cluster_path(op, dtype, cs, N, grid_limit):
+    # Register-holding clusters; cluster sizes that are not powers of two,
+    # slices past the end of short rows (empty CTAs), persistent clusters
+    # looping over rows (grid_limit).
+    x, out = _aligned(7, N, dtype, seed=N + cs, kind="offset50" if op == "ln" else "normal_spike")
+    w, b = _params(N, dtype, seed=cs)
+    opts = {"path": rs.RS_PATH_CLUSTER, "cluster_size": cs, "grid_limit": grid_limit * cs}
+    ok, plan = _servable(op, x, w, b, opts)
+    if not ok:
+        pytest.skip("slice does not fit a CTA's registers at this cluster size")
+    assert plan["ring_values"] == rs.RS_RING_REGISTERS
+    y = _run(op, x, w, b, out=out, options=opts)
+    _check(op, x, y, w, b, what=f"{op} cluster {dtype} N={N} cs={cs}")
+
+
+@pytest.mark.parametrize("op", OPS)
 def test_paths_agree_on_the_same_input(op):
     x, _ = _aligned(64, 3000, "bf16", seed=11)
     w, b = _params(3000, "bf16", seed=11)
-    ys = [_run(op, x, w, b, options={"path": p}) for p in (rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_STREAM)]
+    ys = [_run(op, x, w, b, options={"path": p})
+          for p in (rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_CLUSTER, rs.RS_PATH_STREAM)]
     for y in ys:
         _check(op, x, y, w, b, what=f"{op} paths")
 
@@ -234,7 +256,8 @@ def test_misaligned_pointers_use_element_wise_access(op, dtype, shift):
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("N", [100, 8192, 70000])
-@pytest.mark.parametrize("path", [rs.RS_PATH_AUTO, rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_STREAM])
+@pytest.mark.parametrize("path", [rs.RS_PATH_AUTO, rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_CLUSTER,
+                                  rs.RS_PATH_STREAM])
 def test_in_place(op, dtype, N, path):
     x, _ = _aligned(12, N, dtype, seed=N)
     w, b = _params(N, dtype, seed=N)
@@ -250,7 +273,7 @@ def test_in_place(op, dtype, N, path):
 
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_STREAM])
+@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING, rs.RS_PATH_CLUSTER, rs.RS_PATH_STREAM])
 def test_special_values(op, dtype, path):
     M, N = 8, 1000
     x, out = _aligned(M, N, dtype, seed=9)
