@@ -173,8 +173,10 @@ int64_t ctas_per_sm(const rs_device_info& dev, int block, size_t smem, int regs_
     return n < 1 ? 1 : n;
 }
 
+// RS_PATH_RING.  `nparams` parameter vectors (LayerNorm's weight and bias)
+// are staged in shared memory after the stages, padded to whole units.
 int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_options& o,
-              const rs_device_info& dev, rs_plan* p) {
+              const rs_device_info& dev, rs_plan* p, int nparams = 0) {
     if (vec == 1) return RS_ERR_NO_PATH;  // bulk copies need 16-byte units
     if (o.stages && (o.stages < 2 || o.stages > rs::kRingMaxStages)) return RS_ERR_INVALID_ARG;
     if (o.ring_values < RS_RING_AUTO || o.ring_values > RS_RING_REREAD) return RS_ERR_INVALID_ARG;
@@ -189,7 +191,7 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     if (stage <= 0) return RS_ERR_NO_PATH;
     const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kRingStaticSmem;
     const int stages = o.stages ? o.stages : kRingDefaultStages;
-    const int64_t smem = stage * stages;
+    const int64_t smem = stage * stages + (int64_t)nparams * round_up(N, vec) * elem_size(dtype);
     if (smem > max_dyn || stage >= (1 << 20)) return RS_ERR_NO_PATH;  // mbarrier tx count < 2^20
     const int regs = values == RS_RING_REREAD ? rs::kRingRereadRegs
                      : (rs::rows_block_limit(p->vec_per_thread, vec) == 1024 ? 64 : 128);
@@ -403,6 +405,8 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
     const int vec = vec_ok ? kvec : 1;
     const int64_t units = ceil_div(N, vec);
     const bool norm = op != RS_OP_SOFTMAX;
+    // Parameter vectors the ring kernel stages in shared memory (LayerNorm's).
+    const int nparams = op == RS_OP_LAYERNORM ? (w ? 1 : 0) + (b ? 1 : 0) : 0;
 
     int path = o.path;
     if (path == RS_PATH_AUTO) {
@@ -411,7 +415,7 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         // registers); fp32 rows: the register kernel, whose fp32 values cost
         // no more registers than the bytes they came from.
         if (dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes && N * es <= kRowsMaxRowBytes)
-            rc = plan_ring(dtype, vec, M, N, units, o, *dev, p);
+            rc = plan_ring(dtype, vec, M, N, units, o, *dev, p, nparams);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
         if (N * es <= kRowsMaxRowBytes) rc = plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
@@ -433,7 +437,7 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         return plan_wide(dtype, RS_PATH_STREAM, vec, M, N, o, *dev, p);
     }
     if (path == RS_PATH_ROWS) return plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
-    if (path == RS_PATH_RING) return plan_ring(dtype, vec, M, N, units, o, *dev, p);
+    if (path == RS_PATH_RING) return plan_ring(dtype, vec, M, N, units, o, *dev, p, nparams);
     if (norm) {
         if (path == RS_PATH_STREAM) return plan_norm_stream(vec, M, o, *dev, p);
         // Clusters serve the normalisations with the slice in registers only.

@@ -114,6 +114,10 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
         for (int j = 0; j < nslots; ++j)
             if (cluster_id + j * n_clusters < M) issue(cluster_id + j * n_clusters, j);
     }
+    // Normalisations read their weight and bias units through the read-only
+    // cache (staging the slice in shared memory measured no faster and cost
+    // resident CTAs).
+    const GlobalParams prm{args.w, args.b, args.eps, N, c0};
     cluster.sync();  // every CTA's receive barriers are armed before any pair is sent
 
     bool abort = false;
@@ -268,10 +272,10 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int base = c0 + (tid + k * tpr) * VEC;
+                const int base = (tid + k * tpr) * VEC;  // within the slice
                 float w[VEC], b[VEC];
-                load_param_unit<DT, VEC>(args.w, base, N, w, 1.0f);
-                if constexpr (OP::kOp == RS_OP_LAYERNORM) load_param_unit<DT, VEC>(args.b, base, N, b, 0.0f);
+                prm.template w_unit<DT, VEC>(base, w);
+                if constexpr (OP::kOp == RS_OP_LAYERNORM) prm.template b_unit<DT, VEC>(base, b);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     if constexpr (OP::kOp == RS_OP_RMSNORM) v[k][e] = v[k][e] * r * w[e];

@@ -163,11 +163,76 @@ __device__ __forceinline__ float thread_sum(const float (&v)[VPT][VEC], F f) {
     return acc[0];
 }
 
+// Where a normalisation reads its weight and bias units.  GlobalParams: the
+// caller's vectors in global memory (read-only cache), with 1 and 0 for a
+// null vector or past n.  SharedParams: copies staged once per CTA in shared
+// memory by a persistent kernel, padded to whole 16-byte units with 1 and 0,
+// read at unit offsets relative to the staged range.
+struct GlobalParams {
+    const void* w;
+    const void* b;
+    float eps;
+    int n;
+    int offset;  // element of the vectors that unit offset 0 refers to
+    template <int DT, int VEC>
+    __device__ __forceinline__ void w_unit(int base, float* f) const {
+        load_param_unit<DT, VEC>(w, offset + base, n, f, 1.0f);
+    }
+    template <int DT, int VEC>
+    __device__ __forceinline__ void b_unit(int base, float* f) const {
+        load_param_unit<DT, VEC>(b, offset + base, n, f, 0.0f);
+    }
+};
+
+template <int DT>
+struct SharedParams {
+    using S = typename Traits<DT>::storage;
+    const S* w;  // shared memory, or null for weight 1
+    const S* b;  // shared memory, or null for bias 0
+    float eps;
+    int padded;  // staged elements; units at or past it read 1 and 0
+    template <int DT2, int VEC>
+    __device__ __forceinline__ void w_unit(int base, float* f) const {
+        static_assert(VEC == Traits<DT>::kVec, "staged parameters are read in whole units");
+        if (w && base < padded) {
+            Traits<DT>::unpack(*reinterpret_cast<const uint4*>(w + base), f);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) f[e] = 1.0f;
+        }
+    }
+    template <int DT2, int VEC>
+    __device__ __forceinline__ void b_unit(int base, float* f) const {
+        static_assert(VEC == Traits<DT>::kVec, "staged parameters are read in whole units");
+        if (b && base < padded) {
+            Traits<DT>::unpack(*reinterpret_cast<const uint4*>(b + base), f);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) f[e] = 0.0f;
+        }
+    }
+};
+
+// Copies the elements [c0, c0 + len) of a parameter vector into shared memory
+// `dst`, padded with `pad` up to `padded` elements (all threads of the CTA;
+// the caller synchronises before reading).  A null source stages nothing.
+template <int DT>
+__device__ __forceinline__ void stage_param(typename Traits<DT>::storage* dst, const void* src, int c0, int len,
+                                            int padded, float pad) {
+    using S = typename Traits<DT>::storage;
+    const S* q = static_cast<const S*>(src) + c0;
+    S padv;
+    if constexpr (DT == RS_F32) padv = pad;
+    else if constexpr (DT == RS_BF16) padv = __float2bfloat16_rn(pad);
+    else padv = __float2half_rn(pad);
+    for (int i = threadIdx.x; i < padded; i += blockDim.x) dst[i] = i < len ? q[i] : padv;
+}
+
 struct OpSoftmax {
     static constexpr int kOp = RS_OP_SOFTMAX;
     static constexpr float kFill = kNegInf;
-    template <int DT, int VEC, int VPT>
-    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int, int tpr, int, bool, const RowArgs&,
+    template <int DT, int VEC, int VPT, typename P>
+    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int, int tpr, int, bool, const P&,
                                                  float2* part) {
         const float c = row_exp_and_scale<VPT, VEC>(v, tpr, part);
 #pragma unroll
@@ -182,16 +247,16 @@ struct OpSoftmax {
 struct OpRmsNorm {
     static constexpr int kOp = RS_OP_RMSNORM;
     static constexpr float kFill = 0.0f;  // absent elements add nothing to the sum of squares
-    template <int DT, int VEC, int VPT>
+    template <int DT, int VEC, int VPT, typename P>
     __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool,
-                                                 const RowArgs& a, float2* part) {
+                                                 const P& a, float2* part) {
         float s = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return fmaf(x, x, acc); });
         s = row_sum<0>(s, tpr, part);
         const float r = 1.0f / sqrtf(s / (float)n + a.eps);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             float w[VEC];
-            load_param_unit<DT, VEC>(a.w, (t + k * tpr) * VEC, n, w, 1.0f);
+            a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) v[k][e] = v[k][e] * r * w[e];
         }
@@ -204,9 +269,9 @@ struct OpRmsNorm {
 struct OpLayerNorm {
     static constexpr int kOp = RS_OP_LAYERNORM;
     static constexpr float kFill = 0.0f;
-    template <int DT, int VEC, int VPT>
+    template <int DT, int VEC, int VPT, typename P>
     __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool whole,
-                                                 const RowArgs& a, float2* part) {
+                                                 const P& a, float2* part) {
         float s = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return acc + x; });
         const float mean = row_sum<0>(s, tpr, part) / (float)n;
         float d;
@@ -227,8 +292,8 @@ struct OpLayerNorm {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             float w[VEC], b[VEC];
-            load_param_unit<DT, VEC>(a.w, (t + k * tpr) * VEC, n, w, 1.0f);
-            load_param_unit<DT, VEC>(a.b, (t + k * tpr) * VEC, n, b, 0.0f);
+            a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
+            a.template b_unit<DT, VEC>((t + k * tpr) * VEC, b);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
         }

@@ -45,7 +45,8 @@ rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         const bool active = row < M;
         float v[VPT][VEC];
         load_row_units<DT, VEC, VPT>(in + (active ? row : 0) * ldi, t, tpr, N, active, v, OP::kFill);
-        OP::template apply<DT, VEC, VPT>(v, t, tpr, N, whole, args, part[it & 1]);
+        OP::template apply<DT, VEC, VPT>(v, t, tpr, N, whole, GlobalParams{args.w, args.b, args.eps, N, 0},
+                                         part[it & 1]);
         if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v);
     }
 }

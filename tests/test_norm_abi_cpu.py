@@ -109,6 +109,19 @@ def test_plans_for_typical_hidden_sizes():
         assert p["path"] == rs.RS_PATH_STREAM and p["grid"] == 100
 
 
+def test_layernorm_ring_stages_its_vectors_in_shared_memory():
+    # LayerNorm's ring CTAs copy weight and bias into shared memory once, after
+    # the ring stages (padded to whole 16-byte units); RMSNorm's do not.
+    N = 2047
+    p = _plan(rs.RS_OP_LAYERNORM, 1 << 20, N, rs.RS_BF16, ld=2048, b=B)
+    stage = (N // 8) * 16 * p["rows_per_cta"]
+    assert p["path"] == rs.RS_PATH_RING and p["smem_bytes"] == stage * p["stages"] + 2 * 2048 * 2
+    p = _plan(rs.RS_OP_LAYERNORM, 1 << 20, N, rs.RS_BF16, ld=2048, w=None, b=B)
+    assert p["smem_bytes"] == stage * p["stages"] + 2048 * 2
+    p = _plan(rs.RS_OP_RMSNORM, 1 << 20, N, rs.RS_BF16, ld=2048)
+    assert p["smem_bytes"] == stage * p["stages"]
+
+
 def test_misaligned_parameter_vectors_select_element_wise_kernels():
     p = _plan(rs.RS_OP_RMSNORM, 64, 4096, rs.RS_BF16, w=W + 2)
     assert p["vec_elems"] == 1 and p["path"] == rs.RS_PATH_ROWS and p["vec_per_thread"] in NORM_VPT_SCALAR
