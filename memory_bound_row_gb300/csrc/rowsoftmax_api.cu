@@ -31,6 +31,7 @@ constexpr int64_t kMaxGrid = (int64_t)INT_MAX;
 
 // Auto-planner knobs.
 constexpr int kRowsTargetValues = 32;             // fp32 values a thread holds (auto)
+constexpr int kRowsTargetValuesLn16 = 64;         // ... for LayerNorm on 16-bit rows (measured faster)
 constexpr int kRowsMaxSingleWarpValues = 64;      // ... up to this many when it keeps a row in one warp
 constexpr int64_t kRowsMaxRowBytes = 32 * 1024;   // auto: rows up to this go to RS_PATH_ROWS
 constexpr int64_t kClusterTargetSlice = 64 * 1024;  // auto: bytes of row slice per CTA
@@ -102,7 +103,9 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
         } else {
             int n_inst = 0;
             const int* inst = vpt_table(p->op, dtype, vec, &n_inst);
-            int vt = kRowsTargetValues / vec > 0 ? kRowsTargetValues / vec : 1;
+            const int target =
+                p->op == RS_OP_LAYERNORM && dtype != RS_F32 && vec > 1 ? kRowsTargetValuesLn16 : kRowsTargetValues;
+            int vt = target / vec > 0 ? target / vec : 1;
             if (vt > inst[n_inst - 1]) vt = inst[n_inst - 1];
             // 16-bit rows that one warp can hold at up to 64 values a thread
             // stay in one warp: no CTA barrier per row (measured faster).
@@ -217,9 +220,14 @@ int plan_cluster_hold(int dtype, int vec, int64_t M, int64_t N, const rs_options
     int cs = o.cluster_size;
     int block = 0, vpt = 0;
     int64_t chunk = 0;
-    // Candidate (threads, units a thread) shapes, most values a thread first;
-    // 8 units a thread are compiled for 256-thread CTAs only.
-    static const int kShapes[][2] = {{256, 8}, {512, 4}, {256, 4}, {512, 2}, {256, 2}, {512, 1}, {256, 1}};
+    // Candidate (threads, units a thread) shapes, in order of preference among
+    // equally tight fits: the softmax holds most values a thread, the
+    // normalisations (more per-row instructions after the exchange) prefer more
+    // threads (both measured); 8 units a thread are compiled for 256-thread
+    // CTAs only.
+    static const int kShapesSoftmax[][2] = {{256, 8}, {512, 4}, {256, 4}, {512, 2}, {256, 2}, {512, 1}, {256, 1}};
+    static const int kShapesNorm[][2] = {{512, 4}, {256, 8}, {512, 2}, {256, 4}, {512, 1}, {256, 2}, {256, 1}};
+    const auto& kShapes = p->op == RS_OP_SOFTMAX ? kShapesSoftmax : kShapesNorm;
     for (int c = cs ? cs : 1; c <= (cs ? cs : rs::kMaxCluster); c <<= 1) {
         chunk = round_up(ceil_div(N, c), vec);
         const int64_t units = chunk / vec;
