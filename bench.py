@@ -511,6 +511,107 @@ def run_ours(args, workloads):
         dist.destroy_process_group()
 
 
+SWEEP_CONFIGS = {
+    # name: rs_options (None: the planner's choice).  grid_limit -1 means "one
+    # wave of resident CTAs" and is resolved per shape.
+    "auto": None,
+    "rows, one CTA per row group": {"path": 1},
+    "rows, persistent": {"path": 1, "grid_limit": -1},
+    "ring (bulk copies, persistent)": {"path": 4},
+}
+
+
+def run_sweep_n(args):
+    """The N sweep of the Hugging Face skill page's benchmark harness (fp32
+    randn, M = 4096, N = 128 i for i = 2..99) on this library: every point of
+    every configuration is first checked (finite, row sums 1 within 1e-5, and
+    equal to the planner's configuration within 1e-6 element-wise; the
+    configurations themselves are covered by the parity tests), then timed as
+    graph-replayed back-to-back launches over rotating buffers (more than 4x
+    L2 between two uses of a buffer).  One JSON line per (N, configuration)."""
+    import torch
+
+    import memory_bound_row_gb300 as rs
+    from memory_bound_row_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = rs._abi.load()
+    peak, _ = measured_peaks()
+    rc, info = rs.rowsoftmax_device_info()
+    M = 4096
+    for i in range(2, 100):
+        N = 128 * i
+        w = W.custom(M, N, "f32", seed=0, kind="normal1")
+        x0 = W.generate(w, dev)
+        set_bytes = 2 * M * N * 4
+        nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
+        xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
+        ys = [torch.empty_like(x0) for _ in range(nsets)]
+        first = None
+        for name, opts in SWEEP_CONFIGS.items():
+            o = dict(opts) if opts else None
+            if o and o.get("grid_limit") == -1:
+                o["grid_limit"] = 0
+                rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), M, N, N, N, rs.RS_F32, o, info)
+                if rc != rs.RS_OK:
+                    continue
+                per_sm = max(1, info.max_threads_per_sm // plan["block_threads"])
+                o["grid_limit"] = info.sm_count * per_sm
+            rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), M, N, N, N, rs.RS_F32, o, info)
+            if rc != rs.RS_OK:
+                continue
+            copts = rs._abi._opts(o)
+            stream = torch.cuda.Stream(dev)
+            h = stream.cuda_stream
+
+            def call(k):
+                r = lib.rowsoftmax_fwd_ex(xs[k % nsets].data_ptr(), ys[k % nsets].data_ptr(), M, N, N, N,
+                                          rs.RS_F32, h, copts)
+                if r != rs.RS_OK:
+                    raise rs.RowSoftmaxError(r, rs.rowsoftmax_last_cuda_error())
+
+            with torch.cuda.stream(stream):
+                call(0)
+            stream.synchronize()
+            y = ys[0].double()
+            sums_err = float((y.sum(dim=1) - 1.0).abs().max())
+            err = 0.0 if first is None else float((y - first).abs().max())
+            if first is None:
+                first = y.clone()
+            if not (bool(torch.isfinite(y).all()) and sums_err <= 1e-5 and err <= 1e-6):
+                raise AssertionError(f"N={N} {name}: row sums off by {sums_err:.3e}, {err:.3e} from the planner's")
+            G = 20
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for k in range(G):
+                    call(k)
+                stream.synchronize()
+                with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+                    for k in range(G):
+                        call(k)
+            torch.cuda.synchronize()
+            reps = max(3, args.steps // G)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / (reps * G)
+            gbs = 2 * M * N * 4 / (ms * 1e-3) / 1e9
+            print(json.dumps({"sweep": "fp32 M=4096 N=128i", "N": N, "config": name, "kernel": rs.PATH_NAMES[plan["path"]],
+                              "grid": plan["grid"], "block": plan["block_threads"], "us": round(ms * 1e3, 3),
+                              "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "max_rowsum_err": sums_err}), flush=True)
+            del graph
+        del xs, ys, first
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -526,6 +627,9 @@ def main():
                     help="JSON object of rs_options fields forcing a kernel configuration (tuning, profiling)")
     ap.add_argument("--rows", type=int, default=0,
                     help="use only the first ROWS rows of the workload (smaller profiler captures)")
+    ap.add_argument("--sweep-n", action="store_true",
+                    help="instead of the benchmark line: the fp32 M=4096, N=256..12672 sweep of the row softmax, "
+                         "one JSON line per (N, kernel configuration)")
     args = ap.parse_args()
     args.options = json.loads(args.options) if args.options else None
     if args.warmup < 3:
@@ -536,7 +640,9 @@ def main():
     for n in names:
         if n not in W.WORKLOADS:
             raise SystemExit(f"unknown workload {n}; choose from {', '.join(W.ORDER)} or 'all'")
-    if args.impl == "reference":
+    if args.sweep_n:
+        run_sweep_n(args)
+    elif args.impl == "reference":
         run_reference(args, names)
     else:
         run_ours(args, names)
