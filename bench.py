@@ -548,6 +548,7 @@ def run_sweep_n(args):
         nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
         xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
         ys = [torch.empty_like(x0) for _ in range(nsets)]
+        torch.cuda.synchronize()  # the inputs are made on torch's stream; the timed calls run on their own
         first = None
         for name, opts in SWEEP_CONFIGS.items():
             o = dict(opts) if opts else None

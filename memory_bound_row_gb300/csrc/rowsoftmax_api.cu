@@ -34,6 +34,7 @@ constexpr int kRowsTargetValues = 32;             // fp32 values a thread holds 
 constexpr int kRowsTargetValuesLn16 = 64;         // ... for LayerNorm on 16-bit rows (measured faster)
 constexpr int kRowsMaxSingleWarpValues = 64;      // ... up to this many when it keeps a row in one warp
 constexpr int64_t kRowsMaxRowBytes = 32 * 1024;   // auto: rows up to this go to RS_PATH_ROWS
+constexpr int64_t kRowsMaxRowBytesF32 = 64 * 1024;  // ... fp32 softmax rows (measured: rows beat clusters to 64 KB)
 constexpr int64_t kClusterTargetSlice = 64 * 1024;  // auto: bytes of row slice per CTA
 constexpr int64_t kRingMinRowBytes = 512;           // auto: shorter rows stay on RS_PATH_ROWS
 constexpr int kRingDefaultStages = 2;               // auto: more stages cost resident CTAs (measured)
@@ -228,28 +229,41 @@ int plan_cluster_hold(int dtype, int vec, int64_t M, int64_t N, const rs_options
     static const int kShapesSoftmax[][2] = {{256, 8}, {512, 4}, {256, 4}, {512, 2}, {256, 2}, {512, 1}, {256, 1}};
     static const int kShapesNorm[][2] = {{512, 4}, {256, 8}, {512, 2}, {256, 4}, {512, 1}, {256, 2}, {256, 1}};
     const auto& kShapes = p->op == RS_OP_SOFTMAX ? kShapesSoftmax : kShapesNorm;
-    for (int c = cs ? cs : 1; c <= (cs ? cs : rs::kMaxCluster); c <<= 1) {
-        chunk = round_up(ceil_div(N, c), vec);
-        const int64_t units = chunk / vec;
+    // Cluster size: the smallest whose slices fill a CTA shape to at least 7/8
+    // (idle lanes cost as much as busy ones on a latency-bound row), else the
+    // best fill; any size 1..16, not only powers of two (measured: bf16 rows of
+    // 24576 at 3 CTAs fill 256 x 4 exactly).
+    double best_fill = 0.0;
+    int best_c = 0;
+    for (int c = cs ? cs : 1; c <= (cs ? cs : rs::kMaxCluster); ++c) {
+        const int64_t ch = round_up(ceil_div(N, c), vec);
+        const int64_t units = ch / vec;
+        int b = 0, v = 0;
         int64_t best_cap = 0;
         for (const auto& sh : kShapes) {
             if (o.block_threads && sh[0] != o.block_threads) continue;
             if (o.vec_per_thread && sh[1] != o.vec_per_thread) continue;
             const int64_t cap = (int64_t)sh[0] * sh[1];
             if (cap < units) continue;
-            if (!vpt || cap < best_cap) {  // the tightest fit; ties keep the earlier (more values a thread)
-                block = sh[0];
-                vpt = sh[1];
+            if (!v || cap < best_cap) {  // the tightest fit; ties keep the earlier shape
+                b = sh[0];
+                v = sh[1];
                 best_cap = cap;
             }
         }
-        if (vpt) {
-            cs = c;
-            break;
+        if (!v) continue;
+        const double fill = (double)units / (double)best_cap;
+        if (fill > best_fill + 1e-9) {
+            best_fill = fill;
+            block = b;
+            vpt = v;
+            chunk = ch;
+            best_c = c;
         }
-        if (cs) break;
+        if (fill >= 0.875) break;
     }
     if (!vpt) return RS_ERR_NO_PATH;
+    cs = best_c;
     const size_t slot = (size_t)round_up(chunk * es, 16);
     const int64_t resident_ctas = (int64_t)dev.sm_count * ctas_per_sm(dev, block, 2 * slot, vpt == 8 ? 128 : 64);
     int64_t clusters = resident_ctas / cs;
@@ -422,11 +436,17 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         // 16-bit rows: the ring (bytes in flight in shared memory, not in
         // registers); fp32 rows: the register kernel, whose fp32 values cost
         // no more registers than the bytes they came from.
-        if (dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes && N * es <= kRowsMaxRowBytes)
+        // (A 16-bit softmax row of 32 KB already goes faster through the
+        // register-holding clusters: 6156 vs 5940 GB/s measured.)
+        const int64_t ring_max = norm ? kRowsMaxRowBytes : kRowsMaxRowBytes - 1;
+        if (dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes && N * es <= ring_max)
             rc = plan_ring(dtype, vec, M, N, units, o, *dev, p, nparams);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
-        if (N * es <= kRowsMaxRowBytes) rc = plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
+        const int64_t rows_max = dtype == RS_F32 && !norm ? kRowsMaxRowBytesF32
+                                 : dtype != RS_F32 && !norm && vec_ok ? kRowsMaxRowBytes - 1
+                                                                      : kRowsMaxRowBytes;
+        if (N * es <= rows_max) rc = plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
         if (norm) {
