@@ -58,6 +58,10 @@ def _load():
             lib.orc_decode_array.restype = None
             lib.orc_encode_array.argtypes = [vp, ctypes.c_int, i64, vp]
             lib.orc_encode_array.restype = None
+            lib.orc_softmax_prefix_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, vp, i64]
+            lib.orc_softmax_prefix_f64.restype = ctypes.c_int
+            lib.orc_prefix_len.argtypes = [i64, i64, i64, i64]
+            lib.orc_prefix_len.restype = i64
             lib.orc_rmsnorm_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, ctypes.c_double, vp, i64]
             lib.orc_rmsnorm_f64.restype = ctypes.c_int
             lib.orc_layernorm_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp, ctypes.c_double, vp, i64]
@@ -87,6 +91,28 @@ def softmax_f64(x: np.ndarray, fmt: str, n_cols: int | None = None) -> np.ndarra
     if rc != 0:
         raise ValueError(f"oracle rejected the call (status {rc})")
     return y
+
+
+def softmax_prefix_f64(x: np.ndarray, fmt: str, period: int, offset: int = 0, n_cols: int | None = None,
+                       row0: int = 0) -> np.ndarray:
+    """Row softmax under a causal mask: the rows of ``x`` are rows row0, row0 + 1,
+    ... of the masked tensor; row r keeps its first
+    min(N, max(0, (r mod period) + 1 + offset)) elements, the rest is 0 in the
+    result and never read."""
+    x = _as_storage(np.atleast_2d(x), fmt)
+    M, ld = x.shape
+    N = ld if n_cols is None else int(n_cols)
+    y = np.empty((M, N), dtype=np.float64)
+    rc = _load().orc_softmax_prefix_f64(x.ctypes.data, FORMATS[fmt], M, N, ld, int(row0), int(period), int(offset),
+                                        y.ctypes.data, N)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the call (status {rc})")
+    return y
+
+
+def prefix_len(r: int, n: int, period: int, offset: int = 0) -> int:
+    """L_r of softmax_prefix_f64."""
+    return int(_load().orc_prefix_len(int(r), int(n), int(period), int(offset)))
 
 
 def softmax_store(x: np.ndarray, fmt: str, n_cols: int | None = None, nthreads: int = 1,

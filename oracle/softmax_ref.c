@@ -29,7 +29,10 @@
  *  - output encoding to fp16 / bf16 is round-to-nearest, ties-to-even, done
  *    directly from the double result (no intermediate fp32 rounding).
  *
- * It also holds the plain definitions of RMSNorm and LayerNorm (end of file).
+ * It also holds the plain definitions of RMSNorm and LayerNorm (end of file),
+ * and the row softmax over a prefix of every row (a causal attention mask):
+ * row r keeps its first L_r elements, the rest is treated as -inf and never
+ * read.
  *
  * Parity pins for this file live in tests/test_oracle_pins.py and
  * tests/test_oracle_norm_pins.py.
@@ -188,6 +191,51 @@ int orc_softmax_f64(const void* x, int dtype, int64_t M, int64_t N, int64_t ldx,
     for (int64_t r = 0; r < M; ++r) {
         for (int64_t j = 0; j < N; ++j) xr[j] = orc_load(x, dtype, r * ldx + j);
         orc_row(xr, N, y + r * ldy);
+    }
+    free(xr);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * The row softmax under a causal mask, the attention-score example of the
+ * mohakchugh.is-a.dev post ("How Flash Attention Uses Triton": a softmax that
+ * skips the fully masked causal region).  For scores [B, H, S_q, S_k] viewed
+ * as (B*H*S_q) x S_k rows, row r is query position q = r mod S_q and may see
+ * keys k <= q + (S_k - S_q).  In general, with period P > 0 and diagonal
+ * offset D, row r keeps
+ *     L_r = min(N, max(0, (r mod P) + 1 + D))
+ * elements; the masked ones are -inf by definition, so
+ *     y[r][j] = exp(x[r][j] - m_r) / sum_{k < L_r} exp(x[r][k] - m_r)  (j < L_r)
+ *     y[r][j] = 0                                                      (j >= L_r)
+ * with m_r the max of the kept elements; L_r = 0 is an all -inf row: NaN.
+ * The masked elements are never read (they may hold anything).
+ * ------------------------------------------------------------------------- */
+int64_t orc_prefix_len(int64_t r, int64_t N, int64_t period, int64_t offset)
+{
+    int64_t L = r % period + 1 + offset;
+    if (L < 0) L = 0;
+    if (L > N) L = N;
+    return L;
+}
+
+/* Rows r = row0 .. row0 + M - 1 of the masked tensor (x and y point at row row0). */
+int orc_softmax_prefix_f64(const void* x, int dtype, int64_t M, int64_t N, int64_t ldx, int64_t row0,
+                           int64_t period, int64_t offset, double* y, int64_t ldy)
+{
+    if (orc_check(dtype, M, N, ldx, ldy) || period <= 0 || row0 < 0) return 1;
+    if (M == 0 || N == 0) return 0;
+    double* xr = (double*)malloc((size_t)N * sizeof(double));
+    if (!xr) return 2;
+    for (int64_t r = 0; r < M; ++r) {
+        const int64_t L = orc_prefix_len(row0 + r, N, period, offset);
+        double* yr = y + r * ldy;
+        if (L == 0) {
+            for (int64_t j = 0; j < N; ++j) yr[j] = NAN;
+            continue;
+        }
+        for (int64_t j = 0; j < L; ++j) xr[j] = orc_load(x, dtype, r * ldx + j);
+        orc_row(xr, L, yr);
+        for (int64_t j = L; j < N; ++j) yr[j] = 0.0;
     }
     free(xr);
     return 0;
