@@ -308,6 +308,7 @@ def cpu_baseline(w, x_dev, op: str = "softmax", seconds: float = 3.0) -> dict:
 
 
 def run_ours(args, workloads):
+    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -344,6 +345,8 @@ def run_ours(args, workloads):
             p_b = ctypes.c_void_p(bs.data_ptr()) if op == "layernorm" else None
 
         def call(a, b, st):
+            if op == "softmax" and args.causal:
+                return lib.rowsoftmax_causal_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, w.N, 0, code, st, opts)
             if op == "softmax":
                 return lib.rowsoftmax_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, code, st, opts)
             return lib.rownorm_fwd_ex(OP_CODES[op], a, b, p_w, p_b, w.M, w.N, w.ld, w.ld, OP_EPS[op], code, st,
@@ -406,6 +409,10 @@ def run_ours(args, workloads):
 
         ms_per_step = total_ms / args.steps
         nbytes = op_bytes(op, w)
+        if args.causal:  # the masked part is never read: kept elements read, every element written
+            kept = int(np.minimum(np.arange(w.M, dtype=np.int64) % w.N + 1, w.N).sum())
+            dense_bytes = nbytes
+            nbytes = (kept + w.M * w.N) * w.elem_size
         value = job_gbs(world, nbytes, args.steps, total_ms)
         achieved = nbytes / (kern_ms * 1e-3) / 1e9
 
@@ -465,7 +472,10 @@ def run_ours(args, workloads):
 
         if rank == 0:
             rc, info = rs.rowsoftmax_device_info()
-            if op == "softmax":
+            if op == "softmax" and args.causal:
+                rc, plan = rs.rowsoftmax_causal_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, w.N,
+                                                     0, code, args.options, info)
+            elif op == "softmax":
                 rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code,
                                               args.options, info)
             else:
@@ -499,6 +509,11 @@ def run_ours(args, workloads):
                                "output copied back, every step; "
                                "two buffer pairs overlap step i+1's copy-in with step i"},
                 "gpu_launches": args.steps,
+                **({"causal": {"period": w.N, "diag_offset": 0, "bytes_per_step": nbytes,
+                               "dense_bytes_per_step": dense_bytes,
+                               "dense_equivalent_gbs": round(job_gbs(world, dense_bytes, args.steps, total_ms), 2),
+                               "how": "rowsoftmax_causal_fwd: row r keeps (r mod N) + 1 elements; the masked part "
+                                      "is never read and is written as 0"}} if args.causal else {}),
                 "timing": f"{args.steps // G} replays of a CUDA graph of {G} launches, one event pair",
                 "clocks": clocks,
             }
@@ -628,11 +643,16 @@ def main():
                     help="JSON object of rs_options fields forcing a kernel configuration (tuning, profiling)")
     ap.add_argument("--rows", type=int, default=0,
                     help="use only the first ROWS rows of the workload (smaller profiler captures)")
+    ap.add_argument("--causal", action="store_true",
+                    help="softmax only: time rowsoftmax_causal_fwd with a square causal mask (row r keeps its first "
+                         "(r mod N) + 1 elements, the rest is never read); bytes count the kept reads and all writes")
     ap.add_argument("--sweep-n", action="store_true",
                     help="instead of the benchmark line: the fp32 M=4096, N=256..12672 sweep of the row softmax, "
                          "one JSON line per (N, kernel configuration)")
     args = ap.parse_args()
     args.options = json.loads(args.options) if args.options else None
+    if args.causal and args.op != "softmax":
+        raise SystemExit("--causal applies to the softmax only")
     if args.warmup < 3:
         args.warmup = 3
     from memory_bound_row_gb300 import workloads as W

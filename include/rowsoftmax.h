@@ -150,6 +150,7 @@ typedef struct {
     int withhold_copies;  /* copied from rs_options */
     int op;               /* rs_op the plan serves */
     int strict_order;     /* copied from rs_options */
+    int masked;           /* 1 for rowsoftmax_causal_* plans */
 } rs_plan;
 
 /* Device facts the planner needs; rowsoftmax_plan takes them explicitly so
@@ -193,6 +194,42 @@ RS_API int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N,
 RS_API int rowsoftmax_plan(const void* in, const void* out, int64_t M, int64_t N,
                     int64_t in_row_stride, int64_t out_row_stride, int dtype,
                     const rs_options* opts, const rs_device_info* dev, rs_plan* plan);
+
+/*
+ * Row softmax under a causal mask, without reading the masked part: the
+ * attention-score softmax that skips the fully masked causal region (the
+ * mohakchugh.is-a.dev post, "How Flash Attention Uses Triton").  Row r keeps
+ * its first
+ *
+ *     L_r = min(N, max(0, (r mod period) + 1 + diag_offset))
+ *
+ * elements: y[r][j] is the softmax of those L_r values for j < L_r and exactly
+ * 0 for j >= L_r.  Elements at j >= L_r are never read (they may hold
+ * anything, NaN included); every output element is written.  For attention
+ * scores [B, H, S_q, S_k] stored as (B*H*S_q) x S_k rows: period = S_q and
+ * diag_offset = S_k - S_q.  L_r == 0 is an all -inf row: NaN.  Data model,
+ * ownership, asynchrony and errors are those of rowsoftmax_fwd; period < 1 or
+ * |diag_offset| > 2^62 is RS_ERR_INVALID_ARG.  The register-row, ring and
+ * register-holding cluster kernels implement the mask; a shape that only the
+ * streaming kernels could serve (rows wider than the clusters hold, or wide
+ * rows without 16-byte alignment) returns RS_ERR_NO_PATH.
+ */
+RS_API int rowsoftmax_causal_fwd(const void* in, void* out, int64_t M, int64_t N,
+                                 int64_t in_row_stride, int64_t out_row_stride, int64_t period,
+                                 int64_t diag_offset, int dtype, cudaStream_t stream);
+
+/* rowsoftmax_causal_fwd with forcing options (RS_PATH_STREAM and
+ * RS_RING_REREAD, ring or cluster, return RS_ERR_NO_PATH). */
+RS_API int rowsoftmax_causal_fwd_ex(const void* in, void* out, int64_t M, int64_t N,
+                                    int64_t in_row_stride, int64_t out_row_stride, int64_t period,
+                                    int64_t diag_offset, int dtype, cudaStream_t stream,
+                                    const rs_options* opts);
+
+/* Host-only planner of rowsoftmax_causal_fwd_ex (plan.masked = 1). */
+RS_API int rowsoftmax_causal_plan(const void* in, const void* out, int64_t M, int64_t N,
+                                  int64_t in_row_stride, int64_t out_row_stride, int64_t period,
+                                  int64_t diag_offset, int dtype, const rs_options* opts,
+                                  const rs_device_info* dev, rs_plan* plan);
 
 /*
  * Row normalisations on the same engine (one read of x, one write of y for

@@ -4,8 +4,8 @@ row normalisations (RMSNorm, LayerNorm) on the same row engine.
 The product is ``librowsoftmax.so`` (CUDA, sm_103a; see include/rowsoftmax.h).
 This package holds its sources (``csrc/``), its build (``build.py``), the
 ctypes binding (``_abi.py``, same names as the C entry points) and tensor
-front ends (``softmax``, ``rmsnorm``, ``layernorm``) that only marshal torch
-tensors into the C calls.
+front ends (``softmax``, ``softmax_causal``, ``rmsnorm``, ``layernorm``) that
+only marshal torch tensors into the C calls.
 """
 from __future__ import annotations
 
@@ -32,6 +32,9 @@ from ._abi import (  # noqa: F401
     RS_RING_AUTO,
     RS_RING_REGISTERS,
     RS_RING_REREAD,
+    rowsoftmax_causal_fwd,
+    rowsoftmax_causal_fwd_ex,
+    rowsoftmax_causal_plan,
     rowsoftmax_device_info,
     rowsoftmax_device_status,
     rowsoftmax_fwd,
@@ -108,6 +111,19 @@ def softmax(x, out=None, stream=None, options=None):
     out, M, N, ldi, ldo = _rows_args(x, out)
     s = _stream_handle(x, stream)
     _check(rowsoftmax_fwd_ex(x.data_ptr(), out.data_ptr(), M, N, ldi, ldo, dtype_code(x.dtype), s, options))
+    return out
+
+
+def softmax_causal(x, period: int, diag_offset: int = 0, out=None, stream=None, options=None):
+    """Row softmax under a causal mask: row r of the 2-D CUDA tensor ``x``
+    keeps its first min(N, max(0, (r mod period) + 1 + diag_offset)) elements
+    (the rest is never read and comes out as 0).  For attention scores
+    [B, H, S_q, S_k] flattened to (B*H*S_q, S_k): period = S_q,
+    diag_offset = S_k - S_q."""
+    out, M, N, ldi, ldo = _rows_args(x, out)
+    s = _stream_handle(x, stream)
+    _check(rowsoftmax_causal_fwd_ex(x.data_ptr(), out.data_ptr(), M, N, ldi, ldo, int(period), int(diag_offset),
+                                    dtype_code(x.dtype), s, options))
     return out
 
 

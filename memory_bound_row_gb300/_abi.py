@@ -44,6 +44,9 @@ EXPORTED = (
     "layernorm_fwd",
     "rownorm_fwd_ex",
     "rownorm_plan",
+    "rowsoftmax_causal_fwd",
+    "rowsoftmax_causal_fwd_ex",
+    "rowsoftmax_causal_plan",
 )
 
 
@@ -83,6 +86,7 @@ class rs_plan(ctypes.Structure):
         ("withhold_copies", ctypes.c_int),
         ("op", ctypes.c_int),
         ("strict_order", ctypes.c_int),
+        ("masked", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -145,6 +149,14 @@ def load() -> ctypes.CDLL:
         lib.rownorm_plan.argtypes = [ci, vp, vp, vp, vp, i64, i64, i64, i64, f64, ci, ctypes.POINTER(rs_options),
                                      ctypes.POINTER(rs_device_info), ctypes.POINTER(rs_plan)]
         lib.rownorm_plan.restype = ci
+        lib.rowsoftmax_causal_fwd.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, ci, vp]
+        lib.rowsoftmax_causal_fwd.restype = ci
+        lib.rowsoftmax_causal_fwd_ex.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, ci, vp,
+                                                 ctypes.POINTER(rs_options)]
+        lib.rowsoftmax_causal_fwd_ex.restype = ci
+        lib.rowsoftmax_causal_plan.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, ci, ctypes.POINTER(rs_options),
+                                               ctypes.POINTER(rs_device_info), ctypes.POINTER(rs_plan)]
+        lib.rowsoftmax_causal_plan.restype = ci
         _lib = lib
         return lib
 
@@ -234,4 +246,26 @@ def rownorm_plan(op: int, in_ptr: int, out_ptr: int, weight_ptr: int | None, bia
     dev = ctypes.pointer(device) if device is not None else None
     rc = load().rownorm_plan(op, in_ptr, out_ptr, weight_ptr, bias_ptr, M, N, in_row_stride, out_row_stride, eps,
                              dtype, _opts(options), dev, ctypes.byref(plan))
+    return rc, plan.as_dict()
+
+
+def rowsoftmax_causal_fwd(in_ptr: int, out_ptr: int, M: int, N: int, in_row_stride: int, out_row_stride: int,
+                          period: int, diag_offset: int, dtype: int, stream: int = 0) -> int:
+    return load().rowsoftmax_causal_fwd(in_ptr, out_ptr, M, N, in_row_stride, out_row_stride, period, diag_offset,
+                                        dtype, stream)
+
+
+def rowsoftmax_causal_fwd_ex(in_ptr: int, out_ptr: int, M: int, N: int, in_row_stride: int, out_row_stride: int,
+                             period: int, diag_offset: int, dtype: int, stream: int = 0, options=None) -> int:
+    return load().rowsoftmax_causal_fwd_ex(in_ptr, out_ptr, M, N, in_row_stride, out_row_stride, period,
+                                           diag_offset, dtype, stream, _opts(options))
+
+
+def rowsoftmax_causal_plan(in_ptr: int, out_ptr: int, M: int, N: int, in_row_stride: int, out_row_stride: int,
+                           period: int, diag_offset: int, dtype: int, options=None,
+                           device: rs_device_info | None = None) -> tuple[int, dict]:
+    plan = rs_plan()
+    dev = ctypes.pointer(device) if device is not None else None
+    rc = load().rowsoftmax_causal_plan(in_ptr, out_ptr, M, N, in_row_stride, out_row_stride, period, diag_offset,
+                                       dtype, _opts(options), dev, ctypes.byref(plan))
     return rc, plan.as_dict()

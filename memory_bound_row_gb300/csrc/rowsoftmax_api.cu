@@ -28,6 +28,7 @@ int elem_size(int dtype) { return dtype == RS_F32 ? 4 : 2; }
 // 16-byte unit past N) inside int.
 constexpr int64_t kMaxN = (int64_t)INT_MAX - 64;
 constexpr int64_t kMaxGrid = (int64_t)INT_MAX;
+constexpr int64_t kMaxMaskOffset = (int64_t)1 << 62;  // keeps (r mod P) + 1 + offset inside int64
 
 // Auto-planner knobs.
 constexpr int kRowsTargetValues = 32;             // fp32 values a thread holds (auto)
@@ -185,7 +186,7 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     if (o.stages && (o.stages < 2 || o.stages > rs::kRingMaxStages)) return RS_ERR_INVALID_ARG;
     if (o.ring_values < RS_RING_AUTO || o.ring_values > RS_RING_REREAD) return RS_ERR_INVALID_ARG;
     const int values = o.ring_values == RS_RING_AUTO ? RS_RING_REGISTERS : o.ring_values;
-    if (values == RS_RING_REREAD && p->op != RS_OP_SOFTMAX) return RS_ERR_NO_PATH;
+    if (values == RS_RING_REREAD && (p->op != RS_OP_SOFTMAX || p->masked)) return RS_ERR_NO_PATH;
     rs_options ro = o;
     ro.grid_limit = 0;
     int rc = plan_rows(dtype, vec, M, units, ro, p, values == RS_RING_REGISTERS);
@@ -373,12 +374,19 @@ bool ranges_overlap(uintptr_t q, uint64_t bytes, uintptr_t r, uint64_t rbytes) {
     return q < r + rbytes && r < q + bytes;
 }
 
+// mask_period > 0: the softmax under a causal mask (row r keeps its first
+// min(N, max(0, (r mod mask_period) + 1 + mask_offset)) elements).
 int validate_and_plan_op(int op, const void* in, const void* out, const void* w, const void* b, int64_t M,
                          int64_t N, int64_t ldi, int64_t ldo, double eps, int dtype, const rs_options* opts,
-                         const rs_device_info* dev, rs_plan* p) {
+                         const rs_device_info* dev, rs_plan* p, int64_t mask_period = 0,
+                         int64_t mask_offset = 0) {
     memset(p, 0, sizeof(*p));
     p->dtype = dtype;
     p->op = op;
+    if (mask_period < 0 || (mask_period > 0 && op != RS_OP_SOFTMAX)) return RS_ERR_INVALID_ARG;
+    if (mask_offset < -kMaxMaskOffset || mask_offset > kMaxMaskOffset) return RS_ERR_INVALID_ARG;
+    const bool masked = mask_period > 0;
+    p->masked = masked ? 1 : 0;
     if (op != RS_OP_SOFTMAX && op != RS_OP_RMSNORM && op != RS_OP_LAYERNORM) return RS_ERR_INVALID_ARG;
     if (dtype != RS_F32 && dtype != RS_F16 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED_DTYPE;
     if (M < 0 || N < 0) return RS_ERR_INVALID_ARG;
@@ -449,13 +457,15 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         if (N * es <= rows_max) rc = plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
-        if (norm) {
+        if (norm || masked) {
             if (vec_ok) {
                 rc = plan_cluster_hold(dtype, vec, M, N, o, *dev, p);
                 if (rc == RS_OK) return RS_OK;
                 if (rc != RS_ERR_NO_PATH) return rc;
             }
-            return plan_norm_stream(vec, M, o, *dev, p);
+            // The causal mask is served by the register rows, the ring and the
+            // register-holding clusters only.
+            return norm ? plan_norm_stream(vec, M, o, *dev, p) : RS_ERR_NO_PATH;
         }
         if (vec_ok) {
             rc = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, p);
@@ -466,9 +476,10 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
     }
     if (path == RS_PATH_ROWS) return plan_rows(dtype, vec, M, units, o, p, true, dev->sm_count);
     if (path == RS_PATH_RING) return plan_ring(dtype, vec, M, N, units, o, *dev, p, nparams);
-    if (norm) {
-        if (path == RS_PATH_STREAM) return plan_norm_stream(vec, M, o, *dev, p);
-        // Clusters serve the normalisations with the slice in registers only.
+    if (norm || masked) {
+        if (path == RS_PATH_STREAM) return norm ? plan_norm_stream(vec, M, o, *dev, p) : RS_ERR_NO_PATH;
+        // Clusters serve the normalisations and the causal mask with the slice in
+        // registers only.
         if (vec == 1 || o.ring_values == RS_RING_REREAD) return RS_ERR_NO_PATH;
         return plan_cluster_hold(dtype, vec, M, N, o, *dev, p);
     }
@@ -523,10 +534,11 @@ int current_device(int* dev, rs_device_info* info) {
 // cudaOccupancyMaxActiveClusters for a planned cluster launch, cached by
 // device and launch shape (the query costs far more than a launch).
 struct ClusterKey {
-    int dev, op, dtype, path, values, vec, vpt, block, cs;
+    int dev, op, masked, dtype, path, values, vec, vpt, block, cs;
     size_t smem;
     bool operator==(const ClusterKey& o) const {
-        return dev == o.dev && op == o.op && dtype == o.dtype && path == o.path && values == o.values &&
+        return dev == o.dev && op == o.op && masked == o.masked && dtype == o.dtype && path == o.path &&
+               values == o.values &&
                vec == o.vec && vpt == o.vpt && block == o.block && cs == o.cs && smem == o.smem;
     }
 };
@@ -536,8 +548,8 @@ int g_cluster_vals[64];
 int g_cluster_n = 0;
 
 cudaError_t max_active_clusters_cached(int dev, const rs_plan& p, int* n) {
-    const ClusterKey k{dev, p.op, p.dtype, p.path, p.ring_values, p.vec_elems, p.vec_per_thread, p.block_threads,
-                       p.cluster_size, p.smem_bytes};
+    const ClusterKey k{dev, p.op, p.masked, p.dtype, p.path, p.ring_values, p.vec_elems, p.vec_per_thread,
+                       p.block_threads, p.cluster_size, p.smem_bytes};
     {
         std::lock_guard<std::mutex> lock(g_cluster_mu);
         for (int i = 0; i < g_cluster_n; ++i)
@@ -547,7 +559,10 @@ cudaError_t max_active_clusters_cached(int dev, const rs_plan& p, int* n) {
             }
     }
     cudaError_t e;
-    if (p.op == RS_OP_SOFTMAX) e = rs::wide_max_active_clusters(p, n);
+    if (p.op == RS_OP_SOFTMAX && p.masked) {
+        e = p.dtype == RS_F32 ? rs::causal_max_clusters_f32(p, n)
+            : p.dtype == RS_F16 ? rs::causal_max_clusters_f16(p, n) : rs::causal_max_clusters_bf16(p, n);
+    } else if (p.op == RS_OP_SOFTMAX) e = rs::wide_max_active_clusters(p, n);
     else if (p.dtype == RS_F32) e = rs::norm_max_clusters_f32(p, n);
     else if (p.dtype == RS_F16) e = rs::norm_max_clusters_f16(p, n);
     else e = rs::norm_max_clusters_bf16(p, n);
@@ -611,14 +626,16 @@ namespace {
 
 // Validate, plan on the current device and launch one row operation.
 int run_op(int op, const void* in, void* out, const void* w, const void* b, int64_t M, int64_t N, int64_t ldi,
-           int64_t ldo, double eps, int dtype, cudaStream_t stream, const rs_options* opts) {
+           int64_t ldo, double eps, int dtype, cudaStream_t stream, const rs_options* opts,
+           int64_t mask_period = 0, int64_t mask_offset = 0) {
     // Shape and argument errors first: they need no device.
     rs_device_info probe;
     memset(&probe, 0, sizeof(probe));
     probe.sm_count = 1;
     probe.max_smem_per_block_optin = 1;
     rs_plan plan;
-    int rc = validate_and_plan_op(op, in, out, w, b, M, N, ldi, ldo, eps, dtype, nullptr, &probe, &plan);
+    int rc = validate_and_plan_op(op, in, out, w, b, M, N, ldi, ldo, eps, dtype, nullptr, &probe, &plan, mask_period,
+                                  mask_offset);
     if (rc != RS_OK && rc != RS_ERR_NO_PATH) return rc;
     if (M == 0 || N == 0) return RS_OK;
 
@@ -630,7 +647,8 @@ int run_op(int op, const void* in, void* out, const void* w, const void* b, int6
     if ((rc = check_device_pointer(out, dev)) != RS_OK) return rc;
     if (w && (rc = check_device_pointer(w, dev)) != RS_OK) return rc;
     if (b && (rc = check_device_pointer(b, dev)) != RS_OK) return rc;
-    rc = validate_and_plan_op(op, in, out, w, b, M, N, ldi, ldo, eps, dtype, opts, &info, &plan);
+    rc = validate_and_plan_op(op, in, out, w, b, M, N, ldi, ldo, eps, dtype, opts, &info, &plan, mask_period,
+                              mask_offset);
     if (rc != RS_OK) return rc;
 
     const bool persistent_cluster = plan.path == RS_PATH_CLUSTER && plan.ring_values == RS_RING_REGISTERS;
@@ -652,26 +670,37 @@ int run_op(int op, const void* in, void* out, const void* w, const void* b, int6
     cudaError_t e = cudaSuccess;
     const int n = (int)N;
     if (op != RS_OP_SOFTMAX) {
-        const rs::RowArgs a{w, b, (float)eps};
+        const rs::RowArgs a{w, b, (float)eps, 0, 0, 0};
         switch (dtype) {
             case RS_F32: e = rs::launch_norm_f32(plan, in, out, M, n, ldi, ldo, stream, a); break;
             case RS_F16: e = rs::launch_norm_f16(plan, in, out, M, n, ldi, ldo, stream, a); break;
             default: e = rs::launch_norm_bf16(plan, in, out, M, n, ldi, ldo, stream, a); break;
         }
-    } else if (plan.path == RS_PATH_ROWS) {
+    } else if (mask_period > 0) {
+        const rs::RowArgs a{nullptr, nullptr, 0.0f, mask_period, mask_offset,
+                            rs::remainder_magic((uint64_t)mask_period)};
         switch (dtype) {
-            case RS_F32: e = rs::launch_rows_f32(plan, in, out, M, n, ldi, ldo, stream); break;
-            case RS_F16: e = rs::launch_rows_f16(plan, in, out, M, n, ldi, ldo, stream); break;
-            default: e = rs::launch_rows_bf16(plan, in, out, M, n, ldi, ldo, stream); break;
-        }
-    } else if (plan.path == RS_PATH_RING) {
-        switch (dtype) {
-            case RS_F32: e = rs::launch_ring_f32(plan, in, out, M, n, ldi, ldo, stream); break;
-            case RS_F16: e = rs::launch_ring_f16(plan, in, out, M, n, ldi, ldo, stream); break;
-            default: e = rs::launch_ring_bf16(plan, in, out, M, n, ldi, ldo, stream); break;
+            case RS_F32: e = rs::launch_causal_f32(plan, in, out, M, n, ldi, ldo, stream, a); break;
+            case RS_F16: e = rs::launch_causal_f16(plan, in, out, M, n, ldi, ldo, stream, a); break;
+            default: e = rs::launch_causal_bf16(plan, in, out, M, n, ldi, ldo, stream, a); break;
         }
     } else {
-        e = rs::launch_wide(plan, in, out, M, n, ldi, ldo, stream);
+        const rs::RowArgs a{nullptr, nullptr, 0.0f, 0, 0, 0};
+        if (plan.path == RS_PATH_ROWS) {
+            switch (dtype) {
+                case RS_F32: e = rs::launch_rows_f32(plan, in, out, M, n, ldi, ldo, stream, a); break;
+                case RS_F16: e = rs::launch_rows_f16(plan, in, out, M, n, ldi, ldo, stream, a); break;
+                default: e = rs::launch_rows_bf16(plan, in, out, M, n, ldi, ldo, stream, a); break;
+            }
+        } else if (plan.path == RS_PATH_RING) {
+            switch (dtype) {
+                case RS_F32: e = rs::launch_ring_f32(plan, in, out, M, n, ldi, ldo, stream, a); break;
+                case RS_F16: e = rs::launch_ring_f16(plan, in, out, M, n, ldi, ldo, stream, a); break;
+                default: e = rs::launch_ring_bf16(plan, in, out, M, n, ldi, ldo, stream, a); break;
+            }
+        } else {
+            e = rs::launch_wide(plan, in, out, M, n, ldi, ldo, stream, a);
+        }
     }
     if (e != cudaSuccess) return fail_cuda(e);
     return RS_OK;
@@ -685,6 +714,33 @@ int rowsoftmax_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t i
                       int64_t out_row_stride, int dtype, cudaStream_t stream, const rs_options* opts) {
     return run_op(RS_OP_SOFTMAX, in, out, nullptr, nullptr, M, N, in_row_stride, out_row_stride, 0.0, dtype,
                   stream, opts);
+}
+
+int rowsoftmax_causal_fwd_ex(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                             int64_t out_row_stride, int64_t period, int64_t diag_offset, int dtype,
+                             cudaStream_t stream, const rs_options* opts) {
+    if (period < 1) return RS_ERR_INVALID_ARG;
+    return run_op(RS_OP_SOFTMAX, in, out, nullptr, nullptr, M, N, in_row_stride, out_row_stride, 0.0, dtype, stream,
+                  opts, period, diag_offset);
+}
+
+int rowsoftmax_causal_fwd(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                          int64_t out_row_stride, int64_t period, int64_t diag_offset, int dtype,
+                          cudaStream_t stream) {
+    return rowsoftmax_causal_fwd_ex(in, out, M, N, in_row_stride, out_row_stride, period, diag_offset, dtype,
+                                    stream, nullptr);
+}
+
+int rowsoftmax_causal_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                           int64_t out_row_stride, int64_t period, int64_t diag_offset, int dtype,
+                           const rs_options* opts, const rs_device_info* dev, rs_plan* plan) {
+    if (!plan) return RS_ERR_INVALID_ARG;
+    if (period < 1) {
+        memset(plan, 0, sizeof(*plan));
+        return RS_ERR_INVALID_ARG;
+    }
+    return validate_and_plan_op(RS_OP_SOFTMAX, in, out, nullptr, nullptr, M, N, in_row_stride, out_row_stride, 0.0,
+                                dtype, opts, dev, plan, period, diag_offset);
 }
 
 int rownorm_fwd_ex(int op, const void* in, void* out, const void* weight, const void* bias, int64_t M,
@@ -746,6 +802,9 @@ int rowsoftmax_device_status(unsigned int* flags, int clear) {
     if (e == cudaSuccess) e = rs::read_status_norm_f32(flags, clear != 0);
     if (e == cudaSuccess) e = rs::read_status_norm_f16(flags, clear != 0);
     if (e == cudaSuccess) e = rs::read_status_norm_bf16(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_causal_f32(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_causal_f16(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_causal_bf16(flags, clear != 0);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return fail_cuda(e);

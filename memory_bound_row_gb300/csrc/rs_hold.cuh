@@ -90,13 +90,25 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
     const int64_t cluster_id = blockIdx.x / cs;
     const int64_t n_clusters = gridDim.x / cs;
 
+    // Causal mask: the elements of this CTA's slice that row `row` keeps (the
+    // part of the kept prefix that falls in the slice); only the whole units
+    // that hold them are copied.
+    auto slice_keep = [&](int64_t row) {
+        const int keep = row_keep(args, row, N) - c0;
+        return keep < 0 ? 0 : (keep > len ? len : keep);
+    };
     auto issue = [&](int64_t row, int slot) {
-        if (slice_bytes == 0) {
+        uint32_t bytes = slice_bytes;
+        if constexpr (OP::kMasked) {
+            const int cu = (slice_keep(row) + VEC - 1) / VEC;
+            bytes = (uint32_t)(cu < full ? cu : full) * 16u;
+        }
+        if (bytes == 0) {
             mbar_arrive(&bars[slot]);
             return;
         }
-        mbar_arrive_expect_tx(&bars[slot], slice_bytes);
-        bulk_load(slots + (size_t)slot * slot_stride, in + row * ldi + c0, slice_bytes, &bars[slot]);
+        mbar_arrive_expect_tx(&bars[slot], bytes);
+        bulk_load(slots + (size_t)slot * slot_stride, in + row * ldi + c0, bytes, &bars[slot]);
     };
 
     if (tid == 0) {
@@ -134,7 +146,38 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
         const S* xr = in + row * ldi + c0;
 
         float v[VPT][VEC];
-        if ((tid + (VPT - 1) * tpr) < full) {
+        if constexpr (OP::kMasked) {
+            // Fully kept units from the slot, the rest the fill; then the one
+            // partly kept unit (in the slot, or the slice's ragged tail), if
+            // this thread holds it.
+            const int lv = slice_keep(row);
+            const int whole_units = lv / VEC;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int u = tid + k * tpr;
+                if (u < whole_units) {
+                    T::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)u * 16), v[k]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) v[k][e] = OP::kFill;
+                }
+            }
+            const int us = whole_units;
+            if (lv % VEC && tid <= us && us <= tid + (VPT - 1) * tpr) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    if (tid + k * tpr != us) continue;
+                    if (us < full) {
+                        T::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)us * 16), v[k]);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (us * VEC + e >= lv) v[k][e] = OP::kFill;
+                    } else {
+                        load_unit<DT, VEC>(xr, us * VEC, lv, v[k], OP::kFill);
+                    }
+                }
+            }
+        } else if ((tid + (VPT - 1) * tpr) < full) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
                 T::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)(tid + k * tpr) * 16), v[k]);

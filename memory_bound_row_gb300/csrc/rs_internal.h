@@ -65,11 +65,23 @@ constexpr int kWideHoldMaxVpt = 8;        // units per thread it is instantiated
 
 // Per-call parameters of a row operation: the normalisations' weight and
 // bias vectors (N stored values each, or null) and eps; zero for the softmax.
+// A causal mask (the softmax only): row r keeps its first
+// min(N, max(0, (r mod mask_period) + 1 + mask_offset)) elements; the rest is
+// -inf, never read, and written as 0.  mask_period 0: no mask.
 struct RowArgs {
     const void* w;
     const void* b;
     float eps;
+    int64_t mask_period;
+    int64_t mask_offset;
+    uint64_t mask_magic;  // 2^64 / mask_period rounded up (mod 2^64), for rows and periods below 2^32
 };
+
+// The reciprocal constant of the remainder by direct computation (Lemire,
+// Kaser and Kurz, "Faster Remainder by Direct Computation", 2019): for
+// 32-bit n and d >= 1, n mod d = high64((c * n mod 2^64) * d) with
+// c = floor((2^64 - 1) / d) + 1 (mod 2^64).
+inline uint64_t remainder_magic(uint64_t d) { return d ? ~0ull / d + 1 : 0; }
 
 // Launch of `kern` with the programmatic-dependent-launch attribute (unless
 // `strict`), and a cluster dimension when cluster > 0.  The kernels wait for
@@ -118,20 +130,21 @@ cudaError_t launch_norm_f16(const rs_plan& p, const void* in, void* out, int64_t
                             int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_norm_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                              int64_t ldo, cudaStream_t s, const RowArgs& a);
+// The softmax launchers take the mask in `a` (weight, bias and eps unused).
 cudaError_t launch_rows_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                            int64_t ldi, int64_t ldo, cudaStream_t s);
+                            int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_rows_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                            int64_t ldi, int64_t ldo, cudaStream_t s);
+                            int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_rows_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                             int64_t ldi, int64_t ldo, cudaStream_t s);
+                             int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_ring_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                            int64_t ldi, int64_t ldo, cudaStream_t s);
+                            int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_ring_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                            int64_t ldi, int64_t ldo, cudaStream_t s);
+                            int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_ring_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                             int64_t ldi, int64_t ldo, cudaStream_t s);
+                             int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_wide(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                        int64_t ldi, int64_t ldo, cudaStream_t s);
+                        int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a);
 
 // Number of clusters of the planned wide kernel that fit on the device at
 // once (0: the cluster shape cannot be scheduled).
@@ -143,6 +156,21 @@ cudaError_t read_status_f32(unsigned int* flags, bool clear);
 cudaError_t read_status_f16(unsigned int* flags, bool clear);
 cudaError_t read_status_bf16(unsigned int* flags, bool clear);
 cudaError_t read_status_wide(unsigned int* flags, bool clear);
+// The softmax under a causal mask (a.mask_period > 0): plan.path RS_PATH_ROWS,
+// RS_PATH_RING (rows held in registers) or RS_PATH_CLUSTER (register-holding).
+cudaError_t launch_causal_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                              int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t launch_causal_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                              int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t launch_causal_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                               int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t causal_max_clusters_f32(const rs_plan& p, int* n);
+cudaError_t causal_max_clusters_f16(const rs_plan& p, int* n);
+cudaError_t causal_max_clusters_bf16(const rs_plan& p, int* n);
+cudaError_t read_status_causal_f32(unsigned int* flags, bool clear);
+cudaError_t read_status_causal_f16(unsigned int* flags, bool clear);
+cudaError_t read_status_causal_bf16(unsigned int* flags, bool clear);
+
 // cudaOccupancyMaxActiveClusters of a planned register-holding cluster launch
 // of a normalisation (plan.op).
 cudaError_t norm_max_clusters_f32(const rs_plan& p, int* n);

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(HOLD ? rows_block_limit(VPT, Traits<DT>::kVec)
                                   HOLD ? 1 : kRingRereadMinCtas)
 ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, int stages,
             uint64_t wait_ns, int withhold, RowArgs args) {
-    static_assert(HOLD || OP::kOp == RS_OP_SOFTMAX, "the re-read variant is the softmax's only");
+    static_assert(HOLD || (OP::kOp == RS_OP_SOFTMAX && !OP::kMasked), "the re-read variant is the softmax's only");
     using T = Traits<DT>;
     using S = typename T::storage;
     constexpr int VEC = T::kVec;
@@ -96,13 +96,51 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         for (int k = 0; k < nrows; ++k) bulk_load(dst + (size_t)k * slot, in + (r0 + k) * ldi, slot, &full[s]);
     };
 
+    // Causal mask: the whole units that hold a row's kept prefix are copied.
+    // Warp 0 fills a stage (called by its 32 lanes): lane k issues the copies
+    // of rows k, k + 32, ... so that the per-row lengths are worked out in
+    // parallel (one thread doing them all delayed every stage); lane 0
+    // announces the stage's bytes first.
+    auto copied_units = [&](int64_t row) {
+        const int keep = row_keep(args, row, N);
+        const int cu = (keep + VEC - 1) / VEC;
+        return cu < units_full ? cu : units_full;
+    };
+    auto issue_masked = [&](int s, int64_t g) {
+        const int lane = threadIdx.x & 31;
+        const int64_t r0 = g * rpg;
+        const int nrows = (int)(M - r0 < rpg ? M - r0 : rpg);
+        uint32_t mine = 0;
+        for (int k = lane; k < nrows; k += 32) mine += (uint32_t)copied_units(r0 + k) * 16u;
+        const uint32_t total = __reduce_add_sync(0xffffffffu, mine);
+        if (lane == 0) {
+            if (total == 0) mbar_arrive(&full[s]);
+            else mbar_arrive_expect_tx(&full[s], total);
+        }
+        __syncwarp();
+        if (total == 0 || withhold) return;
+        fence_proxy_async_smem();  // the stage's earlier generic reads before the copies' writes
+        unsigned char* dst = ring + (size_t)s * stage_bytes;
+        for (int k = lane; k < nrows; k += 32) {
+            const uint32_t bytes = (uint32_t)copied_units(r0 + k) * 16u;
+            if (bytes) bulk_load(dst + (size_t)k * slot, in + (r0 + k) * ldi, bytes, &full[s]);
+        }
+    };
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
     wait_prior_grid();
-    if (threadIdx.x == 0) {
+    if constexpr (OP::kMasked) {
+        if (threadIdx.x < 32) {
+            for (int s = 0; s < stages; ++s) {
+                const int64_t g = blockIdx.x + (int64_t)s * gridDim.x;
+                if (g < groups) issue_masked(s, g);
+            }
+        }
+    } else if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             const int64_t g = blockIdx.x + (int64_t)s * gridDim.x;
             if (g < groups) issue(s, g);
@@ -150,7 +188,42 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         const unsigned char* srow = ring + (size_t)s * stage_bytes + (size_t)grp * slot;
         const S* grow = in + (active ? row : 0) * ldi;
 
-        if constexpr (HOLD) {
+        if constexpr (HOLD && OP::kMasked) {
+            // Fully kept units from the stage, the rest the fill (-inf); then
+            // the one unit that holds the end of the kept prefix (staged, or
+            // the row's ragged tail), if this thread has it.
+            float v[VPT][VEC];
+            const int keep = row_keep(args, active ? row : 0, N);
+            const int whole_units = keep / VEC;
+            const int copied = whole_units + (keep % VEC && whole_units < units_full ? 1 : 0);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int u = t + k * tpr;
+                if (active && u < whole_units) {
+                    T::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)u * 16), v[k]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) v[k][e] = OP::kFill;
+                }
+            }
+            const int us = whole_units;
+            if (active && keep % VEC && t <= us && us <= t + (VPT - 1) * tpr) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    if (t + k * tpr != us) continue;
+                    if (us < copied) {
+                        T::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)us * 16), v[k]);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (us * VEC + e >= keep) v[k][e] = OP::kFill;
+                    } else {
+                        load_unit<DT, VEC>(grow, us * VEC, keep, v[k], OP::kFill);
+                    }
+                }
+            }
+            OP::template apply<DT, VEC, VPT>(v, t, tpr, N, false, prm, part[it & 1]);
+            if (active && !abort) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v);
+        } else if constexpr (HOLD) {
             float v[VPT][VEC];
             if (active && (t + (VPT - 1) * tpr) < units_full) {
 #pragma unroll
@@ -226,7 +299,12 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
             abort = true;
             break;
         }
-        if (threadIdx.x == 0) {
+        if constexpr (OP::kMasked) {
+            if (threadIdx.x < 32) {
+                const int64_t gn = g + (int64_t)stages * gridDim.x;
+                if (gn < groups) issue_masked(s, gn);
+            }
+        } else if (threadIdx.x == 0) {
             const int64_t gn = g + (int64_t)stages * gridDim.x;
             if (gn < groups) {
                 fence_proxy_async_smem();
@@ -300,9 +378,12 @@ struct RingDispatch<DT, OP, V0, Vs...> {
     static cudaError_t go(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                           int64_t ldo, cudaStream_t s, const RowArgs& a) {
         if (p.vec_per_thread == V0) {
-            if constexpr (OP::kOp == RS_OP_SOFTMAX) {
+            if constexpr (OP::kOp == RS_OP_SOFTMAX && !OP::kMasked) {
                 if (p.ring_values == RS_RING_REREAD)
                     return launch_ring_one<DT, V0, false, OP>(p, in, out, M, N, ldi, ldo, s, a);
+            }
+            if constexpr (OP::kMasked) {
+                if (p.ring_values == RS_RING_REREAD) return cudaErrorInvalidConfiguration;
             }
             return launch_ring_one<DT, V0, true, OP>(p, in, out, M, N, ldi, ldo, s, a);
         }

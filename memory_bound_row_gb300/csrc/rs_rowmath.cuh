@@ -19,6 +19,20 @@
 
 namespace rs {
 
+// Elements of row `row` that a causal mask keeps (N without a mask).  The
+// remainder uses the host's reciprocal constant when row and period fit 32
+// bits (two multiplications instead of a 64-bit division).
+__device__ __forceinline__ int row_keep(const RowArgs& a, int64_t row, int N) {
+    if (a.mask_period <= 0) return N;
+    int64_t rm;
+    if (((uint64_t)row >> 32) == 0 && ((uint64_t)a.mask_period >> 32) == 0)
+        rm = (int64_t)__umul64hi(a.mask_magic * (uint64_t)row, (uint64_t)a.mask_period);
+    else
+        rm = row % a.mask_period;
+    const int64_t L = rm + 1 + a.mask_offset;
+    return L < 0 ? 0 : (L > N ? N : (int)L);
+}
+
 // Replaces v by exp(v - m_w) and returns the factor c with y = v * c.
 // `part` is a per-iteration shared buffer of at least (blockDim.x / 32)
 // pairs; rows wider than a warp synchronise the CTA once.
@@ -230,6 +244,7 @@ __device__ __forceinline__ void stage_param(typename Traits<DT>::storage* dst, c
 
 struct OpSoftmax {
     static constexpr int kOp = RS_OP_SOFTMAX;
+    static constexpr bool kMasked = false;
     static constexpr float kFill = kNegInf;
     template <int DT, int VEC, int VPT, typename P>
     __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int, int tpr, int, bool, const P&,
@@ -242,10 +257,19 @@ struct OpSoftmax {
     }
 };
 
+// The softmax under a causal mask (RowArgs::mask_period > 0): each row keeps
+// a prefix (row_keep); the kernels copy and read only that prefix, and the rest
+// of the row, filled with -inf, comes out as exactly 0.  A separate type so
+// that the unmasked kernels carry no mask code.
+struct OpSoftmaxCausal : OpSoftmax {
+    static constexpr bool kMasked = true;
+};
+
 // RMSNorm ("Reference Kernel: RMSNorm", Hugging Face "triton-kernels" skill
 // page): y = x * rsqrt(sum(x^2)/N + eps) * w, accumulated in fp32.
 struct OpRmsNorm {
     static constexpr int kOp = RS_OP_RMSNORM;
+    static constexpr bool kMasked = false;
     static constexpr float kFill = 0.0f;  // absent elements add nothing to the sum of squares
     template <int DT, int VEC, int VPT, typename P>
     __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool,
@@ -268,6 +292,7 @@ struct OpRmsNorm {
 // the output is formed as ((x * r) - mean * r) * w + b with two FMAs.
 struct OpLayerNorm {
     static constexpr int kOp = RS_OP_LAYERNORM;
+    static constexpr bool kMasked = false;
     static constexpr float kFill = 0.0f;
     template <int DT, int VEC, int VPT, typename P>
     __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool whole,

@@ -277,10 +277,10 @@ static cudaError_t launch_wide_one(const rs_plan& p, const void* in, void* out, 
 
 template <int DT>
 static cudaError_t launch_wide_dt(const rs_plan& p, const void* in, void* out, int64_t M, int N,
-                                  int64_t ldi, int64_t ldo, cudaStream_t s) {
+                                  int64_t ldi, int64_t ldo, cudaStream_t s, const RowArgs& a) {
     constexpr int KV = Traits<DT>::kVec;
     if (p.path == RS_PATH_CLUSTER && p.vec_elems == KV && p.ring_values == RS_RING_REGISTERS) {
-        return launch_hold<DT, OpSoftmax>(p, in, out, M, N, ldi, ldo, s, RowArgs{});
+        return launch_hold<DT, OpSoftmax>(p, in, out, M, N, ldi, ldo, s, a);
     }
     if (p.path == RS_PATH_CLUSTER && p.vec_elems == KV)
         return launch_wide_one<DT, KV, true>(p, in, out, M, N, ldi, ldo, s);
@@ -292,11 +292,12 @@ static cudaError_t launch_wide_dt(const rs_plan& p, const void* in, void* out, i
 }
 
 cudaError_t launch_wide(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
-                        int64_t ldo, cudaStream_t s) {
+                        int64_t ldo, cudaStream_t s, const RowArgs& a) {
+    if (a.mask_period > 0) return cudaErrorInvalidConfiguration;  // the causal mask has its own instances
     switch (p.dtype) {
-        case RS_F32: return launch_wide_dt<RS_F32>(p, in, out, M, N, ldi, ldo, s);
-        case RS_F16: return launch_wide_dt<RS_F16>(p, in, out, M, N, ldi, ldo, s);
-        case RS_BF16: return launch_wide_dt<RS_BF16>(p, in, out, M, N, ldi, ldo, s);
+        case RS_F32: return launch_wide_dt<RS_F32>(p, in, out, M, N, ldi, ldo, s, a);
+        case RS_F16: return launch_wide_dt<RS_F16>(p, in, out, M, N, ldi, ldo, s, a);
+        case RS_BF16: return launch_wide_dt<RS_BF16>(p, in, out, M, N, ldi, ldo, s, a);
         default: return cudaErrorInvalidValue;
     }
 }

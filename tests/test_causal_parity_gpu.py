@@ -1,0 +1,181 @@
+"""GPU parity of the causal-mask row softmax (rowsoftmax_causal_fwd) against the
+CPU oracle's softmax_prefix_f64, through the C ABI.
+
+Covered: every kernel that implements the mask (register rows, the bulk-copy
+ring, register-holding clusters), every storage type, periods that wrap, positive and negative
+diagonal offsets (rows with nothing kept give NaN rows, as the oracle), NaN
+garbage in the masked part (never read), padded strides, misaligned pointers,
+in-place calls, and the causal benchmark workload at full size, where the
+result must equal the plain softmax of the same -inf-masked scores bit for
+bit (the same kernel, the masked loads skipped).
+"""
+import concurrent.futures as cf
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_row_gb300 as rs
+import oracle
+from memory_bound_row_gb300 import build
+from memory_bound_row_gb300 import workloads as W
+
+from _parity import FMT, compare, to_storage_numpy
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    rc, _ = rs.rowsoftmax_device_status(clear=True)
+    assert rc == rs.RS_OK
+    yield
+    rc, flags = rs.rowsoftmax_device_status(clear=False)
+    assert rc == rs.RS_OK and flags == 0, f"device status word {flags:#x}"
+
+
+def _oracle(x, period, offset, row0=0):
+    """Oracle rows row0 .. row0 + len(x) - 1 (float64), several threads."""
+    fmt = FMT[x.dtype]
+    xs = to_storage_numpy(x)
+    M, N = xs.shape
+    threads = max(1, min(16, os.cpu_count() or 1, M))
+    blocks = [b for b in np.array_split(np.arange(M), threads) if len(b)]
+    out = np.empty((M, N), dtype=np.float64)
+
+    def work(idx):
+        out[idx[0]: idx[-1] + 1] = oracle.softmax_prefix_f64(xs[idx[0]: idx[-1] + 1], fmt, period, offset, N,
+                                                             row0=row0 + int(idx[0]))
+
+    with cf.ThreadPoolExecutor(len(blocks)) as ex:
+        list(ex.map(work, blocks))
+    return out
+
+
+def _garbage(x, period, offset, row0=0):
+    """Write NaN into the masked part of x (which the kernels must not read)."""
+    M, N = x.shape
+    r = torch.arange(row0, row0 + M, device=x.device)
+    keep = (r % period + 1 + offset).clamp(0, N)
+    cols = torch.arange(N, device=x.device)
+    x[cols[None, :] >= keep[:, None]] = float("nan")
+
+
+def _aligned(M, N, dtype, seed, kind="normal1"):
+    vec = 4 if dtype == "f32" else 8
+    ld = -(-N // vec) * vec
+    x = W.generate(W.custom(M, N, dtype, ld=ld, seed=seed, kind=kind), "cuda")[:, :N]
+    out = torch.empty((M, ld), dtype=DT[dtype], device="cuda")[:, :N]
+    return x, out
+
+
+def _run(x, period, offset, out=None, options=None):
+    y = rs.softmax_causal(x, period, offset, out=out, options=options)
+    torch.cuda.synchronize()
+    return y
+
+
+def _servable(x, period, offset, options):
+    rc, dev = rs.rowsoftmax_device_info()
+    M, N = x.shape
+    ld = x.stride(0) if M > 1 else N
+    rc, plan = rs.rowsoftmax_causal_plan(x.data_ptr(), x.data_ptr() + (1 << 44), M, N, ld, ld, period, offset,
+                                         rs.dtype_code(x.dtype), options, dev)
+    assert rc in (rs.RS_OK, rs.RS_ERR_NO_PATH)
+    return rc == rs.RS_OK
+
+
+PATHS = {
+    "auto": None,
+    "rows": {"path": rs.RS_PATH_ROWS},
+    "ring": {"path": rs.RS_PATH_RING},
+    "cluster": {"path": rs.RS_PATH_CLUSTER},
+    "cluster3": {"path": rs.RS_PATH_CLUSTER, "cluster_size": 3},
+}
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [1, 7, 100, 1000, 2048, 4104, 12345])
+@pytest.mark.parametrize("period,offset", [("N", 0), (64, 0), (37, -3), (5, 5)])
+def test_masked_rows_against_the_oracle(path, dtype, N, period, offset):
+    P = N if period == "N" else period
+    M = 3 * P if P <= 64 else min(2 * P, 300)
+    x, out = _aligned(M, N, dtype, seed=N + P)
+    opts = PATHS[path]
+    if opts and not _servable(x, P, offset, opts):
+        pytest.skip("this kernel does not serve the shape")
+    ref = _oracle(x, P, offset)
+    _garbage(x, P, offset)
+    y = _run(x, P, offset, out=out, options=opts)
+    compare(y, ref, dtype, f"causal {path} {dtype} N={N} P={P} D={offset}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cs", [2, 5, 8])
+@pytest.mark.parametrize("N", [65536, 100003])
+def test_wide_rows_on_clusters(dtype, cs, N):
+    M, P = 24, 8
+    x, out = _aligned(M, N, dtype, seed=cs)
+    offset = N // 3  # partial slices, whole masked CTAs and fully kept rows
+    opts = {"path": rs.RS_PATH_CLUSTER, "cluster_size": cs}
+    if not _servable(x, P, offset, opts):
+        pytest.skip("slice does not fit a CTA's registers at this cluster size")
+    ref = _oracle(x, P, offset)
+    _garbage(x, P, offset)
+    y = _run(x, P, offset, out=out, options=opts)
+    compare(y, ref, dtype, f"causal cluster cs={cs} N={N}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_padded_strides_misaligned_and_in_place(dtype):
+    M, N, ld = 96, 1000, 1040
+    P = 32
+    base = W.generate(W.custom(M, N + 8, dtype, ld=ld, seed=4), "cuda")
+    x = base[:, 3: 3 + N]  # misaligned: element-wise kernels
+    ref = _oracle(x, P, 2)
+    _garbage(x, P, 2)
+    y = _run(x, P, 2)
+    compare(y, ref, dtype, "causal misaligned")
+    x2 = W.generate(W.custom(M, N, dtype, ld=ld, seed=5), "cuda")[:, :N]
+    ref2 = _oracle(x2, P, 0)
+    _garbage(x2, P, 0)
+    y2 = _run(x2, P, 0, out=x2)  # in place, padded stride
+    assert y2.data_ptr() == x2.data_ptr()
+    compare(y2, ref2, dtype, "causal in place")
+
+
+def test_causal_workload_full_size_equals_the_plain_softmax():
+    # The bf16 causal-score workload already holds -inf above the diagonal: the
+    # masked call must give the plain call's result bit for bit, without reading
+    # the masked half; with NaN written there instead, still the same.
+    w = W.WORKLOADS["bf16_causal_16x32x2048"]
+    x = W.generate(w, "cuda")
+    plain = rs.softmax(x)
+    masked = _run(x, 2048, 0)
+    assert torch.equal(plain.view(torch.int16), masked.view(torch.int16))
+    rows = torch.tensor([0, 1, 2047, 2048, 4095, 777777, w.M - 1], device="cuda")
+    for r in rows.tolist():
+        ref = oracle.softmax_prefix_f64(to_storage_numpy(x[r: r + 1]), "bf16", 2048, 0, row0=r)
+        compare(masked[r: r + 1], ref, "bf16", f"causal row {r}")
+    _garbage(x, 2048, 0)
+    again = _run(x, 2048, 0)
+    assert torch.equal(plain.view(torch.int16), again.view(torch.int16))
+    del x, plain, masked, again
+    torch.cuda.empty_cache()
+
+
+def test_kv_cache_offset_layout():
+    # Scores [B, H, S_q, S_k] with S_k > S_q (cached keys): period S_q, offset S_k - S_q.
+    B, H, Sq, Sk = 2, 4, 48, 80
+    x = W.generate(W.custom(B * H * Sq, Sk, "f16", seed=9), "cuda")
+    ref = _oracle(x, Sq, Sk - Sq)
+    _garbage(x, Sq, Sk - Sq)
+    y = _run(x, Sq, Sk - Sq)
+    compare(y, ref, "f16", "kv-cache layout")
