@@ -204,8 +204,10 @@ RS_API int rowsoftmax_plan(const void* in, const void* out, int64_t M, int64_t N
  *     L_r = min(N, max(0, (r mod period) + 1 + diag_offset))
  *
  * elements: y[r][j] is the softmax of those L_r values for j < L_r and exactly
- * 0 for j >= L_r.  Elements at j >= L_r are never read (they may hold
- * anything, NaN included); every output element is written.  For attention
+ * 0 for j >= L_r.  Elements at j >= L_r are never used (they may hold
+ * anything, NaN included): the register rows and the clusters do not load
+ * them, the ring stages whole rows and ignores them; every output element is
+ * written.  For attention
  * scores [B, H, S_q, S_k] stored as (B*H*S_q) x S_k rows: period = S_q and
  * diag_offset = S_k - S_q.  L_r == 0 is an all -inf row: NaN.  Data model,
  * ownership, asynchrony and errors are those of rowsoftmax_fwd; period < 1 or

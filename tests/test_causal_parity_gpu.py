@@ -4,7 +4,7 @@ CPU oracle's softmax_prefix_f64, through the C ABI.
 Covered: every kernel that implements the mask (register rows, the bulk-copy
 ring, register-holding clusters), every storage type, periods that wrap, positive and negative
 diagonal offsets (rows with nothing kept give NaN rows, as the oracle), NaN
-garbage in the masked part (never read), padded strides, misaligned pointers,
+garbage in the masked part (never used), padded strides, misaligned pointers,
 in-place calls, and the causal benchmark workload at full size, where the
 result must equal the plain softmax of the same -inf-masked scores bit for
 bit (the same kernel, the masked loads skipped).
@@ -59,7 +59,7 @@ def _oracle(x, period, offset, row0=0):
 
 
 def _garbage(x, period, offset, row0=0):
-    """Write NaN into the masked part of x (which the kernels must not read)."""
+    """Write NaN into the masked part of x (which the kernels must not use)."""
     M, N = x.shape
     r = torch.arange(row0, row0 + M, device=x.device)
     keep = (r % period + 1 + offset).clamp(0, N)
@@ -153,7 +153,7 @@ def test_padded_strides_misaligned_and_in_place(dtype):
 
 def test_causal_workload_full_size_equals_the_plain_softmax():
     # The bf16 causal-score workload already holds -inf above the diagonal: the
-    # masked call must give the plain call's result bit for bit, without reading
+    # masked call must give the plain call's result bit for bit without using
     # the masked half; with NaN written there instead, still the same.
     w = W.WORKLOADS["bf16_causal_16x32x2048"]
     x = W.generate(w, "cuda")
