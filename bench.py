@@ -300,11 +300,24 @@ def cpu_baseline(w, x_dev, op: str = "softmax", seconds: float = 3.0) -> dict:
             break
     dt = (time.perf_counter() - t) / passes
     nbytes = rows * w.N * 2 * w.elem_size
+    # The same oracle on one thread, over the first rows of the sample,
+    # repeated for about a third of `seconds`.
+    rows1 = max(1, rows // cores)
+    passes1 = 0
+    t = time.perf_counter()
+    while True:
+        oracle_op(op, xs[:rows1], fmt, w.N, params, 1, out=out[:rows1])
+        passes1 += 1
+        if time.perf_counter() - t >= seconds / 3:
+            break
+    dt1 = (time.perf_counter() - t) / passes1
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {w.M} rows x {passes} passes, fp64 {op} oracle"
                       f"{' writing ' + w.dtype if op == 'softmax' else ''}, "
                       f"{dt * passes:.1f} s wall on {cores} threads",
-            "rows_per_s": round(rows / dt, 2)}
+            "rows_per_s": round(rows / dt, 2),
+            "single_thread": {"value": round(rows1 * w.N * 2 * w.elem_size / dt1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"first {rows1} rows x {passes1} passes, {dt1 * passes1:.1f} s on 1 thread"}}
 
 
 def run_ours(args, workloads):
@@ -407,6 +420,30 @@ def run_ours(args, workloads):
         total_ms = max_over_ranks(total_ms, dev)
         clocks = sampler.finish() if sampler else None
 
+        # Context for the roofline: a plain device-to-device copy of the same
+        # buffer sets (cudaMemcpyAsync through torch), replayed and timed the
+        # same way on the same box right after the kernel.  It moves the whole
+        # buffers, padding included, and counts those bytes.
+        copy_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(graph_stream):
+            for i in range(G):
+                ys[i % nsets].copy_(xs[i % nsets])
+            graph_stream.synchronize()
+            with torch.cuda.graph(copy_graph, stream=graph_stream, capture_error_mode="relaxed"):
+                for i in range(G):
+                    ys[i % nsets].copy_(xs[i % nsets])
+        torch.cuda.synchronize()
+        c_start = torch.cuda.Event(enable_timing=True)
+        c_end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(graph_stream):
+            c_start.record(graph_stream)
+            for _ in range(replays):
+                copy_graph.replay()
+            c_end.record(graph_stream)
+        torch.cuda.synchronize()
+        copy_gbs = (set_bytes * args.steps) / (c_start.elapsed_time(c_end) * 1e-3) / 1e9
+        del copy_graph
+
         ms_per_step = total_ms / args.steps
         nbytes = op_bytes(op, w)
         if args.causal:  # the least traffic the mask allows: kept elements read, every element written
@@ -499,7 +536,11 @@ def run_ours(args, workloads):
                              "frac": round(achieved / peak, 4), "traffic": None if (args.options or args.rows) else ncu_traffic(traffic_key(op, name)),
                              "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
                              if peak_src == "measured" else "fallback 6.8 TB/s",
-                             "kernel_ms": round(kern_ms, 5)},
+                             "kernel_ms": round(kern_ms, 5),
+                             "same_run_copy_gbs": round(copy_gbs, 1),
+                             "frac_of_same_run_copy": round(achieved / copy_gbs, 4),
+                             "same_run_copy": "device-to-device copy of the same rotating buffer sets "
+                                              "(padding included), same graph replay, timed right after"},
                 "e2e": {"value": round(job_gbs(world, nbytes, 1, e2e_ms), 2), "unit": "GB/s",
                         "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
                         "d2h_bytes_per_step": h_out[0].numel() * h_out[0].element_size(),

@@ -170,6 +170,17 @@ cudaError_t causal_max_clusters_bf16(const rs_plan& p, int* n);
 cudaError_t read_status_causal_f32(unsigned int* flags, bool clear);
 cudaError_t read_status_causal_f16(unsigned int* flags, bool clear);
 cudaError_t read_status_causal_bf16(unsigned int* flags, bool clear);
+// LayerNorm on rows held inside one warp (plan.threads_per_row <= 32),
+// plan.path RS_PATH_ROWS or RS_PATH_RING: OpLayerNormWarp instances.
+cudaError_t launch_lnwarp_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                              int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t launch_lnwarp_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                              int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t launch_lnwarp_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                               int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t read_status_lnwarp_f32(unsigned int* flags, bool clear);
+cudaError_t read_status_lnwarp_f16(unsigned int* flags, bool clear);
+cudaError_t read_status_lnwarp_bf16(unsigned int* flags, bool clear);
 
 // cudaOccupancyMaxActiveClusters of a planned register-holding cluster launch
 // of a normalisation (plan.op).

@@ -325,4 +325,97 @@ struct OpLayerNorm {
     }
 };
 
+// Moments of a set of row values: count c, sum s and the sum q of squared
+// deviations from the set's own mean s / c.  Two disjoint sets merge into
+// their union by the parallel-variance identity (Chan, Golub and LeVeque,
+// "Updating formulae and a pairwise algorithm for computing sample
+// variances"):
+//   q = q_a + q_b + (s_b c_a - s_a c_b)^2 / (c_a c_b (c_a + c_b)).
+// The expression is symmetric in a and b to the bit (products rounded
+// separately, then subtracted), so both lanes of a butterfly step agree.
+__device__ __forceinline__ void merge_moments(float& c, float& s, float& q, float co, float so, float qo) {
+    const float cross = __fmul_rn(so, c) - __fmul_rn(s, co);
+    const float cc = __fmul_rn(c, co);
+    const float t = cc > 0.0f ? __fdividef(__fmul_rn(cross, cross), __fmul_rn(cc, c + co)) : 0.0f;
+    q = (q + qo) + t;
+    s = s + so;
+    c = c + co;
+}
+
+// Moments (s, q) of a row held by an aligned group of `width` lanes (a power
+// of two, at most 32) from each lane's (c, s, q): a butterfly whose steps use
+// the equal-count form of the merge, (s_b - s_a)^2 / (2c), when every lane
+// holds VPT * VEC values.
+template <int VPT, int VEC>
+__device__ __forceinline__ void group_moments(float& s, float& q, float c, int width) {
+    if (__all_sync(0xffffffffu, c == (float)(VPT * VEC))) {
+        float k = 0.5f / (float)(VPT * VEC);
+        for (int o = 1; o < width; o <<= 1) {
+            const float so = __shfl_xor_sync(0xffffffffu, s, o);
+            const float qo = __shfl_xor_sync(0xffffffffu, q, o);
+            const float d = so - s;
+            q = fmaf(__fmul_rn(d, d), k, q + qo);
+            s = s + so;
+            k *= 0.5f;
+        }
+    } else {
+        for (int o = 1; o < width; o <<= 1) {
+            const float co = __shfl_xor_sync(0xffffffffu, c, o);
+            const float so = __shfl_xor_sync(0xffffffffu, s, o);
+            const float qo = __shfl_xor_sync(0xffffffffu, q, o);
+            merge_moments(c, s, q, co, so, qo);
+        }
+    }
+}
+
+// LayerNorm for rows held inside one warp (tpr a power of two, at most 32):
+// each lane takes the moments of its own values about its own mean, with no
+// communication, and one butterfly merges them (OpLayerNorm reduces the mean
+// first and then the deviations from it: two dependent reductions a row).
+// Kept as a separate instance: carrying both reductions in one kernel cost
+// registers and measured slower on rows over several warps.
+struct OpLayerNormWarp {
+    static constexpr int kOp = RS_OP_LAYERNORM;
+    static constexpr bool kMasked = false;
+    static constexpr float kFill = 0.0f;
+    template <int DT, int VEC, int VPT, typename P>
+    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool whole,
+                                                 const P& a, float2*) {
+        float s = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return acc + x; });
+        float c, q;
+        if (whole) {
+            c = (float)(VPT * VEC);
+            const float mt = s * (1.0f / (float)(VPT * VEC));
+            q = thread_sum<VPT, VEC>(v, [mt](float acc, float x, int, int) {
+                const float d = x - mt;
+                return fmaf(d, d, acc);
+            });
+        } else {  // absent elements hold 0, not the mean: leave them out
+            // U whole units, the partial one (n mod VEC elements) held by lane
+            // U mod tpr; lane t holds U / tpr whole units, one more if t < U mod tpr.
+            const int U = n / VEC;
+            const int rem = n - U * VEC;
+            const int r = U & (tpr - 1);
+            c = (float)(VEC * ((U >> (__popc(tpr - 1))) + (t < r ? 1 : 0)) + (t == r ? rem : 0));
+            const float mt = c > 0.0f ? __fdividef(s, c) : 0.0f;
+            q = thread_sum<VPT, VEC>(v, [mt, t, tpr, n](float acc, float x, int k, int e) {
+                const float d = x - mt;
+                return (t + k * tpr) * VEC + e < n ? fmaf(d, d, acc) : acc;
+            });
+        }
+        group_moments<VPT, VEC>(s, q, c, tpr);
+        const float mean = s / (float)n;
+        const float r = 1.0f / sqrtf(q / (float)n + a.eps);
+        const float nmr = -mean * r;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            float w[VEC], b[VEC];
+            a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
+            a.template b_unit<DT, VEC>((t + k * tpr) * VEC, b);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
+        }
+    }
+};
+
 }  // namespace rs

@@ -135,6 +135,32 @@ def test_rows_path_thread_shapes(op, dtype, tpr, vpt, grid_limit):
     _check(op, x, y, w, b, what=f"{op} rows tpr={tpr} vpt={vpt}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING])
+@pytest.mark.parametrize("tpr", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("short", [0, 1, 3, "unit", "half"])
+def test_layernorm_rows_inside_one_warp(dtype, path, tpr, short):
+    # Rows held by one warp take each lane's moments about its own mean and
+    # merge them in one butterfly; ragged rows give the lanes different
+    # counts (a partial unit, lanes with one unit fewer, empty lanes), and a
+    # large common offset with unit variance is where a wrong merge shows.
+    vec = 4 if dtype == "f32" else 8
+    vpt = 2
+    cap = tpr * vpt * vec
+    k = {"unit": vec + 1, "half": cap // 2}.get(short, short)
+    N = max(1, cap - k)
+    x, out = _aligned(50, N, dtype, kind="offset50", seed=tpr + vec)
+    x[7, :] = 1000.0  # a constant row (zero variance)
+    w, b = _params(N, dtype, seed=tpr)
+    opts = {"path": path, "threads_per_row": tpr, "vec_per_thread": vpt}
+    ok, plan = _servable("ln", x, w, b, opts)
+    if not ok:
+        pytest.skip("no plan for this shape")
+    assert plan["threads_per_row"] == tpr
+    y = _run("ln", x, w, b, out=out, options=opts)
+    _check("ln", x, y, w, b, what=f"ln one warp {dtype} tpr={tpr} N={N}")
+
+
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("N", [1, 5, 31, 100, 777, 4096])
