@@ -805,9 +805,9 @@ int rowsoftmax_device_status(unsigned int* flags, int clear) {
     if (e == cudaSuccess) e = rs::read_status_causal_f32(flags, clear != 0);
     if (e == cudaSuccess) e = rs::read_status_causal_f16(flags, clear != 0);
     if (e == cudaSuccess) e = rs::read_status_causal_bf16(flags, clear != 0);
-    if (e == cudaSuccess) e = rs::read_status_lnwarp_f32(flags, clear != 0);
-    if (e == cudaSuccess) e = rs::read_status_lnwarp_f16(flags, clear != 0);
-    if (e == cudaSuccess) e = rs::read_status_lnwarp_bf16(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_lnmerge_f32(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_lnmerge_f16(flags, clear != 0);
+    if (e == cudaSuccess) e = rs::read_status_lnmerge_bf16(flags, clear != 0);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return fail_cuda(e);

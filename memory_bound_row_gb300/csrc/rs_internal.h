@@ -170,17 +170,30 @@ cudaError_t causal_max_clusters_bf16(const rs_plan& p, int* n);
 cudaError_t read_status_causal_f32(unsigned int* flags, bool clear);
 cudaError_t read_status_causal_f16(unsigned int* flags, bool clear);
 cudaError_t read_status_causal_bf16(unsigned int* flags, bool clear);
-// LayerNorm on rows held inside one warp (plan.threads_per_row <= 32),
-// plan.path RS_PATH_ROWS or RS_PATH_RING: OpLayerNormWarp instances.
-cudaError_t launch_lnwarp_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
-                              int64_t ldo, cudaStream_t s, const RowArgs& a);
-cudaError_t launch_lnwarp_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
-                              int64_t ldo, cudaStream_t s, const RowArgs& a);
-cudaError_t launch_lnwarp_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+// Which LayerNorm row operation serves a planned shape on the register rows or
+// the ring: 1 = OpLayerNormWarp (rows inside one warp), 2 = OpLayerNormWhole
+// (vectorised rows that fill their threads exactly over a power-of-two number
+// of warps), 0 = OpLayerNorm (the others, and the other paths).
+inline int layernorm_merge_kind(const rs_plan& p, int64_t N, int vec_full) {
+    if (p.path != RS_PATH_ROWS && p.path != RS_PATH_RING) return 0;
+    const int tpr = p.threads_per_row;
+    if (tpr <= 32) return 1;
+    const int wpr = tpr / 32;
+    if (p.vec_elems == vec_full && (wpr & (wpr - 1)) == 0 &&
+        N == (int64_t)tpr * p.vec_per_thread * p.vec_elems)
+        return 2;
+    return 0;
+}
+// LayerNorm instances with one merge of per-lane moments (kind 1 or 2 above).
+cudaError_t launch_lnmerge_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                                int64_t ldo, cudaStream_t s, const RowArgs& a);
-cudaError_t read_status_lnwarp_f32(unsigned int* flags, bool clear);
-cudaError_t read_status_lnwarp_f16(unsigned int* flags, bool clear);
-cudaError_t read_status_lnwarp_bf16(unsigned int* flags, bool clear);
+cudaError_t launch_lnmerge_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                               int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t launch_lnmerge_bf16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
+                                int64_t ldo, cudaStream_t s, const RowArgs& a);
+cudaError_t read_status_lnmerge_f32(unsigned int* flags, bool clear);
+cudaError_t read_status_lnmerge_f16(unsigned int* flags, bool clear);
+cudaError_t read_status_lnmerge_bf16(unsigned int* flags, bool clear);
 
 // cudaOccupancyMaxActiveClusters of a planned register-holding cluster launch
 // of a normalisation (plan.op).

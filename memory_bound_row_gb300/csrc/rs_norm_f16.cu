@@ -36,8 +36,8 @@ static cudaError_t launch_norm_op(const rs_plan& p, const void* in, void* out, i
 cudaError_t launch_norm_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                             int64_t ldo, cudaStream_t s, const RowArgs& a) {
     if (p.op == RS_OP_RMSNORM) return launch_norm_op<OpRmsNorm>(p, in, out, M, N, ldi, ldo, s, a);
-    if (p.op == RS_OP_LAYERNORM && (p.path == RS_PATH_ROWS || p.path == RS_PATH_RING) && p.threads_per_row <= 32)
-        return launch_lnwarp_f16(p, in, out, M, N, ldi, ldo, s, a);
+    if (p.op == RS_OP_LAYERNORM && layernorm_merge_kind(p, N, Traits<RS_F16>::kVec) != 0)
+        return launch_lnmerge_f16(p, in, out, M, N, ldi, ldo, s, a);
     if (p.op == RS_OP_LAYERNORM) return launch_norm_op<OpLayerNorm>(p, in, out, M, N, ldi, ldo, s, a);
     return cudaErrorInvalidConfiguration;
 }

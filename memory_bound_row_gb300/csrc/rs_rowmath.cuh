@@ -342,22 +342,27 @@ __device__ __forceinline__ void merge_moments(float& c, float& s, float& q, floa
     c = c + co;
 }
 
+// Butterfly over aligned groups of `width` lanes (a power of two, at most 32)
+// whose lanes' sets all hold the same count c: each step's correction is
+// (s_b - s_a)^2 / (2c), with k = 1 / (2c) on entry, halved as c doubles.
+__device__ __forceinline__ void equal_moments(float& s, float& q, float k, int width) {
+    for (int o = 1; o < width; o <<= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, s, o);
+        const float qo = __shfl_xor_sync(0xffffffffu, q, o);
+        const float d = so - s;
+        q = fmaf(__fmul_rn(d, d), k, q + qo);
+        s = s + so;
+        k *= 0.5f;
+    }
+}
+
 // Moments (s, q) of a row held by an aligned group of `width` lanes (a power
-// of two, at most 32) from each lane's (c, s, q): a butterfly whose steps use
-// the equal-count form of the merge, (s_b - s_a)^2 / (2c), when every lane
-// holds VPT * VEC values.
+// of two, at most 32) from each lane's (c, s, q): the equal-count butterfly
+// when every lane holds VPT * VEC values, else the general merge.
 template <int VPT, int VEC>
 __device__ __forceinline__ void group_moments(float& s, float& q, float c, int width) {
     if (__all_sync(0xffffffffu, c == (float)(VPT * VEC))) {
-        float k = 0.5f / (float)(VPT * VEC);
-        for (int o = 1; o < width; o <<= 1) {
-            const float so = __shfl_xor_sync(0xffffffffu, s, o);
-            const float qo = __shfl_xor_sync(0xffffffffu, q, o);
-            const float d = so - s;
-            q = fmaf(__fmul_rn(d, d), k, q + qo);
-            s = s + so;
-            k *= 0.5f;
-        }
+        equal_moments(s, q, 0.5f / (float)(VPT * VEC), width);
     } else {
         for (int o = 1; o < width; o <<= 1) {
             const float co = __shfl_xor_sync(0xffffffffu, c, o);
@@ -368,12 +373,38 @@ __device__ __forceinline__ void group_moments(float& s, float& q, float c, int w
     }
 }
 
+// The LayerNorm output from the row's moments: ((x * r) - mean * r) * w + b.
+template <int DT, int VEC, int VPT, typename P>
+__device__ __forceinline__ void layernorm_out(float (&v)[VPT][VEC], int t, int tpr, int n, float s, float q,
+                                              const P& a) {
+    const float mean = s / (float)n;
+    const float r = 1.0f / sqrtf(q / (float)n + a.eps);
+    const float nmr = -mean * r;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        float w[VEC], b[VEC];
+        a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
+        a.template b_unit<DT, VEC>((t + k * tpr) * VEC, b);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
+    }
+}
+
+// A lane's moments about its own mean when all VPT * VEC of its values lie in
+// the row.
+template <int VPT, int VEC>
+__device__ __forceinline__ float whole_deviations(const float (&v)[VPT][VEC], float s) {
+    const float mt = s * (1.0f / (float)(VPT * VEC));
+    return thread_sum<VPT, VEC>(v, [mt](float acc, float x, int, int) {
+        const float d = x - mt;
+        return fmaf(d, d, acc);
+    });
+}
+
 // LayerNorm for rows held inside one warp (tpr a power of two, at most 32):
 // each lane takes the moments of its own values about its own mean, with no
 // communication, and one butterfly merges them (OpLayerNorm reduces the mean
 // first and then the deviations from it: two dependent reductions a row).
-// Kept as a separate instance: carrying both reductions in one kernel cost
-// registers and measured slower on rows over several warps.
 struct OpLayerNormWarp {
     static constexpr int kOp = RS_OP_LAYERNORM;
     static constexpr bool kMasked = false;
@@ -385,11 +416,7 @@ struct OpLayerNormWarp {
         float c, q;
         if (whole) {
             c = (float)(VPT * VEC);
-            const float mt = s * (1.0f / (float)(VPT * VEC));
-            q = thread_sum<VPT, VEC>(v, [mt](float acc, float x, int, int) {
-                const float d = x - mt;
-                return fmaf(d, d, acc);
-            });
+            q = whole_deviations<VPT, VEC>(v, s);
         } else {  // absent elements hold 0, not the mean: leave them out
             // U whole units, the partial one (n mod VEC elements) held by lane
             // U mod tpr; lane t holds U / tpr whole units, one more if t < U mod tpr.
@@ -404,17 +431,35 @@ struct OpLayerNormWarp {
             });
         }
         group_moments<VPT, VEC>(s, q, c, tpr);
-        const float mean = s / (float)n;
-        const float r = 1.0f / sqrtf(q / (float)n + a.eps);
-        const float nmr = -mean * r;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            float w[VEC], b[VEC];
-            a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
-            a.template b_unit<DT, VEC>((t + k * tpr) * VEC, b);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
-        }
+        layernorm_out<DT, VEC, VPT>(v, t, tpr, n, s, q, a);
+    }
+};
+
+// LayerNorm for rows that fill their threads exactly (n = tpr * VPT * VEC)
+// over a power-of-two number of warps: every lane, and every warp, holds the
+// same count, so the lanes' moments merge in the equal-count butterfly inside
+// each warp and again across the row's warps (one CTA barrier a row).
+struct OpLayerNormWhole {
+    static constexpr int kOp = RS_OP_LAYERNORM;
+    static constexpr bool kMasked = false;
+    static constexpr float kFill = 0.0f;
+    template <int DT, int VEC, int VPT, typename P>
+    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool,
+                                                 const P& a, float2* part) {
+        float s = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return acc + x; });
+        float q = whole_deviations<VPT, VEC>(v, s);
+        equal_moments(s, q, 0.5f / (float)(VPT * VEC), 32);
+        const int warp = threadIdx.x >> 5;
+        const int lane = threadIdx.x & 31;
+        const int wpr = tpr >> 5;
+        if (lane == 0) part[warp] = make_float2(s, q);
+        __syncthreads();
+        const float2 p = lane < wpr ? part[(warp / wpr) * wpr + lane] : make_float2(0.0f, 0.0f);
+        float sj = p.x, qj = p.y;
+        equal_moments(sj, qj, 0.5f / (float)(32 * VPT * VEC), wpr);
+        s = __shfl_sync(0xffffffffu, sj, 0);
+        q = __shfl_sync(0xffffffffu, qj, 0);
+        layernorm_out<DT, VEC, VPT>(v, t, tpr, n, s, q, a);
     }
 };
 

@@ -161,6 +161,29 @@ def test_layernorm_rows_inside_one_warp(dtype, path, tpr, short):
     _check("ln", x, y, w, b, what=f"ln one warp {dtype} tpr={tpr} N={N}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING])
+@pytest.mark.parametrize("tpr,vpt", [(64, 1), (64, 8), (128, 4), (256, 2), (512, 1), (1024, 1), (96, 2), (160, 3)])
+@pytest.mark.parametrize("grid_limit", [0, 3])
+def test_layernorm_rows_that_fill_their_warps(dtype, path, tpr, vpt, grid_limit):
+    # Rows that fill their threads exactly over a power-of-two number of warps
+    # merge equal-count moments across the warps; 3 and 5 warps a row take
+    # the two-reduction LayerNorm.  Persistent grids (grid_limit) loop over
+    # rows, reusing the per-warp partials.
+    vec = 4 if dtype == "f32" else 8
+    N = tpr * vpt * vec
+    x, out = _aligned(40, N, dtype, kind="offset50", seed=tpr * vpt)
+    x[3, :] = -7.0  # a constant row
+    w, b = _params(N, dtype, seed=vpt)
+    opts = {"path": path, "threads_per_row": tpr, "vec_per_thread": vpt, "grid_limit": grid_limit}
+    ok, plan = _servable("ln", x, w, b, opts)
+    if not ok:
+        pytest.skip("no plan for this shape")
+    assert plan["threads_per_row"] == tpr
+    y = _run("ln", x, w, b, out=out, options=opts)
+    _check("ln", x, y, w, b, what=f"ln filled warps {dtype} tpr={tpr} vpt={vpt}")
+
+
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("N", [1, 5, 31, 100, 777, 4096])
