@@ -24,8 +24,11 @@
 //              the textbook parallel-variance identity (Chan, Golub and
 //              LeVeque): mu = sum S_c / N,
 //              sum (x - mu)^2 = sum_c [Q_c + n_c (mu_c - mu)^2],
-//              so the variance is exact algebra of two-pass slice moments and
-//              no global E[x^2] - mu^2 cancellation occurs.
+//              so the variance is exact algebra of slice moments and no global
+//              E[x^2] - mu^2 cancellation occurs.  A slice's own (S_c, Q_c)
+//              come the same way from its threads' moments about their own
+//              means, merged over warps and then over the CTA's warps (one
+//              CTA barrier a row).
 //
 // Waits are bounded by %globaltimer (a wait that runs out sets bit 0 of the
 // device status word, the CTA stops issuing copies, waits a second bounded
@@ -213,9 +216,27 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
         } else if constexpr (OP::kOp == RS_OP_RMSNORM) {
             a0 = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return fmaf(x, x, acc); });
         } else {
+            // LayerNorm: this thread's sum and squared deviations about its own
+            // mean, merged over the warp (m carries the deviations).
             a0 = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return acc + x; });
+            float c, q;
+            if (whole) {
+                c = (float)(VPT * VEC);
+                q = whole_deviations<VPT, VEC>(v, a0);
+            } else {  // absent elements hold 0: leave them out
+                const int U = len / VEC;
+                const int r = U & (tpr - 1);
+                c = (float)(VEC * ((U >> __popc(tpr - 1)) + (tid < r ? 1 : 0)) + (tid == r ? len - U * VEC : 0));
+                const float mt = c > 0.0f ? __fdividef(a0, c) : 0.0f;
+                q = thread_sum<VPT, VEC>(v, [mt, tid, tpr, len](float acc, float x, int k, int e) {
+                    const float d = x - mt;
+                    return (tid + k * tpr) * VEC + e < len ? fmaf(d, d, acc) : acc;
+                });
+            }
+            group_moments<VPT, VEC>(a0, q, c, 32);
+            m = q;
         }
-        a0 = group_sum(a0, 32);
+        if constexpr (OP::kOp != RS_OP_LAYERNORM) a0 = group_sum(a0, 32);
 
         // CTA merge of the warps' partials.  The barrier also ends every read
         // of the slot, which is then handed to the copy of a later row.
@@ -240,28 +261,32 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             pm = __shfl_sync(0xffffffffu, group_sum(pl, pow2_ceil(nwarps)), 0);  // the slice's sum of squares
             pl = 0.0f;
         } else {
-            // The slice's sum, then its squared deviations from its own mean
-            // (a second CTA reduction through the other half of the pairs).
-            const float sc = __shfl_sync(0xffffffffu, group_sum(pl, pow2_ceil(nwarps)), 0);
-            const float mu_c = len > 0 ? sc / (float)len : 0.0f;
-            float d;
-            if (whole) {
-                d = thread_sum<VPT, VEC>(v, [mu_c](float acc, float x, int, int) {
-                    const float dx = x - mu_c;
-                    return fmaf(dx, dx, acc);
-                });
+            // The warps' moments (lanes 0..nwarps-1: deviations, sum) merged into
+            // the slice's sum and squared deviations from its own mean: equal
+            // counts when the slice fills the CTA, else each warp's count.
+            float sj = pl, qj = lane < nwarps ? pm : 0.0f;
+            if (len == tpr * VPT * VEC) {
+                equal_moments(sj, qj, 0.5f / (float)(32 * VPT * VEC), nwarps);
             } else {
-                d = thread_sum<VPT, VEC>(v, [mu_c, tid, tpr, len](float acc, float x, int k, int e) {
-                    const float dx = x - mu_c;
-                    return (tid + k * tpr) * VEC + e < len ? fmaf(dx, dx, acc) : acc;
-                });
+                float cj = 0.0f;
+                if (lane < nwarps) {
+                    const int U = len / VEC;
+                    const int rem = len - U * VEC;
+                    const int qq = U >> __popc(tpr - 1);
+                    const int r = U & (tpr - 1);
+                    const int a = lane * 32;
+                    const int lo = r - a < 0 ? 0 : (r - a > 32 ? 32 : r - a);
+                    cj = (float)(VEC * (32 * qq + lo) + ((rem != 0 && r >= a && r < a + 32) ? rem : 0));
+                }
+                for (int o = 1; o < pow2_ceil(nwarps); o <<= 1) {
+                    const float co = __shfl_xor_sync(0xffffffffu, cj, o);
+                    const float so = __shfl_xor_sync(0xffffffffu, sj, o);
+                    const float qo = __shfl_xor_sync(0xffffffffu, qj, o);
+                    merge_moments(cj, sj, qj, co, so, qo);
+                }
             }
-            d = group_sum(d, 32);
-            if (lane == 0) warp_part[it & 1][warp].x = d;
-            __syncthreads();
-            float q = lane < nwarps ? warp_part[it & 1][lane].x : 0.0f;
-            pm = sc;
-            pl = __shfl_sync(0xffffffffu, group_sum(q, pow2_ceil(nwarps)), 0);
+            pm = __shfl_sync(0xffffffffu, sj, 0);
+            pl = __shfl_sync(0xffffffffu, qj, 0);
         }
 
         // Cluster merge: warp 0 pushes this CTA's pair into slot `rank` of
