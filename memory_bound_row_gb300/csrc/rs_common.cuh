@@ -199,6 +199,20 @@ __device__ __forceinline__ float ex2_approx(float y) {
 // then scaled into base 2.
 __device__ __forceinline__ float exp_diff(float x, float ms) { return ex2_approx((x - ms) * kLog2e); }
 
+// The register-holding cluster kernel takes exponentials against a set's
+// offset: with m the set's max, o = rn(m * log2 e) and exp(x - m) taken as
+// 2^fma(x, log2 e, -o) -- one FMA and one ex2 an element.  Every value of
+// the set shares the rounding of o, which cancels when the set is
+// normalised, and sets merge with weights 2^(o_i - o) built from the same
+// rounded offsets, so the cancellation survives the merges.  (The row
+// kernels keep 2^((x - m) * log2 e), which measured faster there.)
+__device__ __forceinline__ float safe_offset(float o) { return o == kNegInf ? 0.0f : o; }
+__device__ __forceinline__ float exp_off(float x, float os) { return ex2_approx(fmaf(x, kLog2e, -os)); }
+// Weight of a partial sum taken against offset o when the merged offset is os.
+__device__ __forceinline__ float rescale_off(float o, float os) {
+    return o == kNegInf ? 0.0f : ex2_approx(o - os);
+}
+
 // Weight of a partial sum taken against max m when the merged max is ms.
 __device__ __forceinline__ float rescale(float m, float ms) {
     return m == kNegInf ? 0.0f : exp_diff(m, ms);
@@ -225,6 +239,13 @@ __device__ __forceinline__ void group_merge(float& m, float& l, int width) {
     const float mm = group_max(m, width);
     l = group_sum(l * rescale(m, safe_max(mm)), width);
     m = mm;
+}
+
+// group_merge for (offset, l) pairs: o = max_i o_i, l = sum_i l_i 2^(o_i - o).
+__device__ __forceinline__ void group_merge_off(float& o, float& l, int width) {
+    const float oo = group_max(o, width);
+    l = group_sum(l * rescale_off(o, safe_offset(oo)), width);
+    o = oo;
 }
 
 }  // namespace rs

@@ -15,9 +15,11 @@
 // distributed shared memory: every CTA pushes one pair of floats into a slot
 // of every CTA of its cluster (st.async, counted on the receivers' mbarrier)
 // and combines the cluster's pairs itself.  The pair of a slice is
-//   softmax    (m, l): its max and its sum of exp(x - m); pairs merge with the
-//              online normaliser of the mohakchugh.is-a.dev post ("How Flash
-//              Attention Uses Triton"): m = max m_c, l = sum l_c exp(m_c - m);
+//   softmax    (o, l): its offset o = rn(m log2 e), m its max, and its sum
+//              of exp(x - m) taken as 2^fma(x, log2 e, -o); pairs merge with
+//              the online normaliser of the mohakchugh.is-a.dev post ("How
+//              Flash Attention Uses Triton") in the base-2 domain:
+//              o = max o_c, l = sum l_c 2^(o_c - o);
 //   RMSNorm    (sum of x^2, 0): sums add;
 //   LayerNorm  (S_c, Q_c): the slice's sum and its sum of squared deviations
 //              from the slice's own mean mu_c = S_c / n_c; slices combine with
@@ -204,13 +206,13 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
-            m = group_max(m, 32);
-            const float ms = safe_max(m);
+            m = group_max(m, 32) * kLog2e;  // from here on the warp's offset
+            const float os = safe_offset(m);
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    v[k][e] = exp_diff(v[k][e], ms);
+                    v[k][e] = exp_off(v[k][e], os);
                     a0 += v[k][e];
                 }
         } else if constexpr (OP::kOp == RS_OP_RMSNORM) {
@@ -254,7 +256,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             pl = q.y;
         }
         if constexpr (kSoftmax) {
-            group_merge(pm, pl, pow2_ceil(nwarps));  // lanes 0..nwarps-1 hold the CTA's pair
+            group_merge_off(pm, pl, pow2_ceil(nwarps));  // lanes 0..nwarps-1 hold the CTA's pair
             pm = __shfl_sync(0xffffffffu, pm, 0);
             pl = __shfl_sync(0xffffffffu, pl, 0);
         } else if constexpr (OP::kOp == RS_OP_RMSNORM) {
@@ -309,10 +311,10 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             qb = q.y;
         }
         if constexpr (kSoftmax) {
-            group_merge(qa, qb, pow2_ceil(cs));
+            group_merge_off(qa, qb, pow2_ceil(cs));
             qa = __shfl_sync(0xffffffffu, qa, 0);
             qb = __shfl_sync(0xffffffffu, qb, 0);
-            const float c = rescale(m, safe_max(qa)) / qb;
+            const float c = rescale_off(m, safe_offset(qa)) / qb;
             __syncwarp();
             if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
 #pragma unroll
