@@ -171,8 +171,10 @@ def op_bytes(op: str, w) -> int:
     return w.algorithmic_bytes + vectors * w.N * w.elem_size
 
 
-def traffic_key(op: str, name: str) -> str:
-    return name if op == "softmax" else f"{op}:{name}"
+def traffic_key(op: str, name: str, causal: bool = False) -> str:
+    if op == "softmax":
+        return f"causal:{name}" if causal else name
+    return f"{op}:{name}"
 
 
 def oracle_op(op: str, x_np, fmt: str, n_cols: int, params, threads: int, out=None):
@@ -533,7 +535,7 @@ def run_ours(args, workloads):
                                  f"{reuse_mb:.0f} MB pass between two uses of a set (L2 is 129 MB)",
                            "kernel": rs.PATH_NAMES[plan["path"]], "plan": plan},
                 "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(achieved / peak, 4), "traffic": None if (args.options or args.rows) else ncu_traffic(traffic_key(op, name)),
+                             "frac": round(achieved / peak, 4), "traffic": None if (args.options or args.rows) else ncu_traffic(traffic_key(op, name, args.causal)),
                              "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
                              if peak_src == "measured" else "fallback 6.8 TB/s",
                              "kernel_ms": round(kern_ms, 5),
