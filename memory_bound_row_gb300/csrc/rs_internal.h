@@ -173,7 +173,12 @@ cudaError_t read_status_causal_bf16(unsigned int* flags, bool clear);
 // Which LayerNorm row operation serves a planned shape on the register rows or
 // the ring: 1 = OpLayerNormWarp (rows inside one warp), 2 = OpLayerNormWhole
 // (vectorised rows that fill their threads exactly over a power-of-two number
-// of warps), 0 = OpLayerNorm (the others, and the other paths).
+// of warps), 3 = OpLayerNormWholeHeld (kind 2 on the ring with at most 4 units
+// a thread and kHeldThreads threads a CTA: the weight and bias held in
+// registers, kHeldRegs a thread), 0 = OpLayerNorm (the others, and the other
+// paths).
+constexpr int kHeldThreads = 256;
+constexpr int kHeldRegs = 128;
 inline int layernorm_merge_kind(const rs_plan& p, int64_t N, int vec_full) {
     if (p.path != RS_PATH_ROWS && p.path != RS_PATH_RING) return 0;
     const int tpr = p.threads_per_row;
@@ -181,10 +186,10 @@ inline int layernorm_merge_kind(const rs_plan& p, int64_t N, int vec_full) {
     const int wpr = tpr / 32;
     if (p.vec_elems == vec_full && (wpr & (wpr - 1)) == 0 &&
         N == (int64_t)tpr * p.vec_per_thread * p.vec_elems)
-        return 2;
+        return p.path == RS_PATH_RING && p.vec_per_thread <= 4 && p.block_threads <= kHeldThreads ? 3 : 2;
     return 0;
 }
-// LayerNorm instances with one merge of per-lane moments (kind 1 or 2 above).
+// LayerNorm instances with one merge of per-lane moments (kinds 1, 2 and 3 above).
 cudaError_t launch_lnmerge_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                                int64_t ldo, cudaStream_t s, const RowArgs& a);
 cudaError_t launch_lnmerge_f16(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,

@@ -54,8 +54,10 @@ __device__ __forceinline__ void ring_unit(const unsigned char* srow, const typen
 }
 
 template <int DT, int VPT, bool HOLD, typename OP>
-__global__ void __launch_bounds__(HOLD ? rows_block_limit(VPT, Traits<DT>::kVec) : kRingRereadThreads,
-                                  HOLD ? 1 : kRingRereadMinCtas)
+__global__ void __launch_bounds__(HOLD ? (OP::kHeldParams ? kHeldThreads : rows_block_limit(VPT, Traits<DT>::kVec))
+                                       : kRingRereadThreads,
+                                  HOLD ? (OP::kHeldParams ? 65536 / (kHeldThreads * kHeldRegs) : 1)
+                                       : kRingRereadMinCtas)
 ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int tpr, int stages,
             uint64_t wait_ns, int withhold, RowArgs args) {
     static_assert(HOLD || (OP::kOp == RS_OP_SOFTMAX && !OP::kMasked), "the re-read variant is the softmax's only");
@@ -119,10 +121,21 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
     // 33 % faster on 2048-value bf16 rows).  RMSNorm reads its one vector
     // through the read-only cache: staging it cost more in resident CTAs than
     // it saved.
-    constexpr bool kStage = OP::kOp == RS_OP_LAYERNORM;
-    using Params = typename std::conditional<kStage, SharedParams<DT>, GlobalParams>::type;
+    constexpr bool kHeld = OP::kHeldParams;
+    constexpr bool kStage = OP::kOp == RS_OP_LAYERNORM && !kHeld;
+    using Params = typename std::conditional<
+        kHeld, HeldParams<VPT, VEC>,
+        typename std::conditional<kStage, SharedParams<DT>, GlobalParams>::type>::type;
     Params prm;
-    if constexpr (kStage) {
+    if constexpr (kHeld) {
+        const GlobalParams g{args.w, args.b, args.eps, N, 0};
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            g.template w_unit<DT, VEC>((t + k * tpr) * VEC, prm.w[k]);
+            g.template b_unit<DT, VEC>((t + k * tpr) * VEC, prm.b[k]);
+        }
+        prm.eps = args.eps;
+    } else if constexpr (kStage) {
         const int npad = ((N + VEC - 1) / VEC) * VEC;
         S* sw = nullptr;
         S* sb = nullptr;

@@ -196,6 +196,30 @@ struct GlobalParams {
     __device__ __forceinline__ void b_unit(int base, float* f) const {
         load_param_unit<DT, VEC>(b, offset + base, n, f, 0.0f);
     }
+    template <int DT, int VEC>
+    __device__ __forceinline__ void w_unit_k(int, int base, float* f) const { w_unit<DT, VEC>(base, f); }
+    template <int DT, int VEC>
+    __device__ __forceinline__ void b_unit_k(int, int base, float* f) const { b_unit<DT, VEC>(base, f); }
+};
+
+// The weight and bias units of a thread's VPT units held in registers as fp32
+// (a persistent kernel whose threads serve the same columns of every row),
+// read by unit index k.
+template <int VPT, int VEC>
+struct HeldParams {
+    float w[VPT][VEC];
+    float b[VPT][VEC];
+    float eps;
+    template <int DT, int V>
+    __device__ __forceinline__ void w_unit_k(int k, int, float* f) const {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = w[k][e];
+    }
+    template <int DT, int V>
+    __device__ __forceinline__ void b_unit_k(int k, int, float* f) const {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = b[k][e];
+    }
 };
 
 template <int DT>
@@ -225,6 +249,10 @@ struct SharedParams {
             for (int e = 0; e < VEC; ++e) f[e] = 0.0f;
         }
     }
+    template <int DT2, int VEC>
+    __device__ __forceinline__ void w_unit_k(int, int base, float* f) const { w_unit<DT2, VEC>(base, f); }
+    template <int DT2, int VEC>
+    __device__ __forceinline__ void b_unit_k(int, int base, float* f) const { b_unit<DT2, VEC>(base, f); }
 };
 
 // Copies the elements [c0, c0 + len) of a parameter vector into shared memory
@@ -243,6 +271,7 @@ __device__ __forceinline__ void stage_param(typename Traits<DT>::storage* dst, c
 }
 
 struct OpSoftmax {
+    static constexpr bool kHeldParams = false;
     static constexpr int kOp = RS_OP_SOFTMAX;
     static constexpr bool kMasked = false;
     static constexpr float kFill = kNegInf;
@@ -268,6 +297,7 @@ struct OpSoftmaxCausal : OpSoftmax {
 // RMSNorm ("Reference Kernel: RMSNorm", Hugging Face "triton-kernels" skill
 // page): y = x * rsqrt(sum(x^2)/N + eps) * w, accumulated in fp32.
 struct OpRmsNorm {
+    static constexpr bool kHeldParams = false;
     static constexpr int kOp = RS_OP_RMSNORM;
     static constexpr bool kMasked = false;
     static constexpr float kFill = 0.0f;  // absent elements add nothing to the sum of squares
@@ -291,6 +321,7 @@ struct OpRmsNorm {
 // the two moments reduced one after the other (two passes over registers);
 // the output is formed as ((x * r) - mean * r) * w + b with two FMAs.
 struct OpLayerNorm {
+    static constexpr bool kHeldParams = false;
     static constexpr int kOp = RS_OP_LAYERNORM;
     static constexpr bool kMasked = false;
     static constexpr float kFill = 0.0f;
@@ -383,8 +414,8 @@ __device__ __forceinline__ void layernorm_out(float (&v)[VPT][VEC], int t, int t
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         float w[VEC], b[VEC];
-        a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
-        a.template b_unit<DT, VEC>((t + k * tpr) * VEC, b);
+        a.template w_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, w);
+        a.template b_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, b);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
     }
@@ -406,6 +437,7 @@ __device__ __forceinline__ float whole_deviations(const float (&v)[VPT][VEC], fl
 // communication, and one butterfly merges them (OpLayerNorm reduces the mean
 // first and then the deviations from it: two dependent reductions a row).
 struct OpLayerNormWarp {
+    static constexpr bool kHeldParams = false;
     static constexpr int kOp = RS_OP_LAYERNORM;
     static constexpr bool kMasked = false;
     static constexpr float kFill = 0.0f;
@@ -440,6 +472,7 @@ struct OpLayerNormWarp {
 // same count, so the lanes' moments merge in the equal-count butterfly inside
 // each warp and again across the row's warps (one CTA barrier a row).
 struct OpLayerNormWhole {
+    static constexpr bool kHeldParams = false;
     static constexpr int kOp = RS_OP_LAYERNORM;
     static constexpr bool kMasked = false;
     static constexpr float kFill = 0.0f;
@@ -461,6 +494,11 @@ struct OpLayerNormWhole {
         q = __shfl_sync(0xffffffffu, qj, 0);
         layernorm_out<DT, VEC, VPT>(v, t, tpr, n, s, q, a);
     }
+};
+
+// OpLayerNormWhole reading its weight and bias from registers (HeldParams).
+struct OpLayerNormWholeHeld : OpLayerNormWhole {
+    static constexpr bool kHeldParams = true;
 };
 
 }  // namespace rs

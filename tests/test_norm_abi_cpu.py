@@ -122,6 +122,27 @@ def test_layernorm_ring_stages_its_vectors_in_shared_memory():
     assert p["smem_bytes"] == stage * p["stages"]
 
 
+@pytest.mark.parametrize("dtype", [rs.RS_F16, rs.RS_BF16])
+def test_layernorm_rows_of_4_or_8_warps_hold_their_vectors_in_registers(dtype):
+    # 16-bit LayerNorm rows that fill 4 or 8 warps at 4 units a thread run the
+    # instance with weight and bias in registers: 256-thread CTAs, 128
+    # registers a thread, so the persistent grid is 2 CTAs an SM, and nothing
+    # is staged in shared memory beside the ring stages.
+    for N, tpr in [(4096, 128), (8192, 256)]:
+        p = _plan(rs.RS_OP_LAYERNORM, 32768, N, dtype, b=B)
+        assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] == 4 and p["threads_per_row"] == tpr
+        assert p["block_threads"] == 256 and p["grid"] == 2 * 152
+        assert p["smem_bytes"] == (N // 8) * 16 * p["rows_per_cta"] * p["stages"]
+    # rows of 2 warps keep one warp a row (measured faster), RMSNorm keeps its plan,
+    # and a ragged row of the same size keeps the staged vectors
+    p = _plan(rs.RS_OP_LAYERNORM, 32768, 2048, dtype, b=B)
+    assert p["threads_per_row"] <= 32
+    p = _plan(rs.RS_OP_RMSNORM, 32768, 8192, dtype)
+    assert p["path"] == rs.RS_PATH_RING and p["smem_bytes"] == 8192 * 2 * p["rows_per_cta"] * p["stages"]
+    p = _plan(rs.RS_OP_LAYERNORM, 32768, 8184, dtype, ld=8192, b=B)
+    assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] != 4
+
+
 def test_misaligned_parameter_vectors_select_element_wise_kernels():
     p = _plan(rs.RS_OP_RMSNORM, 64, 4096, rs.RS_BF16, w=W + 2)
     assert p["vec_elems"] == 1 and p["path"] == rs.RS_PATH_ROWS and p["vec_per_thread"] in NORM_VPT_SCALAR
