@@ -680,6 +680,120 @@ def run_sweep_n(args):
         torch.cuda.empty_cache()
 
 
+WIDE_SWEEP_N = [8192, 12288, 16384, 20480, 24576, 28672, 32768, 40960, 49152, 65536]
+WIDE_SWEEP_CONFIGS = {"auto": None, "ring": {"path": 4}, "cluster": {"path": 2}}
+
+
+def run_sweep_wide(args):
+    """Wide 16-bit rows (N = 8192..65536, M = 2^28 / N: 512 MB a tensor) for
+    the --op row operation, through the planner's choice, the bulk-copy ring
+    and the register-holding clusters, where each has a plan.  Every point is
+    checked first on 16 sampled rows against the operation evaluated by torch
+    in fp64 on the decoded inputs (softmax also: row sums within 1e-2), and the
+    configurations against each other; then timed as graph-replayed launches
+    over rotating buffers.  One JSON line per (N, configuration)."""
+    import torch
+
+    import memory_bound_row_gb300 as rs
+    from memory_bound_row_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = rs._abi.load()
+    peak, _ = measured_peaks()
+    rc, info = rs.rowsoftmax_device_info()
+    op, dt = args.op, args.sweep_dtype
+    code = {"f16": rs.RS_F16, "bf16": rs.RS_BF16}[dt]
+    tol = {"f16": 2.0 ** -9, "bf16": 2.0 ** -6}[dt]  # a few units in the last place of the output
+    for N in WIDE_SWEEP_N:
+        M = (1 << 28) // N
+        w = W.custom(M, N, dt, seed=5, kind="offset50" if op == "layernorm" else "normal1")
+        x0 = W.generate(w, dev)
+        wt, bs = W.norm_params(N, dt, 5, dev)
+        set_bytes = 2 * M * N * 2
+        nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
+        xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
+        ys = [torch.empty_like(x0) for _ in range(nsets)]
+        rows = torch.linspace(0, M - 1, 16, device=dev).long()
+        xr = x0[rows].double()
+        if op == "softmax":
+            ref = torch.softmax(xr, dim=1)
+        elif op == "rmsnorm":
+            ref = xr * torch.rsqrt((xr * xr).mean(dim=1, keepdim=True) + OP_EPS[op]) * wt.double()
+        else:
+            mu = xr.mean(dim=1, keepdim=True)
+            ref = (xr - mu) * torch.rsqrt(((xr - mu) ** 2).mean(dim=1, keepdim=True) + OP_EPS[op]) * wt.double() \
+                + bs.double()
+        torch.cuda.synchronize()
+        first = None
+        for name, opts in WIDE_SWEEP_CONFIGS.items():
+            copts = rs._abi._opts(opts)
+            if op == "softmax":
+                rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), M, N, N, N, code, opts, info)
+            else:
+                rc, plan = rs.rownorm_plan(OP_CODES[op], xs[0].data_ptr(), ys[0].data_ptr(), wt.data_ptr(),
+                                           bs.data_ptr() if op == "layernorm" else None, M, N, N, N, OP_EPS[op],
+                                           code, opts, info)
+            if rc != rs.RS_OK:
+                continue
+            stream = torch.cuda.Stream(dev)
+            h = stream.cuda_stream
+            pb = bs.data_ptr() if op == "layernorm" else None
+
+            def call(k):
+                if op == "softmax":
+                    r = lib.rowsoftmax_fwd_ex(xs[k % nsets].data_ptr(), ys[k % nsets].data_ptr(), M, N, N, N, code,
+                                              h, copts)
+                else:
+                    r = lib.rownorm_fwd_ex(OP_CODES[op], xs[k % nsets].data_ptr(), ys[k % nsets].data_ptr(),
+                                           wt.data_ptr(), pb, M, N, N, N, OP_EPS[op], code, h, copts)
+                if r != rs.RS_OK:
+                    raise rs.RowSoftmaxError(r, rs.rowsoftmax_last_cuda_error())
+
+            with torch.cuda.stream(stream):
+                call(0)
+            stream.synchronize()
+            y = ys[0][rows].double()
+            err = float(((y - ref).abs() / (1.0 + ref.abs())).max())
+            agree = 0.0 if first is None else float(((y - first).abs() / (1.0 + first.abs())).max())
+            if first is None:
+                first = y.clone()
+            sums = float((y.sum(dim=1) - 1.0).abs().max()) if op == "softmax" else 0.0
+            if not (bool(torch.isfinite(y).all()) and err <= tol and agree <= 2 * tol and sums <= 1e-2):
+                raise AssertionError(f"{op} N={N} {name}: error {err:.3e}, {agree:.3e} from the planner's")
+            G = 20
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for k in range(G):
+                    call(k)
+                stream.synchronize()
+                with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+                    for k in range(G):
+                        call(k)
+            torch.cuda.synchronize()
+            reps = max(3, args.steps // G)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / (reps * G)
+            nbytes = 2 * M * N * 2 + {"softmax": 0, "rmsnorm": 1, "layernorm": 2}[op] * N * 2
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            print(json.dumps({"sweep": f"{dt} wide rows, M = 2^28 / N", "op": op, "N": N, "M": M, "config": name,
+                              "kernel": rs.PATH_NAMES[plan["path"]], "cluster": plan["cluster_size"],
+                              "threads": plan["block_threads"], "units_a_thread": plan["vec_per_thread"],
+                              "grid": plan["grid"], "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                              "frac": round(gbs / peak, 4), "max_rel_err": round(err, 6)}), flush=True)
+            del graph
+        del xs, ys, first
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -701,6 +815,10 @@ def main():
     ap.add_argument("--sweep-n", action="store_true",
                     help="instead of the benchmark line: the fp32 M=4096, N=256..12672 sweep of the row softmax, "
                          "one JSON line per (N, kernel configuration)")
+    ap.add_argument("--sweep-wide", action="store_true",
+                    help="instead of the benchmark line: wide 16-bit rows (N = 8192..65536) of the --op row "
+                         "operation through the planner's choice, the ring and the clusters")
+    ap.add_argument("--sweep-dtype", choices=["bf16", "f16"], default="bf16")
     args = ap.parse_args()
     args.options = json.loads(args.options) if args.options else None
     if args.causal and args.op != "softmax":
@@ -715,6 +833,8 @@ def main():
             raise SystemExit(f"unknown workload {n}; choose from {', '.join(W.ORDER)} or 'all'")
     if args.sweep_n:
         run_sweep_n(args)
+    elif args.sweep_wide:
+        run_sweep_wide(args)
     elif args.impl == "reference":
         run_reference(args, names)
     else:

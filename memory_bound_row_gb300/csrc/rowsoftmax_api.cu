@@ -38,6 +38,8 @@ constexpr int64_t kRowsMaxRowBytes = 32 * 1024;   // auto: rows up to this go to
 constexpr int64_t kRowsMaxRowBytesF32 = 64 * 1024;  // ... fp32 softmax rows (measured: rows beat clusters to 64 KB)
 constexpr int64_t kClusterTargetSlice = 64 * 1024;  // auto: bytes of row slice per CTA
 constexpr int64_t kRingMinRowBytes = 512;           // auto: shorter rows stay on RS_PATH_ROWS
+constexpr int64_t kRingMaxRowBytesSoftmax16 = 64 * 1024;  // auto: the ring's limit for wide 16-bit softmax rows
+constexpr int kClusterThinValues = 16;                // ... taken when the cluster's CTAs hold at most this a thread
 constexpr int kRingDefaultStages = 2;               // auto: more stages cost resident CTAs (measured)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -105,8 +107,11 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
         } else {
             int n_inst = 0;
             const int* inst = vpt_table(p->op, dtype, vec, &n_inst);
-            const int target =
-                p->op == RS_OP_LAYERNORM && dtype != RS_F32 && vec > 1 ? kRowsTargetValuesLn16 : kRowsTargetValues;
+            // (LayerNorm on 16-bit rows over 8192 values: 32 values a thread,
+            // measured 7-19 % faster than 64.)
+            const int target = p->op == RS_OP_LAYERNORM && dtype != RS_F32 && vec > 1 && units * vec <= 8192
+                                   ? kRowsTargetValuesLn16
+                                   : kRowsTargetValues;
             int vt = target / vec > 0 ? target / vec : 1;
             if (vt > inst[n_inst - 1]) vt = inst[n_inst - 1];
             // 16-bit rows that one warp can hold at up to 64 values a thread
@@ -454,12 +459,20 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         int rc = RS_ERR_NO_PATH;
         // 16-bit rows: the ring (bytes in flight in shared memory, not in
         // registers); fp32 rows: the register kernel, whose fp32 values cost
-        // no more registers than the bytes they came from.
-        // (A 16-bit softmax row of 32 KB already goes faster through the
-        // register-holding clusters: 6156 vs 5940 GB/s measured.)
-        const int64_t ring_max = norm ? kRowsMaxRowBytes : kRowsMaxRowBytes - 1;
-        if (dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes && N * es <= ring_max)
-            rc = plan_ring(dtype, vec, M, N, units, o, *dev, p, nparams);
+        // no more registers than the bytes they came from.  The normalisations
+        // take the ring wherever its stages fit (measured 5-185 % faster than
+        // the clusters on rows of 32-64 KB); the softmax below 32 KB, and up to
+        // 64 KB where the cluster plan would spread a row thin (at most
+        // kClusterThinValues values a thread: 3278 -> 5327 GB/s on 40 KB rows;
+        // with fuller cluster shapes the clusters measured as fast or faster).
+        bool ring = dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes &&
+                    (norm || N * es < kRowsMaxRowBytes);
+        if (!ring && !norm && dtype != RS_F32 && vec_ok && N * es < kRingMaxRowBytesSoftmax16) {
+            rs_plan cp = *p;
+            ring = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, &cp) != RS_OK ||
+                   cp.vec_per_thread * cp.vec_elems <= kClusterThinValues;
+        }
+        if (ring) rc = plan_ring(dtype, vec, M, N, units, o, *dev, p, nparams);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
         const int64_t rows_max = dtype == RS_F32 && !norm ? kRowsMaxRowBytesF32

@@ -109,6 +109,17 @@ def _covers(plan, N):
     return plan["cluster_size"] * plan["chunk_elems"] >= N
 
 
+def test_wide_16bit_softmax_rows_take_the_ring_where_clusters_spread_thin():
+    # 16-bit softmax rows of 32-64 KB take the ring when the cluster plan would
+    # hold at most 16 values a thread, and keep well-filled clusters otherwise.
+    p = _plan(8192, 20480, rs.RS_BF16)  # the fill rule's cluster: 5 CTAs of 2 units a thread
+    assert p["path"] == rs.RS_PATH_RING and _covers(p, 20480)
+    for N in (16384, 24576, 28672, 32768):
+        p = _plan(8192, N, rs.RS_BF16)
+        assert p["path"] == rs.RS_PATH_CLUSTER and p["vec_per_thread"] * 8 > 16, N
+    assert _plan(4096, 40960, rs.RS_F16)["path"] == rs.RS_PATH_CLUSTER  # over 64 KB
+
+
 def test_plans_for_the_benchmark_workloads():
     # fp32: register-resident rows; 16-bit: the bulk-copy ring; vocabulary-
     # sized rows: persistent clusters holding their slices in registers.

@@ -143,6 +143,20 @@ def test_layernorm_rows_of_4_or_8_warps_hold_their_vectors_in_registers(dtype):
     assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] != 4
 
 
+def test_wide_16bit_rows_take_the_ring_where_it_fits():
+    # Normalisations: the ring wherever its stages fit, 32 values a thread for
+    # LayerNorm rows over 8192 values; beyond, the clusters.
+    for N in (12288, 20480, 28672):
+        for op in (rs.RS_OP_RMSNORM, rs.RS_OP_LAYERNORM):
+            p = _plan(op, 8192, N, rs.RS_BF16, b=B if op == rs.RS_OP_LAYERNORM else None)
+            assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] == 4 and _covers(p, N), (op, N)
+    assert _plan(rs.RS_OP_RMSNORM, 8192, 32768, rs.RS_BF16)["path"] == rs.RS_PATH_RING
+    p = _plan(rs.RS_OP_LAYERNORM, 8192, 32768, rs.RS_BF16, b=B)  # two 64 KB stages + two 64 KB vectors
+    assert p["path"] == rs.RS_PATH_CLUSTER
+    p = _plan(rs.RS_OP_RMSNORM, 8192, 40960, rs.RS_BF16)  # 1280 threads at 4 units: beyond a CTA
+    assert p["path"] == rs.RS_PATH_CLUSTER and _covers(p, 40960)
+
+
 def test_misaligned_parameter_vectors_select_element_wise_kernels():
     p = _plan(rs.RS_OP_RMSNORM, 64, 4096, rs.RS_BF16, w=W + 2)
     assert p["vec_elems"] == 1 and p["path"] == rs.RS_PATH_ROWS and p["vec_per_thread"] in NORM_VPT_SCALAR
