@@ -135,6 +135,20 @@ def test_rows_path_thread_shapes(op, dtype, tpr, vpt, grid_limit):
     _check(op, x, y, w, b, what=f"{op} rows tpr={tpr} vpt={vpt}")
 
 
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [4096, 8192, 12288, 20480, 28672, 32768, 36000])
+def test_auto_path_wide_16bit_rows(op, dtype, N):
+    # The planner's wide 16-bit rows: the held-parameter LayerNorm (4096,
+    # 8192), the ring with 32 values a thread up to 56 KB (LayerNorm) or 64 KB
+    # (RMSNorm), the clusters beyond; persistent grids loop over the rows.
+    M = 700 if N <= 12288 else 260
+    x, out = _aligned(M, N, dtype, kind="offset50" if op == "ln" else "normal1", seed=N)
+    w, b = _params(N, dtype, seed=N)
+    y = _run(op, x, w, b, out=out)
+    _check(op, x, y, w, b, what=f"{op} auto wide {dtype} N={N}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("path", [rs.RS_PATH_ROWS, rs.RS_PATH_RING])
 @pytest.mark.parametrize("tpr", [1, 2, 4, 8, 16, 32])

@@ -88,6 +88,17 @@ def test_auto_path_small_shapes(dtype, M, N):
     _check(x, _run(x), what=f"{dtype} {M}x{N}")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [16384, 20480, 24576, 28672, 32760, 40960])
+def test_auto_path_wide_16bit_rows(dtype, N):
+    # Where the planner sends wide 16-bit rows: the ring for rows the
+    # clusters would spread thin (20480), the clusters for the others, the
+    # ring's persistent CTAs looping over more rows than they are.
+    M = 700 if N <= 20480 else 300
+    x, out = _aligned(M, N, dtype, kind="normal_spike", seed=N)
+    _check(x, _run(x, out=out), what=f"auto wide {dtype} N={N}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("tpr,vpt", [(1, 1), (2, 2), (4, 3), (8, 5), (16, 8), (32, 1), (32, 6), (64, 4), (96, 2),
                                      (256, 2), (512, 1), (1024, 1), (160, 8)])
