@@ -205,7 +205,8 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     int rc = plan_rows(dtype, vec, M, units, ro, p, values == RS_RING_REGISTERS);
     if (rc != RS_OK) return rc;
     p->path = RS_PATH_RING;  // (the LayerNorm kind depends on the path)
-    const bool held = p->op == RS_OP_LAYERNORM && rs::layernorm_merge_kind(*p, N, vec) == 3;
+    const bool held = (p->op == RS_OP_LAYERNORM && rs::layernorm_merge_kind(*p, N, vec) == 3) ||
+                      (p->op == RS_OP_RMSNORM && rs::rmsnorm_ring_held(*p, vec));
     const int64_t slot = (N / vec) * 16;
     const int64_t stage = slot * p->rows_per_cta;
     if (stage <= 0) return RS_ERR_NO_PATH;

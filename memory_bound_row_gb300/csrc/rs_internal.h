@@ -189,6 +189,13 @@ inline int layernorm_merge_kind(const rs_plan& p, int64_t N, int vec_full) {
         return p.path == RS_PATH_RING && p.vec_per_thread <= 4 && p.block_threads <= kHeldThreads ? 3 : 2;
     return 0;
 }
+// RMSNorm on the ring with the weight held in registers (OpRmsNormHeld): rows
+// of at least 4 warps at up to 4 units a thread in kHeldThreads-thread CTAs
+// (measured 3.9 % faster on 8192-value bf16 rows, no change on rows of 2 warps).
+inline bool rmsnorm_ring_held(const rs_plan& p, int vec_full) {
+    return p.path == RS_PATH_RING && p.vec_elems == vec_full && p.vec_per_thread <= 4 &&
+           p.block_threads <= kHeldThreads && p.threads_per_row >= 128;
+}
 // LayerNorm instances with one merge of per-lane moments (kinds 1, 2 and 3 above).
 cudaError_t launch_lnmerge_f32(const rs_plan& p, const void* in, void* out, int64_t M, int N, int64_t ldi,
                                int64_t ldo, cudaStream_t s, const RowArgs& a);

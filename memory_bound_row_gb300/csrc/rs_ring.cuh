@@ -132,7 +132,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             g.template w_unit<DT, VEC>((t + k * tpr) * VEC, prm.w[k]);
-            g.template b_unit<DT, VEC>((t + k * tpr) * VEC, prm.b[k]);
+            if constexpr (OP::kOp == RS_OP_LAYERNORM) g.template b_unit<DT, VEC>((t + k * tpr) * VEC, prm.b[k]);
         }
         prm.eps = args.eps;
     } else if constexpr (kStage) {

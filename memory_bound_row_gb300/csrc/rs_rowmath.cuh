@@ -310,7 +310,7 @@ struct OpRmsNorm {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             float w[VEC];
-            a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
+            a.template w_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, w);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) v[k][e] = v[k][e] * r * w[e];
         }
@@ -494,6 +494,11 @@ struct OpLayerNormWhole {
         q = __shfl_sync(0xffffffffu, qj, 0);
         layernorm_out<DT, VEC, VPT>(v, t, tpr, n, s, q, a);
     }
+};
+
+// OpRmsNorm reading its weight from registers (HeldParams).
+struct OpRmsNormHeld : OpRmsNorm {
+    static constexpr bool kHeldParams = true;
 };
 
 // OpLayerNormWhole reading its weight and bias from registers (HeldParams).

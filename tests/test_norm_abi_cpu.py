@@ -137,8 +137,15 @@ def test_layernorm_rows_of_4_or_8_warps_hold_their_vectors_in_registers(dtype):
     # and a ragged row of the same size keeps the staged vectors
     p = _plan(rs.RS_OP_LAYERNORM, 32768, 2048, dtype, b=B)
     assert p["threads_per_row"] <= 32
+    # RMSNorm rows of 4 or more warps at 4 units a thread hold their weight too
+    # (2 CTAs an SM); the 12288-value rows' 384-thread CTAs read it from L1
     p = _plan(rs.RS_OP_RMSNORM, 32768, 8192, dtype)
     assert p["path"] == rs.RS_PATH_RING and p["smem_bytes"] == 8192 * 2 * p["rows_per_cta"] * p["stages"]
+    assert p["threads_per_row"] == 256 and p["block_threads"] == 256 and p["grid"] == 2 * 152
+    p = _plan(rs.RS_OP_RMSNORM, 32768, 4096, dtype)
+    assert p["threads_per_row"] == 128 and p["block_threads"] == 256 and p["grid"] == 2 * 152
+    p = _plan(rs.RS_OP_RMSNORM, 32768, 12288, dtype)
+    assert p["threads_per_row"] == 384 and p["grid"] == 2 * 152  # 64 registers, 384 threads: 2 CTAs by threads
     p = _plan(rs.RS_OP_LAYERNORM, 32768, 8184, dtype, ld=8192, b=B)
     assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] != 4
 
