@@ -40,6 +40,10 @@ constexpr int64_t kClusterTargetSlice = 64 * 1024;  // auto: bytes of row slice 
 constexpr int64_t kRingMinRowBytes = 512;           // auto: shorter rows stay on RS_PATH_ROWS
 constexpr int64_t kRingMaxRowBytesSoftmax16 = 64 * 1024;  // auto: the ring's limit for wide 16-bit softmax rows
 constexpr int kClusterThinValues = 16;                // ... taken when the cluster's CTAs hold at most this a thread
+constexpr int kLnHeldMinThreadsF32 = 128;            // auto: fp32 LayerNorm rows not filling a power-of-two
+                                                      // number of warps, of 128..256 threads at 8 units a
+                                                      // thread, take the ring with held weight and bias ...
+constexpr int kLnHeldMinWarpsF32 = 14;               // ... when this many warps of it fit an SM
 constexpr int kRingDefaultStages = 2;               // auto: more stages cost resident CTAs (measured)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -205,8 +209,8 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     int rc = plan_rows(dtype, vec, M, units, ro, p, values == RS_RING_REGISTERS);
     if (rc != RS_OK) return rc;
     p->path = RS_PATH_RING;  // (the LayerNorm kind depends on the path)
-    const bool held = (p->op == RS_OP_LAYERNORM && rs::layernorm_merge_kind(*p, N, vec) == 3) ||
-                      (p->op == RS_OP_RMSNORM && rs::rmsnorm_ring_held(*p, vec));
+    const int lkind = p->op == RS_OP_LAYERNORM ? rs::layernorm_merge_kind(*p, N, vec) : 0;
+    const bool held = lkind == 3 || lkind == 4 || (p->op == RS_OP_RMSNORM && rs::rmsnorm_ring_held(*p, vec));
     const int64_t slot = (N / vec) * 16;
     const int64_t stage = slot * p->rows_per_cta;
     if (stage <= 0) return RS_ERR_NO_PATH;
@@ -473,7 +477,28 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
             ring = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, &cp) != RS_OK ||
                    cp.vec_per_thread * cp.vec_elems <= kClusterThinValues;
         }
-        if (ring) rc = plan_ring(dtype, vec, M, N, units, o, *dev, p, nparams);
+        // LayerNorm on fp32 rows that would take two reductions on the register
+        // rows (ragged, or not a power-of-two number of warps) and span 4 to 8
+        // warps at 8 units a thread: the ring, whose CTAs hold the weight and
+        // bias in registers across their rows, where at least kLnHeldMinWarpsF32
+        // warps fit an SM (measured +8.6 to +10 % on 4100-, 5000- and 7000-value
+        // rows; 6000-value rows, 192-thread CTAs of which 2 fit an SM, -8.7 %;
+        // rows that fill their warps, and rows of 2 warps, faster on the register
+        // rows).
+        rs_options ro = o;
+        if (op == RS_OP_LAYERNORM && dtype == RS_F32 && vec_ok && !o.vec_per_thread && !o.threads_per_row &&
+            !o.block_threads) {
+            const int64_t t8 = round_up(ceil_div(units, 8), 32);
+            const int64_t w8 = t8 / 32;
+            const bool filled = N == t8 * 32 && (w8 & (w8 - 1)) == 0;
+            const int64_t warps_per_sm = (65536 / (t8 * rs::kHeldRegs)) * w8;
+            if (t8 >= kLnHeldMinThreadsF32 && t8 <= rs::kHeldThreads && !filled &&
+                warps_per_sm >= kLnHeldMinWarpsF32) {
+                ring = true;
+                ro.vec_per_thread = 8;
+            }
+        }
+        if (ring) rc = plan_ring(dtype, vec, M, N, units, ro, *dev, p, nparams);
         if (rc == RS_OK) return RS_OK;
         if (rc != RS_ERR_NO_PATH) return rc;
         const int64_t rows_max = dtype == RS_F32 && !norm ? kRowsMaxRowBytesF32

@@ -173,20 +173,24 @@ cudaError_t read_status_causal_bf16(unsigned int* flags, bool clear);
 // Which LayerNorm row operation serves a planned shape on the register rows or
 // the ring: 1 = OpLayerNormWarp (rows inside one warp), 2 = OpLayerNormWhole
 // (vectorised rows that fill their threads exactly over a power-of-two number
-// of warps), 3 = OpLayerNormWholeHeld (kind 2 on the ring with at most 4 units
-// a thread and kHeldThreads threads a CTA: the weight and bias held in
-// registers, kHeldRegs a thread), 0 = OpLayerNorm (the others, and the other
-// paths).
+// of warps), 3 = OpLayerNormWholeHeld (kind 2 on the ring with at most 32
+// values a thread and kHeldThreads threads a CTA: the weight and bias held in
+// registers, kHeldRegs a thread), 4 = OpLayerNormHeld (other fp32 rows of
+// 2 to 8 warps on the ring at 8 units a thread, weight and bias held),
+// 0 = OpLayerNorm (the others, and the other paths).
 constexpr int kHeldThreads = 256;
 constexpr int kHeldRegs = 128;
 inline int layernorm_merge_kind(const rs_plan& p, int64_t N, int vec_full) {
     if (p.path != RS_PATH_ROWS && p.path != RS_PATH_RING) return 0;
     const int tpr = p.threads_per_row;
     if (tpr <= 32) return 1;
+    const bool ring_held = p.path == RS_PATH_RING && p.vec_elems == vec_full &&
+                           p.vec_per_thread * p.vec_elems <= 32 && p.block_threads <= kHeldThreads;
     const int wpr = tpr / 32;
     if (p.vec_elems == vec_full && (wpr & (wpr - 1)) == 0 &&
         N == (int64_t)tpr * p.vec_per_thread * p.vec_elems)
-        return p.path == RS_PATH_RING && p.vec_per_thread <= 4 && p.block_threads <= kHeldThreads ? 3 : 2;
+        return ring_held ? 3 : 2;
+    if (ring_held && vec_full == 4 && p.vec_per_thread == 8) return 4;
     return 0;
 }
 // RMSNorm on the ring with the weight held in registers (OpRmsNormHeld): rows

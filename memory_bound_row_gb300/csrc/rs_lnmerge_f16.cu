@@ -2,9 +2,9 @@
 // fp16 storage, on the register rows and the ring: OpLayerNormWarp for rows
 // inside one warp, OpLayerNormWhole for vectorised rows that fill their
 // threads exactly over a power-of-two number of warps (on the ring with at most
-// 4 units a thread: OpLayerNormWholeHeld, weight and bias in registers).  The
-// other shapes take
-// OpLayerNorm (rs_norm_f16.cu).
+// 32 values a thread: OpLayerNormWholeHeld, weight and bias in registers;
+// other fp32 ring rows at 8 units a thread: OpLayerNormHeld).  The other
+// shapes take OpLayerNorm (rs_norm_f16.cu).
 #include "rs_ring.cuh"
 #include "rs_rows.cuh"
 

@@ -2,9 +2,9 @@
 // fp32 storage, on the register rows and the ring: OpLayerNormWarp for rows
 // inside one warp, OpLayerNormWhole for vectorised rows that fill their
 // threads exactly over a power-of-two number of warps (on the ring with at most
-// 4 units a thread: OpLayerNormWholeHeld, weight and bias in registers).  The
-// other shapes take
-// OpLayerNorm (rs_norm_f32.cu).
+// 32 values a thread: OpLayerNormWholeHeld, weight and bias in registers;
+// other fp32 ring rows at 8 units a thread: OpLayerNormHeld).  The other
+// shapes take OpLayerNorm (rs_norm_f32.cu).
 #include "rs_ring.cuh"
 #include "rs_rows.cuh"
 
@@ -26,7 +26,8 @@ cudaError_t launch_lnmerge_f32(const rs_plan& p, const void* in, void* out, int6
         return cudaErrorInvalidConfiguration;
     }
     if (kind == 3)
-        return RingDispatch<RS_F32, OpLayerNormWholeHeld, 1, 2, 3, 4>::go(p, in, out, M, N, ldi, ldo, s, a);
+        return RingDispatch<RS_F32, OpLayerNormWholeHeld, RS_VPT_NORM_VEC>::go(p, in, out, M, N, ldi, ldo, s, a);
+    if (kind == 4) return RingDispatch<RS_F32, OpLayerNormHeld, 8>::go(p, in, out, M, N, ldi, ldo, s, a);
     if (kind == 2) {
         if (p.path == RS_PATH_RING)
             return RingDispatch<RS_F32, OpLayerNormWhole, RS_VPT_NORM_VEC>::go(p, in, out, M, N, ldi, ldo, s, a);

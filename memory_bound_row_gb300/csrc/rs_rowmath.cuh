@@ -348,8 +348,8 @@ struct OpLayerNorm {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             float w[VEC], b[VEC];
-            a.template w_unit<DT, VEC>((t + k * tpr) * VEC, w);
-            a.template b_unit<DT, VEC>((t + k * tpr) * VEC, b);
+            a.template w_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, w);
+            a.template b_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, b);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
         }
@@ -494,6 +494,11 @@ struct OpLayerNormWhole {
         q = __shfl_sync(0xffffffffu, qj, 0);
         layernorm_out<DT, VEC, VPT>(v, t, tpr, n, s, q, a);
     }
+};
+
+// OpLayerNorm reading its weight and bias from registers (HeldParams).
+struct OpLayerNormHeld : OpLayerNorm {
+    static constexpr bool kHeldParams = true;
 };
 
 // OpRmsNorm reading its weight from registers (HeldParams).

@@ -98,8 +98,9 @@ def test_plans_for_typical_hidden_sizes():
         p = _plan(op, 32768, 8192, rs.RS_BF16)
         assert p["path"] == rs.RS_PATH_RING and p["ring_values"] == rs.RS_RING_REGISTERS and _covers(p, 8192)
         assert p["vec_per_thread"] in NORM_VPT_VEC
-        p = _plan(op, 8192, 5000, rs.RS_F32, ld=5120)   # fp32: register rows
-        assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 4 and _covers(p, 5000)
+        p = _plan(op, 8192, 5000, rs.RS_F32, ld=5120)   # fp32: register rows (LayerNorm: the held ring)
+        assert p["path"] == (rs.RS_PATH_ROWS if op == rs.RS_OP_RMSNORM else rs.RS_PATH_RING)
+        assert p["vec_elems"] == 4 and _covers(p, 5000)
         p = _plan(op, 512, 131072, rs.RS_F16)          # wide rows: a cluster per row, slices in registers
         assert p["path"] == rs.RS_PATH_CLUSTER and p["ring_values"] == rs.RS_RING_REGISTERS
         assert p["cluster_size"] >= 2 and p["grid"] % p["cluster_size"] == 0 and _covers(p, 131072)
@@ -148,6 +149,22 @@ def test_layernorm_rows_of_4_or_8_warps_hold_their_vectors_in_registers(dtype):
     assert p["threads_per_row"] == 384 and p["grid"] == 2 * 152  # 64 registers, 384 threads: 2 CTAs by threads
     p = _plan(rs.RS_OP_LAYERNORM, 32768, 8184, dtype, ld=8192, b=B)
     assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] != 4
+
+
+def test_ragged_fp32_layernorm_rows_of_4_to_8_warps_take_the_held_ring():
+    # fp32 LayerNorm rows that would take two reductions on the register rows
+    # and span 4-8 warps at 8 units a thread go to the ring with weight and
+    # bias in registers, where at least 14 warps of it fit an SM; filled rows,
+    # rows of 2-3 warps and 192-thread rows (2 CTAs, 12 warps an SM) stay.
+    for N, tpr, grid in [(4100, 160, 3 * 152), (5000, 160, 3 * 152), (7000, 224, 2 * 152)]:
+        ld = -(-N // 4) * 4
+        p = _plan(rs.RS_OP_LAYERNORM, 8192, N, rs.RS_F32, ld=ld, b=B)
+        assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] == 8 and p["threads_per_row"] == tpr, N
+        assert p["block_threads"] == tpr and p["grid"] == grid
+        assert p["smem_bytes"] == (N // 4) * 16 * p["stages"]  # no staged vectors
+    for N in (2048, 3000, 4096, 6000, 8192):
+        assert _plan(rs.RS_OP_LAYERNORM, 8192, N, rs.RS_F32, b=B)["path"] == rs.RS_PATH_ROWS, N
+    assert _plan(rs.RS_OP_RMSNORM, 8192, 5000, rs.RS_F32, ld=5120)["path"] == rs.RS_PATH_ROWS
 
 
 def test_wide_16bit_rows_take_the_ring_where_it_fits():
