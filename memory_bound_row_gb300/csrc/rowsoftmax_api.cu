@@ -32,7 +32,7 @@ constexpr int64_t kMaxMaskOffset = (int64_t)1 << 62;  // keeps (r mod P) + 1 + o
 
 // Auto-planner knobs.
 constexpr int kRowsTargetValues = 32;             // fp32 values a thread holds (auto)
-constexpr int kRowsTargetValuesLn16 = 64;         // ... for LayerNorm on 16-bit rows (measured faster)
+constexpr int kRowsTargetValuesLn16 = 64;         // ... for LayerNorm on 16-bit rows up to 8192 values (measured faster)
 constexpr int kRowsMaxSingleWarpValues = 64;      // ... up to this many when it keeps a row in one warp
 constexpr int64_t kRowsMaxRowBytes = 32 * 1024;   // auto: rows up to this go to RS_PATH_ROWS
 constexpr int64_t kRowsMaxRowBytesF32 = 64 * 1024;  // ... fp32 softmax rows (measured: rows beat clusters to 64 KB)
@@ -188,7 +188,8 @@ int64_t ctas_per_sm(const rs_device_info& dev, int block, size_t smem, int regs_
 }
 
 // RS_PATH_RING.  `nparams` parameter vectors (LayerNorm's weight and bias)
-// are staged in shared memory after the stages, padded to whole units.
+// are staged in shared memory after the stages, padded to whole units, unless
+// the plan takes a held-parameter instance (vectors in registers).
 int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_options& o,
               const rs_device_info& dev, rs_plan* p, int nparams = 0) {
     if (vec == 1) return RS_ERR_NO_PATH;  // bulk copies need 16-byte units

@@ -116,11 +116,14 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
             if (g < groups) issue(s, g);
         }
     }
-    // LayerNorm: the weight and bias vectors are staged once per CTA in shared
+    // Where the normalisations read their vectors.  Held instances
+    // (OP::kHeldParams): each thread keeps the weight and bias of its units as
+    // fp32 in registers for the whole loop (it serves the same columns of every
+    // row).  Otherwise LayerNorm stages both vectors once per CTA in shared
     // memory after the ring stages (every row of the CTA reads them; measured
-    // 33 % faster on 2048-value bf16 rows).  RMSNorm reads its one vector
-    // through the read-only cache: staging it cost more in resident CTAs than
-    // it saved.
+    // 33 % faster on 2048-value bf16 rows than the read-only cache), and
+    // RMSNorm reads its one vector through the read-only cache (staging it cost
+    // more in resident CTAs than it saved).
     constexpr bool kHeld = OP::kHeldParams;
     constexpr bool kStage = OP::kOp == RS_OP_LAYERNORM && !kHeld;
     using Params = typename std::conditional<

@@ -181,7 +181,8 @@ __device__ __forceinline__ float thread_sum(const float (&v)[VPT][VEC], F f) {
 // caller's vectors in global memory (read-only cache), with 1 and 0 for a
 // null vector or past n.  SharedParams: copies staged once per CTA in shared
 // memory by a persistent kernel, padded to whole 16-byte units with 1 and 0,
-// read at unit offsets relative to the staged range.
+// read at unit offsets relative to the staged range.  HeldParams (below): a
+// thread's own units in registers, read by unit index.
 struct GlobalParams {
     const void* w;
     const void* b;
