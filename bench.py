@@ -405,12 +405,18 @@ def run_ours(args, workloads):
         torch.cuda.synchronize()
         if sampler:
             sampler.mark_start()
+        # One event between replays as well: the median over the replays is
+        # reported beside the whole region's figure (the events add no work).
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
         with torch.cuda.stream(graph_stream):  # replay() launches on the current stream
             e_start.record(graph_stream)
-            for _ in range(replays):
+            marks[0].record(graph_stream)
+            for i in range(replays):
                 graph.replay()
+                marks[i + 1].record(graph_stream)
             e_end.record(graph_stream)
         torch.cuda.synchronize()
+        per_replay = sorted(marks[i].elapsed_time(marks[i + 1]) / G for i in range(replays))
         if sampler:
             sampler.mark_end()
         if world > 1:
@@ -573,7 +579,12 @@ def run_ours(args, workloads):
                                "min_bytes_gbs": round(job_gbs(world, min_bytes, args.steps, total_ms), 2),
                                "how": "rowsoftmax_causal_fwd: row r keeps (r mod N) + 1 elements, the masked part "
                                       "is not used and is written as 0"}} if args.causal else {}),
-                "timing": f"{args.steps // G} replays of a CUDA graph of {G} launches, one event pair",
+                "timing": f"{args.steps // G} replays of a CUDA graph of {G} launches; one event pair around "
+                          "all of them (value, ms_per_step) and one between consecutive replays (repeats)",
+                "repeats": {"n": replays, "launches_each": G,
+                            "median_ms_per_step": round(per_replay[len(per_replay) // 2], 5),
+                            "min_ms_per_step": round(per_replay[0], 5),
+                            "max_ms_per_step": round(per_replay[-1], 5)},
                 "clocks": clocks,
             }
             if not args.no_cpu_baseline:
