@@ -267,3 +267,46 @@ def test_layout_owner_is_a_bijection():
         assert t == (j // vec) % threads
     assert len(seen) == n
     assert rs.rowsoftmax_layout_owner(-1, 2, 2)[0] == rs.RS_ERR_INVALID_ARG
+
+
+def _c_layout(struct: str, fields):
+    """sizeof and offsetof of a struct of include/rowsoftmax.h, from a small C
+    program compiled against the header (None when no C compiler or CUDA
+    headers are at hand)."""
+    import os
+    import shutil
+    import subprocess
+    import tempfile
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = next((d for d in ("/usr/local/cuda/include", os.path.join(os.environ.get("CUDA_HOME", "/nonexistent"),
+                                                                             "include"))
+                     if os.path.exists(os.path.join(d, "cuda_runtime_api.h"))), None)
+    if not cc or not cuda_inc:
+        return None
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    prints = "".join(f'    printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields)
+    src = (f'#include <stddef.h>\n#include <stdio.h>\n#include "rowsoftmax.h"\nint main(void) {{\n'
+           f'    printf("%zu\\n", sizeof({struct}));\n{prints}    return 0;\n}}\n')
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        with open(c, "w") as fh:
+            fh.write(src)
+        r = subprocess.run([cc, "-std=c11", "-I", os.path.join(root, "include"), "-I", cuda_inc, c, "-o", exe],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+        vals = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    return vals[0], vals[1:]
+
+
+@pytest.mark.parametrize("cls", [rs.rs_options, rs.rs_plan, rs.rs_device_info])
+def test_ctypes_structs_match_the_c_header(cls):
+    # The binding's structs have the C header's size and every field's offset.
+    fields = [name for name, _ in cls._fields_]
+    got = _c_layout(cls.__name__, fields)
+    if got is None:
+        pytest.skip("no C compiler or CUDA headers")
+    size, offsets = got
+    assert ctypes.sizeof(cls) == size
+    assert [getattr(cls, f).offset for f in fields] == offsets
