@@ -6,8 +6,11 @@
 One step is one rowsoftmax_fwd call (the whole hot path: load, max, exp,
 sum, normalise, store) over one batch of the workload.  With --op rmsnorm or
 layernorm a step is one rmsnorm_fwd / layernorm_fwd call (with weight, and
-bias for LayerNorm) on the same shapes.  The default workload
-is fp32 8192 x 5000 with row stride 5120.  Rank 0 prints one JSON line per
+bias for LayerNorm) on the same shapes.  The default workload is the largest
+one, bf16 attention scores [16, 32, 2048, 2048] as 1048576 x 2048 rows
+(8.59 GB moved per step), timed with the plain rowsoftmax_fwd; the line also
+carries, under "all_configs", the device-timed figures of the other four
+workloads from the same run.  Rank 0 prints one JSON line per
 workload with achieved HBM GB/s (bytes = M * N * (in + out element size)),
 rows/s, the roofline fraction of the kernel against the measured HBM copy
 bandwidth, the end-to-end figure through the C ABI with host buffers, the
@@ -36,7 +39,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "fp32_8192x5000_ld5120"
+DEFAULT_WORKLOAD = "bf16_causal_16x32x2048"
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "memory_bound_row_gb300", "csrc")
@@ -322,7 +325,26 @@ def cpu_baseline(w, x_dev, op: str = "softmax", seconds: float = 3.0) -> dict:
                               "sample": f"first {rows1} rows x {passes1} passes, {dt1 * passes1:.1f} s on 1 thread"}}
 
 
-def run_ours(args, workloads):
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e bandwidth as specified (nominal, not measured)
+
+
+def pick_graph_launches(steps: int, nsets: int, est_ms: float) -> int:
+    """Launches per CUDA graph: the largest divisor of `steps` (at most 64)
+    whose replay holds about a millisecond of work or less, so that long
+    kernels get several replays for the per-replay median while short ones
+    are not stretched by host launch cost; a multiple of the rotating buffer
+    sets where one qualifies."""
+    divisors = [g for g in range(1, min(64, steps) + 1) if steps % g == 0]
+    fit = [g for g in divisors if g == 1 or g * est_ms <= 1.0]
+    pref = [g for g in fit if g % nsets == 0]
+    return max(pref or fit)
+
+
+def measure(args, name, ctx, full: bool):
+    """Times K graph-replayed launches of the row operation on workload
+    `name`.  Returns the JSON line (rank 0; None elsewhere).  With full=False
+    only the device-timed figures are taken (no end-to-end leg, clocks or CPU
+    baseline): the compact per-workload summary of the headline line."""
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -330,151 +352,156 @@ def run_ours(args, workloads):
     import memory_bound_row_gb300 as rs
     from memory_bound_row_gb300 import workloads as W
 
-    world, rank, local = dist_setup()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-    lib = rs._abi.load()
-    peak, peak_src = measured_peaks()
-
-    opts = rs._abi._opts(args.options)
+    lib, dev, world, rank, local, peak, peak_src, opts = (ctx[k] for k in (
+        "lib", "dev", "world", "rank", "local", "peak", "peak_src", "opts"))
     op = args.op
-    for name in workloads:
-        w = op_workload(op, name)
-        if args.rows:
-            w = W.Workload(w.name, w.dtype, min(args.rows, w.M), w.N, w.ld, w.seed, w.kind,
-                           f"first {min(args.rows, w.M)} rows of: {w.description}")
-        code = {"f32": rs.RS_F32, "f16": rs.RS_F16, "bf16": rs.RS_BF16}[w.dtype]
-        set_bytes = 2 * w.M * w.ld * w.elem_size
-        nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
-        xs = [W.generate(w, dev) for _ in range(1)]
-        xs += [xs[0].clone() for _ in range(nsets - 1)]
-        ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
-        stream = torch.cuda.current_stream(dev)
-        s_handle = ctypes.c_void_p(stream.cuda_stream)
-        args_list = [(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr())) for x, y in zip(xs, ys)]
-        if op != "softmax":
-            wt, bs = W.norm_params(w.N, w.dtype, w.seed, dev)
-            p_w = ctypes.c_void_p(wt.data_ptr())
-            p_b = ctypes.c_void_p(bs.data_ptr()) if op == "layernorm" else None
+    causal = args.causal and full
+    w = op_workload(op, name)
+    if args.rows and full:
+        w = W.Workload(w.name, w.dtype, min(args.rows, w.M), w.N, w.ld, w.seed, w.kind,
+                       f"first {min(args.rows, w.M)} rows of: {w.description}")
+    code = {"f32": rs.RS_F32, "f16": rs.RS_F16, "bf16": rs.RS_BF16}[w.dtype]
+    set_bytes = 2 * w.M * w.ld * w.elem_size
+    nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
+    xs = [W.generate(w, dev) for _ in range(1)]
+    xs += [xs[0].clone() for _ in range(nsets - 1)]
+    ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+    stream = torch.cuda.current_stream(dev)
+    s_handle = ctypes.c_void_p(stream.cuda_stream)
+    args_list = [(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr())) for x, y in zip(xs, ys)]
+    wt = bs = None
+    if op != "softmax":
+        wt, bs = W.norm_params(w.N, w.dtype, w.seed, dev)
+        p_w = ctypes.c_void_p(wt.data_ptr())
+        p_b = ctypes.c_void_p(bs.data_ptr()) if op == "layernorm" else None
 
-        def call(a, b, st):
-            if op == "softmax" and args.causal:
-                return lib.rowsoftmax_causal_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, w.N, 0, code, st, opts)
-            if op == "softmax":
-                return lib.rowsoftmax_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, code, st, opts)
-            return lib.rownorm_fwd_ex(OP_CODES[op], a, b, p_w, p_b, w.M, w.N, w.ld, w.ld, OP_EPS[op], code, st,
-                                      opts)
+    def call(a, b, st):
+        if op == "softmax" and causal:
+            return lib.rowsoftmax_causal_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, w.N, 0, code, st, opts)
+        if op == "softmax":
+            return lib.rowsoftmax_fwd_ex(a, b, w.M, w.N, w.ld, w.ld, code, st, opts)
+        return lib.rownorm_fwd_ex(OP_CODES[op], a, b, p_w, p_b, w.M, w.N, w.ld, w.ld, OP_EPS[op], code, st, opts)
 
-        def step(i, st=None):
-            a, b = args_list[i % nsets]
-            rc = call(a, b, st if st is not None else s_handle)
-            if rc != rs.RS_OK:
-                raise rs.RowSoftmaxError(rc, rs.rowsoftmax_last_cuda_error())
+    def step(i, st=None):
+        a, b = args_list[i % nsets]
+        rc = call(a, b, st if st is not None else s_handle)
+        if rc != rs.RS_OK:
+            raise rs.RowSoftmaxError(rc, rs.rowsoftmax_last_cuda_error())
 
-        for i in range(max(3, args.warmup)):
-            step(i)
-        torch.cuda.synchronize()
+    # Warm-up launches, launched directly; their average (an upper bound of
+    # the kernel's time) sizes the graphs below.
+    warm = max(3, args.warmup)
+    step(0)
+    torch.cuda.synchronize()
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for i in range(1, warm):
+        step(i)
+    w1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = w0.elapsed_time(w1) / max(1, warm - 1)
 
-        # The K timed steps are replayed from a CUDA graph of G consecutive
-        # launches (G the largest divisor of K up to 64), so host launch cost
-        # does not stretch short kernels; one event pair brackets all K.
-        divisors = [g for g in range(1, min(64, args.steps) + 1) if args.steps % g == 0]
-        G = max([g for g in divisors if g % nsets == 0] or divisors)
-        reuse_mb = min(G, nsets) * set_bytes / 1e6  # bytes of other sets between two uses of one set
-        graph_stream = torch.cuda.Stream(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(graph_stream):
-            g_handle = ctypes.c_void_p(graph_stream.cuda_stream)
-            for i in range(G):  # same buffers as the capture, outside it
+    # The K timed steps are replayed from a CUDA graph of G consecutive
+    # launches (pick_graph_launches), so host launch cost does not stretch
+    # short kernels; the graph is replayed once untimed before the events
+    # (its first replay carries the upload), then K / G times inside them.
+    G = pick_graph_launches(args.steps, nsets, est_ms)
+    reuse_mb = min(G, nsets) * set_bytes / 1e6  # bytes of other sets between two uses of one set
+    graph_stream = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(graph_stream):
+        g_handle = ctypes.c_void_p(graph_stream.cuda_stream)
+        for i in range(G):  # same buffers as the capture, outside it
+            step(i, g_handle)
+        graph_stream.synchronize()
+        with torch.cuda.graph(graph, stream=graph_stream, capture_error_mode="relaxed"):
+            for i in range(G):
                 step(i, g_handle)
-            graph_stream.synchronize()
-            with torch.cuda.graph(graph, stream=graph_stream, capture_error_mode="relaxed"):
-                for i in range(G):
-                    step(i, g_handle)
-        torch.cuda.synchronize()
-        replays = args.steps // G
-        # rotating sets stay ahead of L2: consecutive replays reuse set i % nsets
-        e_start = torch.cuda.Event(enable_timing=True)
-        e_end = torch.cuda.Event(enable_timing=True)
-        sampler = ClockSampler(local) if rank == 0 else None
-        time.sleep(0.3 if sampler else 0)
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        if sampler:
-            sampler.mark_start()
-        # One event between replays as well: the median over the replays is
-        # reported beside the whole region's figure (the events add no work).
-        marks = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
-        with torch.cuda.stream(graph_stream):  # replay() launches on the current stream
-            e_start.record(graph_stream)
-            marks[0].record(graph_stream)
-            for i in range(replays):
-                graph.replay()
-                marks[i + 1].record(graph_stream)
-            e_end.record(graph_stream)
-        torch.cuda.synchronize()
-        per_replay = sorted(marks[i].elapsed_time(marks[i + 1]) / G for i in range(replays))
-        if sampler:
-            sampler.mark_end()
-        if world > 1:
-            dist.barrier()
-        total_ms = e_start.elapsed_time(e_end)
-        # Every step is exactly one launch of the library's kernel, back to
-        # back on graph_stream: the average launch duration is total / K.
-        kern_ms = total_ms / args.steps
-        total_ms = max_over_ranks(total_ms, dev)
-        clocks = sampler.finish() if sampler else None
+        graph.replay()  # untimed: the first replay of a fresh graph
+    torch.cuda.synchronize()
+    replays = args.steps // G
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if (rank == 0 and full) else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    # One event between replays as well: the median over the replays is
+    # reported beside the whole region's figure (the events add no work).
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+    with torch.cuda.stream(graph_stream):  # replay() launches on the current stream
+        e_start.record(graph_stream)
+        marks[0].record(graph_stream)
+        for i in range(replays):
+            graph.replay()
+            marks[i + 1].record(graph_stream)
+        e_end.record(graph_stream)
+    torch.cuda.synchronize()
+    per_replay = sorted(marks[i].elapsed_time(marks[i + 1]) / G for i in range(replays))
+    if sampler:
+        sampler.mark_end()
+    if world > 1:
+        dist.barrier()
+    total_ms = e_start.elapsed_time(e_end)
+    # Every step is exactly one launch of the library's kernel, back to back
+    # on graph_stream: the average launch duration is total / K.
+    kern_ms = total_ms / args.steps
+    total_ms = max_over_ranks(total_ms, dev)
+    clocks = sampler.finish() if sampler else None
 
-        # Context for the roofline: a plain device-to-device copy of the same
-        # buffer sets (torch copy_, whole buffers, padding included), timed
-        # over K steps on the same box right after the kernel, both replayed
-        # from a CUDA graph as the kernel is and launched directly as the
-        # measured peak was; the faster counts.  (Each way has sizes where it
-        # measured far below the other: graph-captured copies of 512 MB and
-        # more at half the bandwidth, direct launches of ~50 us copies about
-        # 5 % low.)
-        def time_copies(use_graph):
-            if use_graph:
-                cg = torch.cuda.CUDAGraph()
-                with torch.cuda.stream(graph_stream):
+    # Context for the roofline: a plain device-to-device copy of the same
+    # buffer sets (torch copy_, whole buffers, padding included), timed over
+    # K steps on the same box right after the kernel, both replayed from a
+    # CUDA graph as the kernel is and launched directly as the measured peak
+    # was; the faster counts.  (Each way has sizes where it measured far below
+    # the other: graph-captured copies of 512 MB and more at half the
+    # bandwidth, direct launches of ~50 us copies about 5 % low.)
+    def time_copies(use_graph):
+        if use_graph:
+            cg = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(graph_stream):
+                for i in range(G):
+                    ys[i % nsets].copy_(xs[i % nsets])
+                graph_stream.synchronize()
+                with torch.cuda.graph(cg, stream=graph_stream, capture_error_mode="relaxed"):
                     for i in range(G):
                         ys[i % nsets].copy_(xs[i % nsets])
-                    graph_stream.synchronize()
-                    with torch.cuda.graph(cg, stream=graph_stream, capture_error_mode="relaxed"):
-                        for i in range(G):
-                            ys[i % nsets].copy_(xs[i % nsets])
-            else:
-                with torch.cuda.stream(graph_stream):
-                    for i in range(3):
-                        ys[i % nsets].copy_(xs[i % nsets])
-            torch.cuda.synchronize()
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
+                cg.replay()
+        else:
             with torch.cuda.stream(graph_stream):
-                c0.record(graph_stream)
-                if use_graph:
-                    for _ in range(replays):
-                        cg.replay()
-                else:
-                    for i in range(args.steps):
-                        ys[i % nsets].copy_(xs[i % nsets])
-                c1.record(graph_stream)
-            torch.cuda.synchronize()
-            return (set_bytes * args.steps) / (c0.elapsed_time(c1) * 1e-3) / 1e9
+                for i in range(3):
+                    ys[i % nsets].copy_(xs[i % nsets])
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(graph_stream):
+            c0.record(graph_stream)
+            if use_graph:
+                for _ in range(replays):
+                    cg.replay()
+            else:
+                for i in range(args.steps):
+                    ys[i % nsets].copy_(xs[i % nsets])
+            c1.record(graph_stream)
+        torch.cuda.synchronize()
+        return (set_bytes * args.steps) / (c0.elapsed_time(c1) * 1e-3) / 1e9
 
-        copy_gbs = max(time_copies(True), time_copies(False))
+    copy_gbs = max(time_copies(True), time_copies(False))
 
-        ms_per_step = total_ms / args.steps
-        nbytes = op_bytes(op, w)
-        if args.causal:  # the least traffic the mask allows: kept elements read, every element written
-            kept = int(np.minimum(np.arange(w.M, dtype=np.int64) % w.N + 1, w.N).sum())
-            min_bytes = (kept + w.M * w.N) * w.elem_size
-        value = job_gbs(world, nbytes, args.steps, total_ms)
-        achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    ms_per_step = total_ms / args.steps
+    nbytes = op_bytes(op, w)
+    if causal:  # the least traffic the mask allows: kept elements read, every element written
+        kept = int(np.minimum(np.arange(w.M, dtype=np.int64) % w.N + 1, w.N).sum())
+        min_bytes = (kept + w.M * w.N) * w.elem_size
+    value = job_gbs(world, nbytes, args.steps, total_ms)
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
 
+    e2e = None
+    if full:
         # End to end through the C ABI with host buffers: every step copies
         # its input in from pinned host memory, runs the call and copies the
         # output back.  Two device buffer pairs let step i+1's copy-in overlap
@@ -524,23 +551,44 @@ def run_ours(args, workloads):
         e1.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+        e2e = {"value": round(job_gbs(world, nbytes, 1, e2e_ms), 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
+               "d2h_bytes_per_step": h_out[0].numel() * h_out[0].element_size(),
+               "ms_per_step": round(e2e_ms, 4),
+               "how": f"pinned host input copied in, "
+                      f"{('rowsoftmax_causal_fwd' if causal else 'rowsoftmax_fwd') if op == 'softmax' else op + '_fwd'}, "
+                      "output copied back, every step; two buffer pairs overlap step i+1's copy-in with step i"}
+        del h_in, h_out, d_in, d_out
 
-        rc, flags = rs.rowsoftmax_device_status()
-        if rc != rs.RS_OK or flags:
-            raise RuntimeError(f"device status word {flags:#x} after the run")
+    rc, flags = rs.rowsoftmax_device_status()
+    if rc != rs.RS_OK or flags:
+        raise RuntimeError(f"device status word {flags:#x} after the run")
 
-        if rank == 0:
-            rc, info = rs.rowsoftmax_device_info()
-            if op == "softmax" and args.causal:
-                rc, plan = rs.rowsoftmax_causal_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, w.N,
-                                                     0, code, args.options, info)
-            elif op == "softmax":
-                rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code,
-                                              args.options, info)
-            else:
-                rc, plan = rs.rownorm_plan(OP_CODES[op], xs[0].data_ptr(), ys[0].data_ptr(), wt.data_ptr(),
-                                           bs.data_ptr() if op == "layernorm" else None, w.M, w.N, w.ld, w.ld,
-                                           OP_EPS[op], code, args.options, info)
+    line = None
+    if rank == 0:
+        rc, info = rs.rowsoftmax_device_info()
+        if op == "softmax" and causal:
+            rc, plan = rs.rowsoftmax_causal_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, w.N,
+                                                 0, code, args.options, info)
+        elif op == "softmax":
+            rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), w.M, w.N, w.ld, w.ld, code,
+                                          args.options, info)
+        else:
+            rc, plan = rs.rownorm_plan(OP_CODES[op], xs[0].data_ptr(), ys[0].data_ptr(), wt.data_ptr(),
+                                       bs.data_ptr() if op == "layernorm" else None, w.M, w.N, w.ld, w.ld,
+                                       OP_EPS[op], code, args.options, info)
+        repeats = {"n": replays, "launches_each": G,
+                   "median_ms_per_step": round(per_replay[len(per_replay) // 2], 5),
+                   "min_ms_per_step": round(per_replay[0], 5),
+                   "max_ms_per_step": round(per_replay[-1], 5)}
+        if not full:
+            line = {"workload": name, "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms_per_step, 5),
+                    "rows_per_s": round(world * w.M / (ms_per_step * 1e-3), 1), "frac": round(achieved / peak, 4),
+                    "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                    "frac_of_same_run_copy": round(achieved / copy_gbs, 4), "same_run_copy_gbs": round(copy_gbs, 1),
+                    "kernel": rs.PATH_NAMES[plan["path"]], "bytes_per_step": nbytes, "steps": args.steps,
+                    "repeats": repeats}
+        else:
             line = {
                 "metric": OP_METRIC[op], "value": round(value, 2), "unit": "GB/s",
                 "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
@@ -548,6 +596,7 @@ def run_ours(args, workloads):
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "rows_per_s": round(world * w.M / (ms_per_step * 1e-3), 1),
                 "hbm_roofline_frac": round(value / world / peak, 4),
+                "hbm_nominal_frac": round(value / world / NOMINAL_HBM_GBS, 4),
                 "config": {"workload": name if not args.rows else f"{name} (first {w.M} rows)", "op": op,
                            "M": w.M, "N": w.N, "row_stride": w.ld, "storage": w.dtype,
                            "options": args.options,
@@ -556,45 +605,71 @@ def run_ours(args, workloads):
                                  f"{reuse_mb:.0f} MB pass between two uses of a set (L2 is 129 MB)",
                            "kernel": rs.PATH_NAMES[plan["path"]], "plan": plan},
                 "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(achieved / peak, 4), "traffic": None if (args.options or args.rows) else ncu_traffic(traffic_key(op, name, args.causal)),
+                             "frac": round(achieved / peak, 4),
+                             "traffic": None if (args.options or args.rows)
+                             else ncu_traffic(traffic_key(op, name, causal)),
                              "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
                              if peak_src == "measured" else "fallback 6.8 TB/s",
+                             "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                             "nominal_peak": NOMINAL_HBM_GBS,
+                             "nominal_source": "GB300 HBM3e bandwidth as specified, 7.9 TB/s (not measured)",
                              "kernel_ms": round(kern_ms, 5),
                              "same_run_copy_gbs": round(copy_gbs, 1),
                              "frac_of_same_run_copy": round(achieved / copy_gbs, 4),
                              "same_run_copy": "torch copy_ of the same rotating buffer sets (padding included), K "
                                               "steps timed right after, the faster of graph-replayed and "
                                               "directly launched"},
-                "e2e": {"value": round(job_gbs(world, nbytes, 1, e2e_ms), 2), "unit": "GB/s",
-                        "h2d_bytes_per_step": h_in.numel() * h_in.element_size(),
-                        "d2h_bytes_per_step": h_out[0].numel() * h_out[0].element_size(),
-                        "ms_per_step": round(e2e_ms, 4),
-                        "how": f"pinned host input copied in, {'rowsoftmax_fwd' if op == 'softmax' else op + '_fwd'}, "
-                               "output copied back, every step; "
-                               "two buffer pairs overlap step i+1's copy-in with step i"},
+                "e2e": e2e,
                 "gpu_launches": args.steps,
                 **({"causal": {"period": w.N, "diag_offset": 0,
                                "value_counts": "M x N x (in + out) bytes, as the plain softmax line",
                                "min_bytes_per_step": min_bytes,
                                "min_bytes_gbs": round(job_gbs(world, min_bytes, args.steps, total_ms), 2),
                                "how": "rowsoftmax_causal_fwd: row r keeps (r mod N) + 1 elements, the masked part "
-                                      "is not used and is written as 0"}} if args.causal else {}),
-                "timing": f"{args.steps // G} replays of a CUDA graph of {G} launches; one event pair around "
-                          "all of them (value, ms_per_step) and one between consecutive replays (repeats)",
-                "repeats": {"n": replays, "launches_each": G,
-                            "median_ms_per_step": round(per_replay[len(per_replay) // 2], 5),
-                            "min_ms_per_step": round(per_replay[0], 5),
-                            "max_ms_per_step": round(per_replay[-1], 5)},
+                                      "is not used and is written as 0"}} if causal else {}),
+                "timing": f"{replays} replays of a CUDA graph of {G} launches after one untimed replay; one event "
+                          "pair around all of them (value, ms_per_step) and one between consecutive replays "
+                          "(repeats)",
+                "repeats": repeats,
                 "clocks": clocks,
             }
             if not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_baseline(w, xs[0], op)
+    del xs, ys, graph
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_ours(args, workloads):
+    import torch
+    import torch.distributed as dist
+
+    import memory_bound_row_gb300 as rs
+    from memory_bound_row_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    peak, peak_src = measured_peaks()
+    ctx = {"lib": rs._abi.load(), "dev": dev, "world": world, "rank": rank, "local": local, "peak": peak,
+           "peak_src": peak_src, "opts": rs._abi._opts(args.options)}
+    for name in workloads:
+        # The other workloads first (device-timed only), so that the headline
+        # line carries every workload's figure from the same run.
+        others = []
+        if args.summary_all:
+            for other in W.ORDER:
+                if other != name:
+                    others.append(measure(args, other, ctx, full=False))
+        line = measure(args, name, ctx, full=True)
+        if rank == 0:
+            if others:
+                line["all_configs"] = others
             print(json.dumps(line), flush=True)
-        del xs, ys, h_in, h_out, d_in, d_out, graph
-        torch.cuda.empty_cache()
     if world > 1:
         dist.destroy_process_group()
-
 
 SWEEP_CONFIGS = {
     # name: rs_options (None: the planner's choice).  grid_limit -1 means "one
@@ -823,6 +898,9 @@ def main():
                     help="the row operation timed (softmax: the fused row softmax; rmsnorm, layernorm: the "
                          "normalisations on the same row engine)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-summary", action="store_true",
+                    help="leave out the device-timed figures of the other workloads (all_configs) that the default "
+                         "run adds to its line")
     ap.add_argument("--options", default=None,
                     help="JSON object of rs_options fields forcing a kernel configuration (tuning, profiling)")
     ap.add_argument("--rows", type=int, default=0,
@@ -843,6 +921,8 @@ def main():
         raise SystemExit("--causal applies to the softmax only")
     if args.warmup < 3:
         args.warmup = 3
+    args.summary_all = (args.workload == DEFAULT_WORKLOAD and not args.no_summary and not args.rows
+                        and not args.options and not args.causal)
     from memory_bound_row_gb300 import workloads as W
 
     names = W.ORDER if args.workload == "all" else [args.workload]

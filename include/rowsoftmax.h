@@ -123,11 +123,16 @@ typedef struct {
     int ring_values;      /* RS_PATH_RING: rs_ring_values */
     int force_scalar;     /* 1: element-wise accesses even when 16-byte vectors would be legal */
     int64_t grid_limit;   /* >0: cap on CTAs (rows loop inside the kernel); 0: one launch slot per row group */
-    int64_t wait_limit_us;  /* RS_PATH_RING: >0 bounds each mbarrier wait (default 4 s) */
-    int withhold_copies;  /* RS_PATH_RING, failure-path tests only: post the expected bytes of every
-                             stage but never issue the copies, so each wait runs out after
-                             wait_limit_us, bit 0 of the device status word is set and the output
-                             is left unwritten; no fault, trap or unbounded wait is involved */
+    int64_t wait_limit_us;  /* RS_PATH_RING and the register-holding RS_PATH_CLUSTER kernel: >0 bounds
+                               each wait for a bulk copy (default 4 s; the cluster's waits for its
+                               peers' pairs take three times this limit) */
+    int withhold_copies;  /* RS_PATH_RING or RS_PATH_CLUSTER (register-holding), failure-path tests
+                             only: post the expected bytes of every stage or slot but never issue
+                             the copies, so each copy wait runs out after wait_limit_us (which must be
+                             set, at most 1 s), bit 0 of the device status word is set and the rows
+                             whose waits ran out are left unwritten (the ring's other rows of the
+                             same iteration may be partly written); no fault, trap or unbounded wait
+                             is involved.  A plan on another kernel returns RS_ERR_NO_PATH */
     int strict_order;     /* 1: launch without programmatic dependent launch (see "Execution") */
 } rs_options;
 
@@ -300,7 +305,8 @@ RS_API int rowsoftmax_last_cuda_error(void);
  * Device-side status word of the current device.  The ring and cluster
  * kernels bound every wait on an mbarrier; a wait that runs out sets bit 0
  * and its CTA abandons the rows it was serving: the output of a call that
- * reported a timeout is undefined in those rows.  Reads the word
+ * reported a timeout is undefined (unwritten, or partly written) in those
+ * rows, and in the ring's other rows of the same row group.  Reads the word
  * (synchronously, with cudaMemcpyFromSymbol) into *flags and clears it when
  * `clear` is nonzero.  Returns RS_OK or RS_ERR_CUDA.
  */

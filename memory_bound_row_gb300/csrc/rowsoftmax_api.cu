@@ -318,6 +318,7 @@ int plan_wide(int dtype, int path, int vec, int64_t M, int64_t N, const rs_optio
         const int rc = plan_cluster_hold(dtype, vec, M, N, o, dev, p);
         if (rc == RS_OK || o.ring_values == RS_RING_REGISTERS) return rc;
     }
+    if (o.withhold_copies) return RS_ERR_NO_PATH;  // only the register-holding clusters implement it
     if (o.ring_values < RS_RING_AUTO || o.ring_values > RS_RING_REREAD) return RS_ERR_INVALID_ARG;
     const int es = elem_size(dtype);
     const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kWideStaticSmem;
@@ -424,8 +425,10 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         o.wait_limit_us < 0 || o.withhold_copies < 0 || o.withhold_copies > 1 || o.strict_order < 0 ||
         o.strict_order > 1)
         return RS_ERR_INVALID_ARG;
-    // Withholding copies is only defined for the ring, and needs a short wait limit.
-    if (o.withhold_copies && (o.path != RS_PATH_RING || o.wait_limit_us <= 0 || o.wait_limit_us > 1000000))
+    // Withholding copies is only defined for the ring and the register-holding
+    // clusters, and needs a short wait limit.
+    if (o.withhold_copies && ((o.path != RS_PATH_RING && o.path != RS_PATH_CLUSTER) || o.wait_limit_us <= 0 ||
+                              o.wait_limit_us > 1000000))
         return RS_ERR_INVALID_ARG;
     p->wait_limit_us = o.wait_limit_us;
     p->withhold_copies = o.withhold_copies;

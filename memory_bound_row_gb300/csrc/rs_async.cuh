@@ -128,11 +128,12 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t pa
     return true;
 }
 
-static __device__ __noinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                              uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait_cluster(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

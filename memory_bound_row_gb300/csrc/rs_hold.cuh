@@ -32,9 +32,16 @@
 //              means, merged over warps and then over the CTA's warps (one
 //              CTA barrier a row).
 //
-// Waits are bounded by %globaltimer (a wait that runs out sets bit 0 of the
-// device status word, the CTA stops issuing copies, waits a second bounded
-// time for its copies in flight and leaves its rows unwritten).
+// Waits are bounded by %globaltimer.  A copy wait that runs out sets bit 0 of
+// the device status word; the CTA stops issuing copies and storing rows but
+// keeps taking part in the exchange (it still pushes a pair per row and waits
+// for its peers' pairs, under a limit three times the copy wait's, since a
+// peer may itself be waiting out a copy), so its peers' rows complete; at the
+// end it waits, bounded again, for its copies in flight.  A receive barrier is
+// re-armed only after the phase it armed has completed; if a receive wait
+// itself runs out (a peer stalled for longer than its own copy waits allow,
+// which bounded waits exclude), the CTA stops waiting on and re-arming its
+// receive barriers.  Rows of a call that reported a timeout are undefined.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -60,7 +67,7 @@ __device__ __forceinline__ int hold_slice_len(int rank, int chunk, int N) {
 template <int DT, int VPT, typename OP>
 __global__ void __launch_bounds__(VPT <= 4 ? kWideHoldThreads : kWideHoldThreads / 2, 2)
 wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t ldo, int chunk, int nslots,
-                 RowArgs args) {
+                 uint64_t wait_ns, int withhold, RowArgs args) {
     using T = Traits<DT>;
     using S = typename T::storage;
     constexpr int VEC = T::kVec;
@@ -76,6 +83,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
     __shared__ __align__(8) uint64_t recv_bar[2];  // all CTAs' pairs of a row received
     __shared__ __align__(8) float2 recv[2][kMaxCluster];
     __shared__ float2 warp_part[2][kWideHoldThreads / 32];
+    __shared__ int exchange_broken;  // a receive wait ran out: stop waiting on and re-arming recv_bar
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -113,6 +121,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             return;
         }
         mbar_arrive_expect_tx(&bars[slot], bytes);
+        if (withhold) return;  // failure-path test: the awaited bytes never come
         bulk_load(slots + (size_t)slot * slot_stride, in + row * ldi + c0, bytes, &bars[slot]);
     };
 
@@ -124,6 +133,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
         mbar_arrive_expect_tx(&recv_bar[0], pair_bytes);  // armed for rows 0 and 1 of this cluster
         mbar_arrive_expect_tx(&recv_bar[1], pair_bytes);
         fence_mbar_init();
+        exchange_broken = 0;
     }
     __syncthreads();
     wait_prior_grid();
@@ -143,7 +153,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
     for (int64_t row = cluster_id; row < M; row += n_clusters, ++it) {
         const int slot = (int)(it % nslots);
         const uint32_t parity = (uint32_t)((it / nslots) & 1);
-        if (!abort && !mbar_wait_bounded(&bars[slot], parity)) {
+        if (!abort && !mbar_wait_bounded(&bars[slot], parity, wait_ns)) {
             abort = true;
             flag_timeout();
         }
@@ -300,9 +310,16 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             const uint32_t dbar = map_to_rank(smem_addr(&recv_bar[rb]), (uint32_t)lane);
             st_async_pair(dst, pm, pl, dbar);
         }
-        if (!abort && !mbar_wait_cluster_bounded(&recv_bar[rb], (uint32_t)((it >> 1) & 1))) {
-            abort = true;
-            flag_timeout();
+        // Waited for even after an abort (the phase must complete before it is
+        // re-armed, and the peers' pairs must land before this CTA exits).
+        bool received = false;
+        if (!*reinterpret_cast<volatile int*>(&exchange_broken)) {
+            received = mbar_wait_cluster_bounded(&recv_bar[rb], (uint32_t)((it >> 1) & 1), 3 * wait_ns);
+            if (!received) {
+                *reinterpret_cast<volatile int*>(&exchange_broken) = 1;
+                abort = true;
+                flag_timeout();
+            }
         }
         float qa = kSoftmax ? kNegInf : 0.0f, qb = 0.0f;
         if (lane < cs) {
@@ -316,7 +333,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             qb = __shfl_sync(0xffffffffu, qb, 0);
             const float c = rescale_off(m, safe_offset(qa)) / qb;
             __syncwarp();
-            if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
+            if (tid == 0 && received) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
@@ -339,7 +356,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
                 nmr = -mean * r;
             }
             __syncwarp();
-            if (tid == 0) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
+            if (tid == 0 && received) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int base = (tid + k * tpr) * VEC;  // within the slice
@@ -361,7 +378,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
     if (abort && tid == 0 && abort_it >= 0) {
         for (int64_t j = abort_it; j < abort_it + nslots; ++j) {
             if (cluster_id + j * n_clusters >= M) break;
-            (void)mbar_wait_bounded(&bars[j % nslots], (uint32_t)((j / nslots) & 1));
+            (void)mbar_wait_bounded(&bars[j % nslots], (uint32_t)((j / nslots) & 1), wait_ns);
         }
     }
     cluster.sync();  // no CTA leaves while a peer's pair may still be in flight to it
@@ -399,8 +416,10 @@ cudaError_t launch_hold_one(const rs_plan& p, const void* in, void* out, int64_t
     if (err != cudaSuccess) return err;
     // Cluster grids are launched in strict stream order: with programmatic
     // dependent launch the persistent clusters measured about 10 % slower.
+    const uint64_t wait_ns = p.wait_limit_us > 0 ? (uint64_t)p.wait_limit_us * 1000ull : kWaitLimitNs;
     return launch_kernel(wide_hold_kernel<DT, VPT, OP>, (unsigned)p.grid, (unsigned)p.block_threads, p.smem_bytes,
-                         s, p.cluster_size, true, in, out, M, N, ldi, ldo, (int)p.chunk_elems, p.stages, a);
+                         s, p.cluster_size, true, in, out, M, N, ldi, ldo, (int)p.chunk_elems, p.stages, wait_ns,
+                         p.withhold_copies, a);
 }
 
 template <int DT, typename OP>

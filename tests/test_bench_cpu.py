@@ -77,3 +77,22 @@ def test_reference_arm_prints_one_json_line_with_the_contract_keys(op):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "fp32_1024x1024"
+
+
+def test_graph_size_gives_long_kernels_several_replays():
+    # K = 20 (the driver's run): a 1.4 ms launch is replayed alone 20 times,
+    # a 0.17 ms launch in graphs of 5, a 50 us launch in one graph of 20.
+    assert bench.pick_graph_launches(20, 1, 1.37) == 1
+    assert bench.pick_graph_launches(20, 1, 0.171) == 5
+    assert bench.pick_graph_launches(20, 2, 0.05) == 20
+    assert bench.pick_graph_launches(2000, 2, 0.003) == 50
+    # a multiple of the rotating buffer sets where one fits
+    assert bench.pick_graph_launches(24, 4, 0.05) == 12
+    for k in (1, 3, 7, 20, 400):
+        g = bench.pick_graph_launches(k, 3, 0.2)
+        assert k % g == 0 and 1 <= g <= 64
+
+
+def test_default_workload_is_the_largest():
+    sizes = {n: W.WORKLOADS[n].algorithmic_bytes for n in W.ORDER}
+    assert bench.DEFAULT_WORKLOAD == max(sizes, key=sizes.get) == "bf16_causal_16x32x2048"
