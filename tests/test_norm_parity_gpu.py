@@ -23,7 +23,7 @@ import memory_bound_row_gb300 as rs
 from memory_bound_row_gb300 import build
 from memory_bound_row_gb300 import workloads as W
 
-from _parity import compare_norm, oracle_norm_rows
+from _parity import check_all_rows, compare_norm, oracle_norm_rows
 
 pytestmark = pytest.mark.gpu
 
