@@ -66,6 +66,12 @@ def _load():
             lib.orc_rmsnorm_f64.restype = ctypes.c_int
             lib.orc_layernorm_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp, ctypes.c_double, vp, i64]
             lib.orc_layernorm_f64.restype = ctypes.c_int
+            lib.orc_softmax_partial_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp]
+            lib.orc_softmax_partial_f64.restype = ctypes.c_int
+            lib.orc_merge_pairs_f64.argtypes = [vp, i64, i64, vp]
+            lib.orc_merge_pairs_f64.restype = ctypes.c_int
+            lib.orc_softmax_finish_f64.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp, i64]
+            lib.orc_softmax_finish_f64.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -182,6 +188,46 @@ def layernorm_f64(x: np.ndarray, fmt: str, weight=None, bias=None, eps: float = 
     y = np.empty((M, N), dtype=np.float64)
     rc = _load().orc_layernorm_f64(x.ctypes.data, FORMATS[fmt], M, N, ld, None if w is None else w.ctypes.data,
                                    None if b is None else b.ctypes.data, float(eps), y.ctypes.data, N)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the call (status {rc})")
+    return y
+
+
+def softmax_partial_f64(x: np.ndarray, fmt: str, n_cols: int | None = None) -> np.ndarray:
+    """The (m, l) pair of every row of ``x`` over its first ``n_cols`` columns
+    (one shard of a row split by columns): m the max, l the sum of exp(x - m).
+    Returns an (M, 2) float64 array."""
+    x = _as_storage(np.atleast_2d(x), fmt)
+    M, ld = x.shape
+    N = ld if n_cols is None else int(n_cols)
+    ml = np.empty((M, 2), dtype=np.float64)
+    rc = _load().orc_softmax_partial_f64(x.ctypes.data, FORMATS[fmt], M, N, ld, ml.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the call (status {rc})")
+    return ml
+
+
+def merge_pairs_f64(pairs: np.ndarray) -> np.ndarray:
+    """Merge of the (R, M, 2) pairs of R shards into (M, 2), shard 0 first."""
+    pairs = np.ascontiguousarray(pairs, dtype=np.float64)
+    if pairs.ndim != 3 or pairs.shape[2] != 2:
+        raise ValueError("pairs must have shape (R, M, 2)")
+    R, M, _ = pairs.shape
+    out = np.empty((M, 2), dtype=np.float64)
+    rc = _load().orc_merge_pairs_f64(pairs.ctypes.data, R, M, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the call (status {rc})")
+    return out
+
+
+def softmax_finish_f64(x: np.ndarray, fmt: str, pairs: np.ndarray, n_cols: int | None = None) -> np.ndarray:
+    """y = exp(x - m) / l over the rows of ``x`` with the merged (M, 2) pairs."""
+    x = _as_storage(np.atleast_2d(x), fmt)
+    M, ld = x.shape
+    N = ld if n_cols is None else int(n_cols)
+    pairs = np.ascontiguousarray(pairs, dtype=np.float64).reshape(M, 2)
+    y = np.empty((M, N), dtype=np.float64)
+    rc = _load().orc_softmax_finish_f64(x.ctypes.data, FORMATS[fmt], M, N, ld, pairs.ctypes.data, y.ctypes.data, N)
     if rc != 0:
         raise ValueError(f"oracle rejected the call (status {rc})")
     return y

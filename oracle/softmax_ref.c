@@ -29,13 +29,15 @@
  *  - output encoding to fp16 / bf16 is round-to-nearest, ties-to-even, done
  *    directly from the double result (no intermediate fp32 rounding).
  *
- * It also holds the plain definitions of RMSNorm and LayerNorm (end of file),
- * and the row softmax over a prefix of every row (a causal attention mask):
- * row r keeps its first L_r elements, the rest is treated as -inf and never
- * read.
+ * It also holds the plain definitions of RMSNorm and LayerNorm, the row
+ * softmax over a prefix of every row (a causal attention mask: row r keeps its
+ * first L_r elements, the rest is treated as -inf and never read), and the
+ * three steps of the softmax of a row split by columns into shards (partial
+ * pairs, their merge, the finish; end of file).
  *
- * Parity pins for this file live in tests/test_oracle_pins.py and
- * tests/test_oracle_norm_pins.py.
+ * Parity pins for this file live in tests/test_oracle_pins.py,
+ * tests/test_oracle_norm_pins.py, tests/test_oracle_prefix_pins.py and
+ * tests/test_oracle_split_pins.py.
  */
 #include <math.h>
 #include <pthread.h>
@@ -353,6 +355,94 @@ int orc_layernorm_f64(const void* x, int dtype, int64_t M, int64_t N, int64_t ld
         for (int64_t j = 0; j < N; ++j)
             y[r * ldy + j] = (orc_load(x, dtype, r * ldx + j) - mu) / sd * orc_vec(w, dtype, j, 1.0) +
                              orc_vec(b, dtype, j, 0.0);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * A row split by columns into shards (the vocabulary-parallel softmax, where
+ * each device holds a block of columns of every row).  The online normaliser
+ * of the mohakchugh.is-a.dev post ("How Flash Attention Uses Triton") carries
+ * a running pair (m, l) -- the max seen so far and the sum of exp(x - m) over
+ * the values seen -- and combines two pairs as
+ *     m = max(m1, m2),   l = l1 exp(m1 - m) + l2 exp(m2 - m),
+ * starting from (-inf, 0).  Here:
+ *   partial: each shard reduces its columns of row r to (m, l) with
+ *            m = max_j x_j, l = sum_j exp(x_j - m);
+ *   merge:   the R shards' pairs of a row are combined with the rule above,
+ *            shard 0 first;
+ *   finish:  each shard writes y_j = exp(x_j - m) / l for its columns with the
+ *            merged pair.
+ * In exact arithmetic this is the row softmax of the whole row, however the
+ * columns are split.  Readings where the recurrence leaves a case open: a
+ * shard with no column, or whose entries are all -inf, contributes the
+ * starting pair (-inf, 0) (it holds no mass of the row; the plain formula's
+ * (-inf) - (-inf) would otherwise turn a well-defined row into NaN); a pair
+ * whose max is -inf enters a merge with weight 0 times its sum, so a NaN sum
+ * still reaches the result; NaN entries never win the max and make the sum
+ * NaN; the finish of a row whose merged max is -inf is NaN (the whole row is
+ * -inf: the plain formula's NaN row).
+ * Pairs are stored as two doubles (m, l) per row.
+ * ------------------------------------------------------------------------- */
+static void orc_partial_row(const void* x, int dtype, int64_t off, int64_t N, double* m_out, double* l_out)
+{
+    double m = -INFINITY;
+    int any_nan = 0;
+    for (int64_t j = 0; j < N; ++j) {
+        const double v = orc_load(x, dtype, off + j);
+        if (v > m) m = v;
+        if (v != v) any_nan = 1;
+    }
+    double l = 0.0;
+    if (m == -INFINITY) {
+        l = any_nan ? NAN : 0.0;  /* all -inf (or empty): the starting pair */
+    } else {
+        for (int64_t j = 0; j < N; ++j) l += exp(orc_load(x, dtype, off + j) - m);
+    }
+    *m_out = m;
+    *l_out = l;
+}
+
+/* ml[2 r] = m_r, ml[2 r + 1] = l_r for the M rows of x (N columns, stride ldx). */
+int orc_softmax_partial_f64(const void* x, int dtype, int64_t M, int64_t N, int64_t ldx, double* ml)
+{
+    if (orc_check(dtype, M, N, ldx, N) || (M > 0 && ldx < N)) return 1;
+    for (int64_t r = 0; r < M; ++r) orc_partial_row(x, dtype, r * ldx, N, &ml[2 * r], &ml[2 * r + 1]);
+    return 0;
+}
+
+/* One step of the online normaliser: (m, l) absorbs (m2, l2). */
+static void orc_absorb(double* m, double* l, double m2, double l2)
+{
+    const double mn = m2 > *m ? m2 : *m;
+    const double a = *m == -INFINITY ? *l * 0.0 : *l * exp(*m - mn);
+    const double b = m2 == -INFINITY ? l2 * 0.0 : l2 * exp(m2 - mn);
+    *m = mn;
+    *l = a + b;
+}
+
+/* ml_in: R x M pairs, shard-major (pair of shard s, row r at ml_in[2 (s M + r)]);
+ * ml_out: the M merged pairs. */
+int orc_merge_pairs_f64(const double* ml_in, int64_t R, int64_t M, double* ml_out)
+{
+    if (R < 0 || M < 0) return 1;
+    for (int64_t r = 0; r < M; ++r) {
+        double m = -INFINITY, l = 0.0;
+        for (int64_t s = 0; s < R; ++s) orc_absorb(&m, &l, ml_in[2 * (s * M + r)], ml_in[2 * (s * M + r) + 1]);
+        ml_out[2 * r] = m;
+        ml_out[2 * r + 1] = l;
+    }
+    return 0;
+}
+
+/* y[r][j] = exp(x[r][j] - m_r) / l_r with the merged pairs ml (two doubles a row). */
+int orc_softmax_finish_f64(const void* x, int dtype, int64_t M, int64_t N, int64_t ldx, const double* ml,
+                           double* y, int64_t ldy)
+{
+    if (orc_check(dtype, M, N, ldx, ldy)) return 1;
+    for (int64_t r = 0; r < M; ++r) {
+        const double m = ml[2 * r], l = ml[2 * r + 1];
+        for (int64_t j = 0; j < N; ++j) y[r * ldy + j] = exp(orc_load(x, dtype, r * ldx + j) - m) / l;
     }
     return 0;
 }
