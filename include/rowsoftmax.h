@@ -290,6 +290,69 @@ RS_API int rownorm_plan(int op, const void* in, const void* out, const void* wei
                         double eps, int dtype, const rs_options* opts, const rs_device_info* dev,
                         rs_plan* plan);
 
+/*
+ * The softmax of rows split by columns into shards: the vocabulary-parallel
+ * softmax, where each device holds a block of columns of every row (logits
+ * over a vocabulary sharded across devices), and, on one device, the split
+ * of a few very wide rows into blocks so that every multiprocessor works on
+ * them.  The steps are those of the online normaliser of the
+ * mohakchugh.is-a.dev post ("How Flash Attention Uses Triton"): each shard
+ * reduces its columns of a row to a pair (m, l) -- m the max, l the sum of
+ * exp(x - m) -- the pairs of a row are merged as
+ *     m = max(m1, m2),   l = l1 exp(m1 - m) + l2 exp(m2 - m),
+ * from (-inf, 0), and each shard writes exp(x - m) / l with the merged pair.
+ * In exact arithmetic the result is the row softmax of the whole row.
+ *
+ * Pairs are stored as two fp32 values {m, l} per row (8 bytes, 8-byte aligned
+ * device memory), m in the units of x (so m + log(l) is the log of the sum of
+ * exp over the shard).  A shard whose columns of a row are all -inf, or that
+ * has no column, gives (-inf, 0); NaN entries make l NaN; a row whose merged
+ * max is -inf finishes as NaN (the whole row was -inf).  Data model, device
+ * pointers, asynchrony and error codes are those of rowsoftmax_fwd; a pair
+ * array that overlaps a tensor it is read or written with is RS_ERR_OVERLAP.
+ * Typical use on R devices, each holding x[:, c_s : c_s + N_s]:
+ *     rowsoftmax_partial_fwd(x_s, pairs_s, M, N_s, ...);
+ *     all-gather pairs_s over the devices into R x M pairs (shard-major);
+ *     rowsoftmax_finish_fwd(x_s, y_s, all_pairs, R, M, N_s, ...);
+ */
+
+/* ml[r] = (m, l) of row r over its N columns (one shard).  N may be 0 (the
+ * pairs are then (-inf, 0) and `in` is not read).  `ml` holds M pairs. */
+RS_API int rowsoftmax_partial_fwd(const void* in, void* ml, int64_t M, int64_t N, int64_t in_row_stride, int dtype,
+                                  cudaStream_t stream);
+
+/* ml_out[r] = the merge of the R pairs ml_in[s * M + r], s = 0 .. R - 1 (R x M
+ * pairs, shard-major: the layout of an all-gather of the shards' pair
+ * arrays).  R == 0 gives (-inf, 0).  The two arrays must not overlap. */
+RS_API int rowsoftmax_merge_ml(const void* ml_in, void* ml_out, int64_t R, int64_t M, cudaStream_t stream);
+
+/* y[r][j] = exp(x[r][j] - m_r) / l_r for the N columns of this shard, with
+ * (m_r, l_r) the merge of the R >= 1 pairs ml[s * M + r] (R == 1: an already
+ * merged pair array).  In place (in == out, equal strides) is allowed; `ml`
+ * must not overlap `out`.  R < 1 is RS_ERR_INVALID_ARG. */
+RS_API int rowsoftmax_finish_fwd(const void* in, void* out, const void* ml, int64_t R, int64_t M, int64_t N,
+                                 int64_t in_row_stride, int64_t out_row_stride, int dtype, cudaStream_t stream);
+
+/* Host-only: the workspace bytes rowsoftmax_split_fwd needs for M rows of N
+ * columns (0 for an empty problem): M * (S + 1) pairs, S the blocks a row is
+ * split into (about 4096 (row, block) items in all, blocks of at least 32 KB). */
+RS_API int rowsoftmax_split_workspace_size(int64_t M, int64_t N, int dtype, size_t* bytes);
+
+/* The row softmax of rowsoftmax_fwd computed as above on one device: each row
+ * is split into S blocks, one pair per (row, block) is written to
+ * `workspace`, the pairs are merged and every block finishes.  x is read
+ * twice (the second read mostly from L2 when the input fits there) and y
+ * written once.  For rows too few to fill the device and too wide for the
+ * cluster kernels (a few rows of millions of values); with many rows
+ * rowsoftmax_fwd, which reads x once, is faster.  `workspace` is caller-owned
+ * device memory of at least rowsoftmax_split_workspace_size bytes, 8-byte
+ * aligned, not overlapping x or y (RS_ERR_INVALID_ARG when too small);
+ * its contents on entry do not matter and are undefined afterwards.
+ * In place (in == out, equal strides) is allowed. */
+RS_API int rowsoftmax_split_fwd(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                                int64_t out_row_stride, int dtype, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
 /* Host-only: fill `dev` for the current CUDA device.  Returns RS_OK or
  * RS_ERR_CUDA. */
 RS_API int rowsoftmax_device_info(rs_device_info* dev);

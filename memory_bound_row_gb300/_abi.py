@@ -47,6 +47,11 @@ EXPORTED = (
     "rowsoftmax_causal_fwd",
     "rowsoftmax_causal_fwd_ex",
     "rowsoftmax_causal_plan",
+    "rowsoftmax_partial_fwd",
+    "rowsoftmax_merge_ml",
+    "rowsoftmax_finish_fwd",
+    "rowsoftmax_split_workspace_size",
+    "rowsoftmax_split_fwd",
 )
 
 
@@ -157,6 +162,16 @@ def load() -> ctypes.CDLL:
         lib.rowsoftmax_causal_plan.argtypes = [vp, vp, i64, i64, i64, i64, i64, i64, ci, ctypes.POINTER(rs_options),
                                                ctypes.POINTER(rs_device_info), ctypes.POINTER(rs_plan)]
         lib.rowsoftmax_causal_plan.restype = ci
+        lib.rowsoftmax_partial_fwd.argtypes = [vp, vp, i64, i64, i64, ci, vp]
+        lib.rowsoftmax_partial_fwd.restype = ci
+        lib.rowsoftmax_merge_ml.argtypes = [vp, vp, i64, i64, vp]
+        lib.rowsoftmax_merge_ml.restype = ci
+        lib.rowsoftmax_finish_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ci, vp]
+        lib.rowsoftmax_finish_fwd.restype = ci
+        lib.rowsoftmax_split_workspace_size.argtypes = [i64, i64, ci, ctypes.POINTER(ctypes.c_size_t)]
+        lib.rowsoftmax_split_workspace_size.restype = ci
+        lib.rowsoftmax_split_fwd.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, ctypes.c_size_t, vp]
+        lib.rowsoftmax_split_fwd.restype = ci
         _lib = lib
         return lib
 
@@ -269,3 +284,30 @@ def rowsoftmax_causal_plan(in_ptr: int, out_ptr: int, M: int, N: int, in_row_str
     rc = load().rowsoftmax_causal_plan(in_ptr, out_ptr, M, N, in_row_stride, out_row_stride, period, diag_offset,
                                        dtype, _opts(options), dev, ctypes.byref(plan))
     return rc, plan.as_dict()
+
+
+def rowsoftmax_partial_fwd(in_ptr: int | None, ml_ptr: int, M: int, N: int, in_row_stride: int, dtype: int,
+                           stream: int = 0) -> int:
+    return load().rowsoftmax_partial_fwd(in_ptr, ml_ptr, M, N, in_row_stride, dtype, stream)
+
+
+def rowsoftmax_merge_ml(ml_in_ptr: int | None, ml_out_ptr: int, R: int, M: int, stream: int = 0) -> int:
+    return load().rowsoftmax_merge_ml(ml_in_ptr, ml_out_ptr, R, M, stream)
+
+
+def rowsoftmax_finish_fwd(in_ptr: int, out_ptr: int, ml_ptr: int, R: int, M: int, N: int, in_row_stride: int,
+                          out_row_stride: int, dtype: int, stream: int = 0) -> int:
+    return load().rowsoftmax_finish_fwd(in_ptr, out_ptr, ml_ptr, R, M, N, in_row_stride, out_row_stride, dtype,
+                                        stream)
+
+
+def rowsoftmax_split_workspace_size(M: int, N: int, dtype: int) -> tuple[int, int]:
+    n = ctypes.c_size_t(0)
+    rc = load().rowsoftmax_split_workspace_size(M, N, dtype, ctypes.byref(n))
+    return rc, n.value
+
+
+def rowsoftmax_split_fwd(in_ptr: int, out_ptr: int, M: int, N: int, in_row_stride: int, out_row_stride: int,
+                         dtype: int, workspace_ptr: int | None, workspace_bytes: int, stream: int = 0) -> int:
+    return load().rowsoftmax_split_fwd(in_ptr, out_ptr, M, N, in_row_stride, out_row_stride, dtype, workspace_ptr,
+                                       workspace_bytes, stream)

@@ -8,6 +8,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "rowsoftmax.h"
@@ -874,6 +875,194 @@ int rowsoftmax_layout_owner(int64_t j, int threads, int vec, int* thread, int64_
     *thread = (int)((j / vec) % threads);
     *slot = (j / ((int64_t)threads * vec)) * vec + j % vec;
     return RS_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The softmax of rows split by columns: partial pairs, their merge, the finish,
+// and the one-device split of few wide rows (kernels in rs_split.cu).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kSplitTargetItems = 4096;     // (row, block) items a split call aims for
+constexpr int64_t kSplitMinBlockUnits = 2048;   // 16-byte units of the narrowest block (32 KB)
+constexpr int64_t kPairBytes = 8;               // one float2 {m, l}
+
+// Row-major tensor of M rows x N elements of size es at `p`, row stride ld:
+// pointer, alignment and extent checks; *ext = its byte extent.
+int check_tensor(const void* p, int64_t M, int64_t N, int64_t ld, int es, uint64_t* ext) {
+    *ext = 0;
+    if (M == 0 || N == 0) return RS_OK;
+    if (!p) return RS_ERR_INVALID_ARG;
+    if ((uintptr_t)p % es) return RS_ERR_INVALID_ARG;
+    if (ld < N) return RS_ERR_INVALID_ARG;
+    if ((M - 1) > (INT64_MAX / es - N) / ld) return RS_ERR_INVALID_ARG;
+    *ext = (uint64_t)(((M - 1) * ld + N) * es);
+    if ((uintptr_t)p > UINTPTR_MAX - *ext) return RS_ERR_INVALID_ARG;
+    return RS_OK;
+}
+
+// n float2 pairs at p: non-null, 8-byte aligned, no address overflow.
+int check_pairs(const void* p, int64_t n, uint64_t* ext) {
+    *ext = 0;
+    if (n == 0) return RS_OK;
+    if (!p || (uintptr_t)p % kPairBytes) return RS_ERR_INVALID_ARG;
+    if (n > INT64_MAX / kPairBytes) return RS_ERR_INVALID_ARG;
+    *ext = (uint64_t)(n * kPairBytes);
+    if ((uintptr_t)p > UINTPTR_MAX - *ext) return RS_ERR_INVALID_ARG;
+    return RS_OK;
+}
+
+int split_vec(const void* in, const void* out, int64_t M, int64_t ldi, int64_t ldo, int dtype) {
+    const int es = elem_size(dtype);
+    const bool strides = M == 1 || ((ldi * es) % 16 == 0 && (ldo * es) % 16 == 0);
+    return (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0 && strides ? 16 / es : 1;
+}
+
+// Blocks per row (S) and their width (B) of a one-device split: about
+// kSplitTargetItems items, blocks of at least kSplitMinBlockUnits units,
+// widths a whole number of 16-byte units.
+void split_shape(int64_t M, int64_t N, int dtype, int64_t* S, int64_t* B) {
+    const int64_t kvec = 16 / elem_size(dtype);
+    const int64_t units = ceil_div(N, kvec);
+    int64_t s = ceil_div(kSplitTargetItems, M);
+    const int64_t smax = ceil_div(units, kSplitMinBlockUnits);
+    if (s > smax) s = smax;
+    if (s < 1) s = 1;
+    const int64_t b = round_up(ceil_div(N, s), kvec);
+    *B = b;
+    *S = ceil_div(N, b);
+}
+
+// Current device, its facts, and device-pointer checks of the non-null pointers.
+int split_device(rs::SplitLaunch* L, std::initializer_list<const void*> ptrs) {
+    int dev = 0;
+    rs_device_info info;
+    int rc = current_device(&dev, &info);
+    if (rc != RS_OK) return rc;
+    for (const void* p : ptrs)
+        if (p && (rc = check_device_pointer(p, dev)) != RS_OK) return rc;
+    L->sm_count = info.sm_count;
+    L->strict = false;
+    return RS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rowsoftmax_partial_fwd(const void* in, void* ml, int64_t M, int64_t N, int64_t in_row_stride, int dtype,
+                           cudaStream_t stream) {
+    if (dtype != RS_F32 && dtype != RS_F16 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED_DTYPE;
+    if (M < 0 || N < 0 || N > kMaxN) return RS_ERR_INVALID_ARG;
+    if (M == 0) return RS_OK;
+    const int es = elem_size(dtype);
+    uint64_t ext_i = 0, ext_p = 0;
+    int rc = check_tensor(in, M, N, in_row_stride, es, &ext_i);
+    if (rc != RS_OK) return rc;
+    if ((rc = check_pairs(ml, M, &ext_p)) != RS_OK) return rc;
+    if (N > 0 && ranges_overlap((uintptr_t)in, ext_i, (uintptr_t)ml, ext_p)) return RS_ERR_OVERLAP;
+    rs::SplitLaunch L;
+    if ((rc = split_device(&L, {N > 0 ? in : nullptr, ml})) != RS_OK) return rc;
+    const int64_t ldi = N > 0 ? in_row_stride : 0;
+    L.vec = N > 0 ? split_vec(in, in, M, ldi, ldi, dtype) : 1;
+    const cudaError_t e =
+        rs::launch_split_partial(L, dtype, in, static_cast<float2*>(ml), M, (int)N, ldi, 1, (int)N, stream);
+    return e == cudaSuccess ? RS_OK : fail_cuda(e);
+}
+
+int rowsoftmax_merge_ml(const void* ml_in, void* ml_out, int64_t R, int64_t M, cudaStream_t stream) {
+    if (R < 0 || M < 0) return RS_ERR_INVALID_ARG;
+    if (M == 0) return RS_OK;
+    if (R > 0 && M > INT64_MAX / R) return RS_ERR_INVALID_ARG;
+    uint64_t ext_in = 0, ext_out = 0;
+    int rc = check_pairs(ml_in, R * M, &ext_in);
+    if (rc != RS_OK) return rc;
+    if ((rc = check_pairs(ml_out, M, &ext_out)) != RS_OK) return rc;
+    if (R > 0 && ranges_overlap((uintptr_t)ml_in, ext_in, (uintptr_t)ml_out, ext_out)) return RS_ERR_OVERLAP;
+    rs::SplitLaunch L;
+    if ((rc = split_device(&L, {R > 0 ? ml_in : nullptr, ml_out})) != RS_OK) return rc;
+    L.vec = 1;
+    const cudaError_t e = rs::launch_split_merge(L, static_cast<const float2*>(ml_in), static_cast<float2*>(ml_out),
+                                                 R, 1, M, M, stream);
+    return e == cudaSuccess ? RS_OK : fail_cuda(e);
+}
+
+int rowsoftmax_finish_fwd(const void* in, void* out, const void* ml, int64_t R, int64_t M, int64_t N,
+                          int64_t in_row_stride, int64_t out_row_stride, int dtype, cudaStream_t stream) {
+    if (dtype != RS_F32 && dtype != RS_F16 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED_DTYPE;
+    if (M < 0 || N < 0 || R < 1 || N > kMaxN) return RS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return RS_OK;
+    if (M > INT64_MAX / R) return RS_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    uint64_t ext_i = 0, ext_o = 0, ext_p = 0;
+    int rc = check_tensor(in, M, N, in_row_stride, es, &ext_i);
+    if (rc != RS_OK) return rc;
+    if ((rc = check_tensor(out, M, N, out_row_stride, es, &ext_o)) != RS_OK) return rc;
+    if ((rc = check_pairs(ml, R * M, &ext_p)) != RS_OK) return rc;
+    if (ranges_overlap((uintptr_t)in, ext_i, (uintptr_t)out, ext_o) &&
+        !(in == out && in_row_stride == out_row_stride))
+        return RS_ERR_OVERLAP;
+    if (ranges_overlap((uintptr_t)ml, ext_p, (uintptr_t)out, ext_o)) return RS_ERR_OVERLAP;
+    rs::SplitLaunch L;
+    if ((rc = split_device(&L, {in, out, ml})) != RS_OK) return rc;
+    L.vec = split_vec(in, out, M, in_row_stride, out_row_stride, dtype);
+    const cudaError_t e = rs::launch_split_finish(L, dtype, in, out, static_cast<const float2*>(ml), R, 1, M, M,
+                                                  (int)N, in_row_stride, out_row_stride, stream);
+    return e == cudaSuccess ? RS_OK : fail_cuda(e);
+}
+
+int rowsoftmax_split_workspace_size(int64_t M, int64_t N, int dtype, size_t* bytes) {
+    if (!bytes) return RS_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (dtype != RS_F32 && dtype != RS_F16 && dtype != RS_BF16) return RS_ERR_UNSUPPORTED_DTYPE;
+    if (M < 0 || N < 0 || N > kMaxN) return RS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return RS_OK;
+    int64_t S = 0, B = 0;
+    split_shape(M, N, dtype, &S, &B);
+    if (M > (INT64_MAX / kPairBytes) / (S + 1)) return RS_ERR_INVALID_ARG;
+    *bytes = (size_t)(M * (S + 1) * kPairBytes);
+    return RS_OK;
+}
+
+int rowsoftmax_split_fwd(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                         int64_t out_row_stride, int dtype, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    size_t need = 0;
+    int rc = rowsoftmax_split_workspace_size(M, N, dtype, &need);
+    if (rc != RS_OK) return rc;
+    if (M == 0 || N == 0) return RS_OK;
+    const int es = elem_size(dtype);
+    uint64_t ext_i = 0, ext_o = 0, ext_w = 0;
+    if ((rc = check_tensor(in, M, N, in_row_stride, es, &ext_i)) != RS_OK) return rc;
+    if ((rc = check_tensor(out, M, N, out_row_stride, es, &ext_o)) != RS_OK) return rc;
+    if (workspace_bytes < need) return RS_ERR_INVALID_ARG;
+    if ((rc = check_pairs(workspace, (int64_t)(need / kPairBytes), &ext_w)) != RS_OK) return rc;
+    if (ranges_overlap((uintptr_t)in, ext_i, (uintptr_t)out, ext_o) &&
+        !(in == out && in_row_stride == out_row_stride))
+        return RS_ERR_OVERLAP;
+    if (ranges_overlap((uintptr_t)workspace, ext_w, (uintptr_t)in, ext_i) ||
+        ranges_overlap((uintptr_t)workspace, ext_w, (uintptr_t)out, ext_o))
+        return RS_ERR_OVERLAP;
+    rs::SplitLaunch L;
+    if ((rc = split_device(&L, {in, out, workspace})) != RS_OK) return rc;
+    int64_t S = 0, B = 0;
+    split_shape(M, N, dtype, &S, &B);
+    L.vec = split_vec(in, out, M, in_row_stride, out_row_stride, dtype);
+    float2* parts = static_cast<float2*>(workspace);  // M x S pairs, row-major
+    float2* merged = parts + M * S;                   // M pairs
+    cudaError_t e = rs::launch_split_partial(L, dtype, in, parts, M, (int)N, in_row_stride, (int)S, (int)B, stream);
+    // Up to 32 pairs a row are merged by each finishing warp itself; more are
+    // merged once per row first.
+    if (e == cudaSuccess && S > 32) e = rs::launch_split_merge(L, parts, merged, S, S, 1, M, stream);
+    if (e == cudaSuccess) {
+        e = S > 32 ? rs::launch_split_finish(L, dtype, in, out, merged, 1, 1, 0, M, (int)N, in_row_stride,
+                                             out_row_stride, stream)
+                   : rs::launch_split_finish(L, dtype, in, out, parts, S, S, 1, M, (int)N, in_row_stride,
+                                             out_row_stride, stream);
+    }
+    return e == cudaSuccess ? RS_OK : fail_cuda(e);
 }
 
 }  // extern "C"

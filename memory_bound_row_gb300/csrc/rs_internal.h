@@ -220,4 +220,22 @@ cudaError_t read_status_norm_f32(unsigned int* flags, bool clear);
 cudaError_t read_status_norm_f16(unsigned int* flags, bool clear);
 cudaError_t read_status_norm_bf16(unsigned int* flags, bool clear);
 
+// The softmax of rows split by columns (rs_split.cu).  Pairs are float2
+// {m, l}; the kernels use programmatic dependent launch unless `strict`.
+struct SplitLaunch {
+    int sm_count;
+    int vec;      // elements per access: the 16-byte width, or 1 (element-wise)
+    bool strict;  // launch in strict stream order
+};
+// ml[r * S + b] = the pair of columns [b * B, min(N, (b + 1) * B)) of row r.
+cudaError_t launch_split_partial(const SplitLaunch& L, int dtype, const void* in, float2* ml, int64_t M, int N,
+                                 int64_t ldi, int S, int B, cudaStream_t s);
+// out[r] = the merge of the R pairs ml[r * sr + s * ss], s = 0 .. R - 1.
+cudaError_t launch_split_merge(const SplitLaunch& L, const float2* ml, float2* out, int64_t R, int64_t sr, int64_t ss,
+                               int64_t M, cudaStream_t s);
+// y = exp(x - m) / l with (m, l) the merge of row r's R pairs as above.
+cudaError_t launch_split_finish(const SplitLaunch& L, int dtype, const void* in, void* out, const float2* ml,
+                                int64_t R, int64_t sr, int64_t ss, int64_t M, int N, int64_t ldi, int64_t ldo,
+                                cudaStream_t s);
+
 }  // namespace rs
