@@ -887,6 +887,137 @@ def run_sweep_wide(args):
         torch.cuda.empty_cache()
 
 
+SPLIT_SHAPES = [(1, 1 << 26, "f16"), (4, 1 << 22, "bf16"), (16, 1 << 20, "f16"), (64, 1 << 18, "bf16"),
+                (512, 131072, "f16")]
+
+
+def graph_ms(call, steps: int, stream) -> float:
+    """Milliseconds per call: `steps` calls replayed from one CUDA graph,
+    after one untimed replay, between CUDA events on `stream`."""
+    import torch
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for k in range(steps):
+            call(k)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+            for k in range(steps):
+                call(k)
+        graph.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_split(args):
+    """The split-row softmax measured on one device (one JSON line each):
+    (1) rowsoftmax_split_fwd against rowsoftmax_fwd on few, very wide rows
+    (M x N below; GB/s counts M N (in + out) bytes; the split reads x twice);
+    (2) the two steps of the vocabulary-parallel softmax on the bf16 causal
+    scores split into two column shards of 1024: rowsoftmax_partial_fwd on a
+    shard (bytes: its elements read, 8 a row written) and rowsoftmax_finish_fwd
+    with both shards' pairs (its elements read and written, the pairs read).
+    Every configuration is first checked against rowsoftmax_fwd on the same
+    input (max |difference| within 2^-7 for 16-bit, 1e-6 for fp32); timings
+    are graph-replayed launches over rotating buffers (more than 4x L2
+    between two uses of a buffer where the tensors are smaller than that)."""
+    import torch
+
+    import memory_bound_row_gb300 as rs
+    from memory_bound_row_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = rs._abi.load()
+    peak, _ = measured_peaks()
+    stream = torch.cuda.Stream(dev)
+    h = stream.cuda_stream
+    steps = max(4, min(args.steps, 64))
+    for M, N, dt in SPLIT_SHAPES:
+        code = {"f32": rs.RS_F32, "f16": rs.RS_F16, "bf16": rs.RS_BF16}[dt]
+        w = W.custom(M, N, dt, seed=9, kind="normal_spike")
+        set_bytes = 2 * M * N * w.elem_size
+        nsets = max(1, math.ceil(4 * L2_BYTES / set_bytes))
+        xs = [W.generate(w, dev)]
+        xs += [xs[0].clone() for _ in range(nsets - 1)]
+        ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+        rc, need = rs.rowsoftmax_split_workspace_size(M, N, code)
+        wss = [torch.empty(max(need, 8), dtype=torch.uint8, device=dev) for _ in range(nsets)]
+        ref = rs.softmax(xs[0])
+        got = rs.softmax_split(xs[0], workspace=wss[0])
+        torch.cuda.synchronize()
+        diff = float((ref.double() - got.double()).abs().max())
+        if not diff <= (1e-6 if dt == "f32" else 2.0 ** -7):
+            raise AssertionError(f"split {M}x{N}: differs from rowsoftmax_fwd by {diff:.3e}")
+        del ref, got
+
+        def fwd(k):
+            r = lib.rowsoftmax_fwd(xs[k % nsets].data_ptr(), ys[k % nsets].data_ptr(), M, N, N, N, code, h)
+            if r != rs.RS_OK:
+                raise rs.RowSoftmaxError(r)
+
+        def split(k):
+            r = lib.rowsoftmax_split_fwd(xs[k % nsets].data_ptr(), ys[k % nsets].data_ptr(), M, N, N, N, code,
+                                         wss[k % nsets].data_ptr(), need, h)
+            if r != rs.RS_OK:
+                raise rs.RowSoftmaxError(r)
+
+        rc, info = rs.rowsoftmax_device_info()
+        rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), M, N, N, N, code, None, info)
+        nbytes = M * N * 2 * w.elem_size
+        for name, fn in (("rowsoftmax_fwd (" + rs.PATH_NAMES[plan["path"]] + ")", fwd), ("rowsoftmax_split_fwd", split)):
+            ms = graph_ms(fn, steps, stream)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            print(json.dumps({"split": "few wide rows", "M": M, "N": N, "storage": dt, "call": name,
+                              "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "max_diff_to_fwd": diff}), flush=True)
+        del xs, ys, wss
+        torch.cuda.empty_cache()
+
+    # The vocabulary-parallel steps on the bf16 causal scores, two shards.
+    wl = W.WORKLOADS["bf16_causal_16x32x2048"]
+    M, N, half = wl.M, wl.N, wl.N // 2
+    x = W.generate(wl, dev)
+    y = torch.empty_like(x)
+    pairs = torch.empty((2, M, 2), dtype=torch.float32, device=dev)
+    for s in range(2):
+        rs.softmax_partial(x[:, s * half:(s + 1) * half], ml=pairs[s])
+    for s in range(2):
+        rs.softmax_finish(x[:, s * half:(s + 1) * half], pairs, out=y[:, s * half:(s + 1) * half])
+    ref = rs.softmax(x)
+    torch.cuda.synchronize()
+    diff = float((ref.double() - y.double()).abs().max())
+    if not diff <= 2.0 ** -7:
+        raise AssertionError(f"two shards differ from rowsoftmax_fwd by {diff:.3e}")
+    del ref
+    code = rs.RS_BF16
+    xp = [x[:, 0:half], x[:, half:N]]
+
+    def partial(k):
+        r = lib.rowsoftmax_partial_fwd(xp[k % 2].data_ptr(), pairs[k % 2].data_ptr(), M, half, N, code, h)
+        if r != rs.RS_OK:
+            raise rs.RowSoftmaxError(r)
+
+    def finish(k):
+        r = lib.rowsoftmax_finish_fwd(xp[k % 2].data_ptr(), y[:, (k % 2) * half:].data_ptr(), pairs.data_ptr(), 2, M,
+                                      half, N, N, code, h)
+        if r != rs.RS_OK:
+            raise rs.RowSoftmaxError(r)
+
+    for name, fn, nbytes in (("rowsoftmax_partial_fwd", partial, M * half * 2 + M * 8),
+                             ("rowsoftmax_finish_fwd (R = 2)", finish, M * half * 4 + 2 * M * 8)):
+        ms = graph_ms(fn, steps, stream)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"split": "vocabulary-parallel steps, one of two column shards", "M": M, "N_shard": half,
+                          "storage": "bf16", "call": name, "us": round(ms * 1e3, 2), "bytes": nbytes,
+                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "max_diff_to_fwd": diff}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -915,6 +1046,10 @@ def main():
                     help="instead of the benchmark line: wide 16-bit rows (N = 8192..65536) of the --op row "
                          "operation through the planner's choice, the ring and the clusters")
     ap.add_argument("--sweep-dtype", choices=["bf16", "f16"], default="bf16")
+    ap.add_argument("--split", action="store_true",
+                    help="instead of the benchmark line: the split-row softmax (few wide rows through "
+                         "rowsoftmax_split_fwd against rowsoftmax_fwd, and the vocabulary-parallel partial and "
+                         "finish steps on two column shards of the bf16 causal scores)")
     args = ap.parse_args()
     args.options = json.loads(args.options) if args.options else None
     if args.causal and args.op != "softmax":
@@ -929,7 +1064,9 @@ def main():
     for n in names:
         if n not in W.WORKLOADS:
             raise SystemExit(f"unknown workload {n}; choose from {', '.join(W.ORDER)} or 'all'")
-    if args.sweep_n:
+    if args.split:
+        run_split(args)
+    elif args.sweep_n:
         run_sweep_n(args)
     elif args.sweep_wide:
         run_sweep_wide(args)

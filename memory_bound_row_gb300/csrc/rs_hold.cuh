@@ -334,10 +334,21 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             const float c = rescale_off(m, safe_offset(qa)) / qb;
             __syncwarp();
             if (tid == 0 && received) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
+            if constexpr (OP::kMasked) {
+                // past the kept prefix: exactly 0, or NaN when the row keeps nothing
+                const int lv = slice_keep(row);
+                const float masked = row_keep(args, row, N) > 0 ? 0.0f : __int_as_float(0x7fffffff);
 #pragma unroll
-            for (int k = 0; k < VPT; ++k)
+                for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+                    for (int e = 0; e < VEC; ++e)
+                        v[k][e] = (tid + k * tpr) * VEC + e < lv ? v[k][e] * c : masked;
+            } else {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+            }
         } else {
             float r, nmr = 0.0f;
             if constexpr (OP::kOp == RS_OP_RMSNORM) {

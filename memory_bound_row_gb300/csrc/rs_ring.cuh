@@ -204,7 +204,7 @@ ring_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
                     }
                 }
             }
-            OP::template apply<DT, VEC, VPT>(v, t, tpr, N, false, prm, part[it & 1]);
+            OP::template apply<DT, VEC, VPT>(v, t, tpr, keep, false, prm, part[it & 1]);
             if (active && !abort) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v);
         } else if constexpr (HOLD) {
             float v[VPT][VEC];

@@ -289,10 +289,75 @@ struct OpSoftmax {
 
 // The softmax under a causal mask (RowArgs::mask_period > 0): each row keeps
 // a prefix (row_keep); the kernels copy and read only that prefix, and the rest
-// of the row, filled with -inf, comes out as exactly 0.  A separate type so
-// that the unmasked kernels carry no mask code.
+// of the row comes out as exactly 0 (NaN for a row that keeps nothing: an all
+// -inf row).  `n` is the row's kept length.  Slot k of the row's threads
+// covers elements [k tpr VEC, (k + 1) tpr VEC); the slots past the kept
+// prefix hold only the fill, so their max, exponentials, sum and scaling are
+// skipped (about half the arithmetic of a causal attention row), and only the
+// last kept slot is masked element by element.  A separate type so that the
+// unmasked kernels carry no mask code.
 struct OpSoftmaxCausal : OpSoftmax {
     static constexpr bool kMasked = true;
+    template <int DT, int VEC, int VPT, typename P>
+    __device__ static __forceinline__ void apply(float (&v)[VPT][VEC], int t, int tpr, int n, bool, const P&,
+                                                 float2* part) {
+        const int kk = (n + tpr * VEC - 1) / (tpr * VEC);  // slots holding a kept element
+        const int width = tpr < 32 ? tpr : 32;
+        float m = kNegInf;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            if (k < kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+        m = group_max(m, width);
+        const float ms = safe_max(m);
+        float l = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            if (k < kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    v[k][e] = exp_diff(v[k][e], ms);
+                    l += v[k][e];
+                }
+        l = group_sum(l, width);
+        float c;
+        if (tpr <= 32) {
+            c = 1.0f / l;
+        } else {
+            const int warp = threadIdx.x >> 5;
+            const int lane = threadIdx.x & 31;
+            const int wpr = tpr >> 5;
+            if (lane == 0) part[warp] = make_float2(m, l);
+            __syncthreads();
+            const int w0 = (warp / wpr) * wpr;
+            const int ww = pow2_ceil(wpr);
+            float pm = kNegInf, pl = 0.0f;
+            if (lane < wpr) {
+                const float2 q = part[w0 + lane];
+                pm = q.x;
+                pl = q.y;
+            }
+            const float mrow = __shfl_sync(0xffffffffu, group_max(pm, ww), 0);
+            const float mrs = safe_max(mrow);
+            const float srow = __shfl_sync(0xffffffffu, group_sum(pl * rescale(pm, mrs), ww), 0);
+            c = rescale(m, mrs) / srow;
+        }
+        const float masked = n > 0 ? 0.0f : __int_as_float(0x7fffffff);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            if (k + 1 < kk) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] *= c;
+            } else if (k + 1 == kk) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = (t + k * tpr) * VEC + e < n ? v[k][e] * c : masked;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = masked;
+            }
+        }
+    }
 };
 
 // RMSNorm ("Reference Kernel: RMSNorm", Hugging Face "triton-kernels" skill

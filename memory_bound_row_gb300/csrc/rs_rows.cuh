@@ -48,8 +48,8 @@ rows_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64_t 
         int keep = N;
         if constexpr (OP::kMasked) keep = row_keep(args, active ? row : 0, N);
         load_row_units<DT, VEC, VPT>(in + (active ? row : 0) * ldi, t, tpr, keep, active, v, OP::kFill);
-        OP::template apply<DT, VEC, VPT>(v, t, tpr, N, whole, GlobalParams{args.w, args.b, args.eps, N, 0},
-                                         part[it & 1]);
+        OP::template apply<DT, VEC, VPT>(v, t, tpr, OP::kMasked ? keep : N, whole,
+                                         GlobalParams{args.w, args.b, args.eps, N, 0}, part[it & 1]);
         if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v);
     }
 }

@@ -71,11 +71,35 @@ __device__ __forceinline__ float2 warp_merged_pair(const float2* ml, int64_t r, 
     return make_float2(m, l);
 }
 
+// Sum of a batch's values as a tree (short rounding chains).
+template <int B, int VEC>
+__device__ __forceinline__ float batch_sum(const float (&v)[B][VEC]) {
+    float u[B];
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+        float w[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) w[e] = v[k][e];
+#pragma unroll
+        for (int h = VEC / 2; h > 0; h /= 2)
+#pragma unroll
+            for (int e = 0; e < h; ++e) w[e] += w[e + h];
+        u[k] = w[0];
+    }
+#pragma unroll
+    for (int h = B / 2; h > 0; h /= 2)
+#pragma unroll
+        for (int k = 0; k < h; ++k) u[k] += u[k + h];
+    return u[0];
+}
+
 // One pair per (row, block) item: item q = r * S + b covers columns
 // [b * B, min(N, (b + 1) * B)) of row r and writes ml[q].  TPI threads serve
 // an item (256 / TPI items a CTA at a time); each thread takes units t,
 // t + TPI, ... of the item, kPartialBatch at a time, and keeps a running
-// (m, l): a batch's max raises m (rescaling l once), then its exps are added.
+// (m, l): a batch's max raises m (rescaling l once), then the batch's exps,
+// summed as a tree, are added to l with compensated (Kahan) summation, so
+// that a thread's long run of batches adds no more than a few roundings.
 template <int DT, int VEC, int TPI>
 __global__ void __launch_bounds__(kSplitThreads)
 partial_kernel(const void* in_, float2* ml, int64_t M, int N, int64_t ldi, int S, int B) {
@@ -97,6 +121,7 @@ partial_kernel(const void* in_, float2* ml, int64_t M, int N, int64_t ldi, int S
     for (int64_t g = blockIdx.x; g * kIpc < items; g += gridDim.x, ++it) {
         const int64_t q = g * kIpc + sub;
         float m = kNegInf, l = 0.0f;
+        float comp = 0.0f;  // the compensation of l's running sum
         if (q < items) {
             const int64_t r = q / S;
             const int64_t c0 = (q - r * S) * (int64_t)B;
@@ -121,14 +146,20 @@ partial_kernel(const void* in_, float2* ml, int64_t M, int N, int64_t ldi, int S
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, v[k][e]);
                 if (bm > m) {
-                    l *= rescale(m, bm);
+                    const float f = rescale(m, bm);
+                    l *= f;
+                    comp *= f;
                     m = bm;
                 }
                 const float ms = safe_max(m);
 #pragma unroll
                 for (int k = 0; k < kPartialBatch; ++k)
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) l += exp_diff(v[k][e], ms);
+                    for (int e = 0; e < VEC; ++e) v[k][e] = exp_diff(v[k][e], ms);
+                const float y = batch_sum<kPartialBatch, VEC>(v) - comp;
+                const float sum = l + y;
+                comp = (sum - l) - y;
+                l = sum;
             }
         }
         group_merge(m, l, 32);
@@ -152,19 +183,34 @@ partial_kernel(const void* in_, float2* ml, int64_t M, int N, int64_t ldi, int S
     allow_next_grid();
 }
 
-// One warp per row: out[r] = the merge of the R pairs ml[r * sr + s * ss].
+// One CTA per row: out[r] = the merge of the R pairs ml[r * sr + s * ss]
+// (R / 256 a thread, then warp butterflies and the CTA's warps: a tree).
 __global__ void __launch_bounds__(kSplitThreads)
 merge_kernel(const float2* ml, float2* out, int64_t R, int64_t sr, int64_t ss, int64_t M) {
+    __shared__ float2 part[2][kSplitThreads / 32];
     const int lane = threadIdx.x & 31;
-    const int64_t warps = (int64_t)gridDim.x * (kSplitThreads / 32);
+    const int warp = threadIdx.x >> 5;
     wait_prior_grid();
-    for (int64_t r = (int64_t)blockIdx.x * (kSplitThreads / 32) + (threadIdx.x >> 5); r < M; r += warps) {
-        if (R == 0) {
-            if (lane == 0) out[r] = make_float2(kNegInf, 0.0f);
-            continue;
+    int it = 0;
+    for (int64_t r = blockIdx.x; r < M; r += gridDim.x, ++it) {
+        float m = kNegInf, l = 0.0f;
+        for (int64_t s = threadIdx.x; s < R; s += kSplitThreads) {
+            const float2 p = ml[r * sr + s * ss];
+            absorb(m, l, p.x, p.y);
         }
-        const float2 p = warp_merged_pair(ml, r, R, sr, ss, lane);
-        if (lane == 0) out[r] = p;
+        group_merge(m, l, 32);
+        if (lane == 0) part[it & 1][warp] = make_float2(m, l);
+        __syncthreads();
+        if (warp == 0) {
+            float pm = kNegInf, pl = 0.0f;
+            if (lane < kSplitThreads / 32) {
+                const float2 p = part[it & 1][lane];
+                pm = p.x;
+                pl = p.y;
+            }
+            group_merge(pm, pl, kSplitThreads / 32);
+            if (lane == 0) out[r] = make_float2(pm, pl);
+        }
     }
     allow_next_grid();
 }
@@ -305,7 +351,7 @@ cudaError_t launch_split_partial(const SplitLaunch& L, int dtype, const void* in
 
 cudaError_t launch_split_merge(const SplitLaunch& L, const float2* ml, float2* out, int64_t R, int64_t sr, int64_t ss,
                                int64_t M, cudaStream_t s) {
-    return launch_kernel(merge_kernel, grid_of(merge_kernel, (M + 7) / 8, L.sm_count), kSplitThreads, 0, s, 0, L.strict,
+    return launch_kernel(merge_kernel, grid_of(merge_kernel, M, L.sm_count), kSplitThreads, 0, s, 0, L.strict,
                          ml, out, R, sr, ss, M);
 }
 

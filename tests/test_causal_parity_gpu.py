@@ -178,3 +178,37 @@ def test_kv_cache_offset_layout():
     _garbage(x, Sq, Sk - Sq)
     y = _run(x, Sq, Sk - Sq)
     compare(y, ref, "f16", "kv-cache layout")
+
+
+@pytest.mark.parametrize("path", ["rows", "ring", "cluster"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_non_finite_values_in_the_kept_prefix(path, dtype):
+    # A NaN or +inf inside the kept prefix makes the kept part NaN; the masked
+    # part stays exactly 0, as the definition states (the softmax of the kept
+    # values, 0 past them); a row that keeps nothing is NaN throughout.
+    N = 2048 if path != "cluster" else 65536
+    P, offset = 16, (0 if path != "cluster" else N // 2)
+    M = 2 * P
+    x, out = _aligned(M, N, dtype, seed=77)
+    keep = [min(N, max(0, r % P + 1 + offset)) for r in range(M)]
+    x[1, 0] = float("nan")
+    x[5, keep[5] - 1] = float("inf")
+    x[9, keep[9] // 2] = float("nan")
+    opts = PATHS[path]
+    if not _servable(x, P, offset, opts):
+        pytest.skip("this kernel does not serve the shape")
+    ref = _oracle(x, P, offset)
+    _garbage(x, P, offset)
+    y = _run(x, P, offset, out=out, options=opts)
+    compare(y, ref, dtype, f"non-finite kept values, {path} {dtype}")
+    yd = y.double().cpu().numpy()
+    for r in (1, 5, 9):
+        assert np.all(np.isnan(yd[r, :keep[r]])) and np.all(yd[r, keep[r]:] == 0.0)
+    # a period with an empty prefix (offset -1 on row 0 of each period)
+    x2, out2 = _aligned(M, N, dtype, seed=78)
+    if not _servable(x2, P, -1, opts):
+        return
+    ref2 = _oracle(x2, P, -1)
+    y2 = _run(x2, P, -1, out=out2, options=opts)
+    compare(y2, ref2, dtype, f"empty prefixes, {path} {dtype}")
+    assert bool(torch.isnan(y2[0]).all()) and bool(torch.isnan(y2[P]).all())
