@@ -119,7 +119,8 @@ typedef struct {
     int vec_per_thread;   /* RS_PATH_ROWS: 16-byte vectors (or elements, when scalar) per thread */
     int block_threads;    /* threads per CTA (RS_PATH_ROWS: multiple of threads_per_row) */
     int cluster_size;     /* RS_PATH_CLUSTER / RS_PATH_STREAM: CTAs per row, 1..16 */
-    int stages;           /* RS_PATH_RING: shared-memory stages per CTA, 2..8 */
+    int stages;           /* RS_PATH_RING: shared-memory stages per CTA, 2..8; register-holding
+                             RS_PATH_CLUSTER: landing slots per CTA, 1..4 */
     int ring_values;      /* RS_PATH_RING: rs_ring_values */
     int force_scalar;     /* 1: element-wise accesses even when 16-byte vectors would be legal */
     int64_t grid_limit;   /* >0: cap on CTAs (rows loop inside the kernel); 0: one launch slot per row group */

@@ -241,7 +241,7 @@ int plan_cluster_hold(int dtype, int vec, int64_t M, int64_t N, const rs_options
                       rs_plan* p) {
     const int es = elem_size(dtype);
     const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kWideStaticSmem;
-    if (o.stages && (o.stages < 1 || o.stages > 2)) return RS_ERR_INVALID_ARG;
+    if (o.stages && (o.stages < 1 || o.stages > rs::kWideHoldMaxSlots)) return RS_ERR_INVALID_ARG;
     int cs = o.cluster_size;
     int block = 0, vpt = 0;
     int64_t chunk = 0;

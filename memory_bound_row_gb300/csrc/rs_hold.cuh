@@ -79,7 +79,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
     const int rank = (int)cluster.block_rank();
 
     extern __shared__ __align__(128) unsigned char slots[];
-    __shared__ __align__(8) uint64_t bars[2];      // slot filled
+    __shared__ __align__(8) uint64_t bars[kWideHoldMaxSlots];  // slot filled
     __shared__ __align__(8) uint64_t recv_bar[2];  // all CTAs' pairs of a row received
     __shared__ __align__(8) float2 recv[2][kMaxCluster];
     __shared__ float2 warp_part[2][kWideHoldThreads / 32];
@@ -126,8 +126,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
     };
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int j = 0; j < nslots; ++j) mbar_init(&bars[j], 1);
         mbar_init(&recv_bar[0], 1);
         mbar_init(&recv_bar[1], 1);
         mbar_arrive_expect_tx(&recv_bar[0], pair_bytes);  // armed for rows 0 and 1 of this cluster

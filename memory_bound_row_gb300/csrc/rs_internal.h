@@ -62,6 +62,7 @@ constexpr int kMaxCluster = 16;        // needs the non-portable cluster-size op
 constexpr size_t kWideStaticSmem = 1024;  // upper bound of the kernel's static shared memory
 constexpr int kWideHoldThreads = 512;     // max threads per CTA of the register-holding cluster kernel
 constexpr int kWideHoldMaxVpt = 8;        // units per thread it is instantiated for: 1, 2, 4, 8 (8: 256 threads)
+constexpr int kWideHoldMaxSlots = 4;      // shared-memory landing slots per CTA of that kernel
 
 // Per-call parameters of a row operation: the normalisations' weight and
 // bias vectors (N stored values each, or null) and eps; zero for the softmax.
