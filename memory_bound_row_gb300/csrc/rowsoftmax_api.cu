@@ -147,7 +147,11 @@ int plan_rows(int dtype, int vec, int64_t M, int64_t units, const rs_options& o,
         if (block % tpr != 0 || block % 32 != 0) return RS_ERR_INVALID_ARG;
         if (block > block_limit) return RS_ERR_NO_PATH;
     } else {
-        int rpc = tpr >= 256 ? 1 : 256 / tpr;
+        // fp32 softmax rows of one or two warps: 128-thread CTAs (measured on
+        // M = 4096, N = 768 .. 2048: +1 % at one warp a row, +6 to +10 % at two,
+        // against 256-thread CTAs); others 256.
+        const int cta = p->op == RS_OP_SOFTMAX && dtype == RS_F32 && vec > 1 && (tpr == 32 || tpr == 64) ? 128 : 256;
+        int rpc = tpr >= cta ? 1 : cta / tpr;
         // Few rows: fewer rows a CTA, so that at least two CTAs reach each SM.
         if (sm_count > 0 && rpc > 1) {
             const int64_t fit = M / (2 * (int64_t)sm_count);

@@ -333,8 +333,10 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             const float c = rescale_off(m, safe_offset(qa)) / qb;
             __syncwarp();
             if (tid == 0 && received) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
-            if constexpr (OP::kMasked) {
-                // past the kept prefix: exactly 0, or NaN when the row keeps nothing
+            if (OP::kMasked && !isfinite(c)) {
+                // a NaN or +inf in the kept prefix, or an empty prefix: past the
+                // prefix exactly 0 (NaN when the row keeps nothing); elsewhere the
+                // fill's exp(-inf) = 0 times a finite c is already 0
                 const int lv = slice_keep(row);
                 const float masked = row_keep(args, row, N) > 0 ? 0.0f : __int_as_float(0x7fffffff);
 #pragma unroll

@@ -303,12 +303,11 @@ struct OpSoftmaxCausal : OpSoftmax {
                                                  float2* part) {
         const int kk = (n + tpr * VEC - 1) / (tpr * VEC);  // slots holding a kept element
         const int width = tpr < 32 ? tpr : 32;
-        float m = kNegInf;
+        float m = kNegInf;  // (the fill past the prefix is -inf: no effect on the max)
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
-            if (k < kk)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
         m = group_max(m, width);
         const float ms = safe_max(m);
         float l = 0.0f;
@@ -343,19 +342,21 @@ struct OpSoftmaxCausal : OpSoftmax {
             const float srow = __shfl_sync(0xffffffffu, group_sum(pl * rescale(pm, mrs), ww), 0);
             c = rescale(m, mrs) / srow;
         }
-        const float masked = n > 0 ? 0.0f : __int_as_float(0x7fffffff);
+        if (isfinite(c)) {
+            // kept slots: exp(x - m) * c, which is 0 for the fill inside the
+            // last kept slot; skipped slots: 0
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            if (k + 1 < kk) {
+            for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] *= c;
-            } else if (k + 1 == kk) {
+                for (int e = 0; e < VEC; ++e) v[k][e] = k < kk ? v[k][e] * c : 0.0f;
+        } else {
+            // a NaN or +inf in the prefix, or an empty prefix (rare): the kept
+            // part as the formula gives it, the rest 0 (NaN without a prefix)
+            const float masked = n > 0 ? 0.0f : __int_as_float(0x7fffffff);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) v[k][e] = (t + k * tpr) * VEC + e < n ? v[k][e] * c : masked;
-            } else {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] = masked;
-            }
         }
     }
 };

@@ -146,8 +146,20 @@ def test_few_rows_are_spread_over_the_sms():
     p = _plan(1024, 1024, rs.RS_F32)
     assert p["grid"] >= 2 * 152 and p["block_threads"] % 32 == 0
     assert p["rows_per_cta"] * p["grid"] >= 1024
-    p = _plan(1 << 16, 1024, rs.RS_F32)  # many rows: full 256-thread CTAs
+    p = _plan(1 << 16, 1024, rs.RS_F32)  # many rows of one warp: full 128-thread CTAs
+    assert p["block_threads"] == 128 and p["threads_per_row"] == 32
+    p = _plan(1 << 16, 512, rs.RS_F32)   # rows narrower than a warp: 256-thread CTAs
     assert p["block_threads"] == 256
+
+
+def test_fp32_rows_of_one_or_two_warps_take_128_thread_ctas():
+    # the N sweep around the one-warp / two-warp switch (M = 4096): 128-thread
+    # CTAs measured faster than 256 for both row widths
+    for N, tpr in [(1024, 32), (1152, 64), (1536, 64), (2048, 64)]:
+        p = _plan(4096, N, rs.RS_F32)
+        assert p["path"] == rs.RS_PATH_ROWS and p["threads_per_row"] == tpr and p["block_threads"] == 128, (N, p)
+    p = _plan(4096, 3072, rs.RS_F32)  # three warps a row: unchanged
+    assert p["threads_per_row"] == 96 and p["block_threads"] == 192
 
 
 def test_ring_plan_is_persistent_and_fits_shared_memory():
