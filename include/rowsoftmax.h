@@ -354,6 +354,37 @@ RS_API int rowsoftmax_split_fwd(const void* in, void* out, int64_t M, int64_t N,
                                 int64_t out_row_stride, int dtype, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream);
 
+/*
+ * rowsoftmax_split_fwd for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is an interface choice of this library.
+ * Some callers may not call cudaMalloc around a softmax: a serving loop whose
+ * device memory is all reserved up front by another allocator (a framework's
+ * caching allocator or memory pool owns it, and memory taken behind its back
+ * can make its own later allocations fail), or code on a latency-critical
+ * path where cudaMalloc, which can synchronise the device, is not allowed.
+ * This entry point needs no workspace argument: the split's pairs go to a
+ * buffer of RS_SPLIT_NOALLOC_MAX_BYTES (1 MiB) that the library defines in
+ * device memory, which every GPU that loads the library holds until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.  The caller still passes `in` and `out`; everything else is as
+ * rowsoftmax_split_fwd.
+ *   - Problems whose workspace (rowsoftmax_split_workspace_size) exceeds
+ *     RS_SPLIT_NOALLOC_MAX_BYTES return RS_ERR_INVALID_ARG before anything
+ *     is launched (up to 65536 rows fit, whatever N).
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *     first call before any stream capture.
+ *   - Every call shares the one buffer, and the buffer keeps the last call's
+ *     contents.  Nothing in it has to start at zero: each call writes every
+ *     pair it later reads.  Calls whose kernels overlap on the GPU (on
+ *     different streams, or from different host threads, without ordering
+ *     between them) race on the buffer and give undefined results: order
+ *     them, for instance on one stream.
+ */
+#define RS_SPLIT_NOALLOC_MAX_BYTES (1u << 20)
+RS_API int rowsoftmax_split_fwd_noalloc(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                                        int64_t out_row_stride, int dtype, cudaStream_t stream);
+
 /* Host-only: fill `dev` for the current CUDA device.  Returns RS_OK or
  * RS_ERR_CUDA. */
 RS_API int rowsoftmax_device_info(rs_device_info* dev);

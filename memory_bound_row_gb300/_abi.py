@@ -52,6 +52,7 @@ EXPORTED = (
     "rowsoftmax_finish_fwd",
     "rowsoftmax_split_workspace_size",
     "rowsoftmax_split_fwd",
+    "rowsoftmax_split_fwd_noalloc",
 )
 
 
@@ -172,6 +173,8 @@ def load() -> ctypes.CDLL:
         lib.rowsoftmax_split_workspace_size.restype = ci
         lib.rowsoftmax_split_fwd.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp, ctypes.c_size_t, vp]
         lib.rowsoftmax_split_fwd.restype = ci
+        lib.rowsoftmax_split_fwd_noalloc.argtypes = [vp, vp, i64, i64, i64, i64, ci, vp]
+        lib.rowsoftmax_split_fwd_noalloc.restype = ci
         _lib = lib
         return lib
 
@@ -311,3 +314,13 @@ def rowsoftmax_split_fwd(in_ptr: int, out_ptr: int, M: int, N: int, in_row_strid
                          dtype: int, workspace_ptr: int | None, workspace_bytes: int, stream: int = 0) -> int:
     return load().rowsoftmax_split_fwd(in_ptr, out_ptr, M, N, in_row_stride, out_row_stride, dtype, workspace_ptr,
                                        workspace_bytes, stream)
+
+
+# Largest workspace rowsoftmax_split_fwd_noalloc serves (RS_SPLIT_NOALLOC_MAX_BYTES).
+RS_SPLIT_NOALLOC_MAX_BYTES = 1 << 20
+
+
+def rowsoftmax_split_fwd_noalloc(in_ptr: int, out_ptr: int, M: int, N: int, in_row_stride: int,
+                                 out_row_stride: int, dtype: int, stream: int = 0) -> int:
+    return load().rowsoftmax_split_fwd_noalloc(in_ptr, out_ptr, M, N, in_row_stride, out_row_stride, dtype,
+                                               stream)

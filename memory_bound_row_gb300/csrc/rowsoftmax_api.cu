@@ -1070,3 +1070,26 @@ int rowsoftmax_split_fwd(const void* in, void* out, int64_t M, int64_t N, int64_
 }
 
 }  // extern "C"
+
+extern "C" {
+
+// rowsoftmax_split_fwd with its workspace in the library's fixed device
+// buffer instead of the caller's (see the header for who needs this).
+int rowsoftmax_split_fwd_noalloc(const void* in, void* out, int64_t M, int64_t N, int64_t in_row_stride,
+                                 int64_t out_row_stride, int dtype, cudaStream_t stream) {
+    size_t need = 0;
+    int rc = rowsoftmax_split_workspace_size(M, N, dtype, &need);
+    if (rc != RS_OK) return rc;
+    if (M == 0 || N == 0) return RS_OK;
+    if (need > (size_t)RS_SPLIT_NOALLOC_MAX_BYTES) return RS_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    const cudaError_t e = rs::split_noalloc_scratch(&scratch);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail_cuda(e);
+    }
+    return rowsoftmax_split_fwd(in, out, M, N, in_row_stride, out_row_stride, dtype, scratch,
+                                (size_t)RS_SPLIT_NOALLOC_MAX_BYTES, stream);
+}
+
+}  // extern "C"

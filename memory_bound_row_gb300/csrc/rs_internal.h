@@ -238,5 +238,8 @@ cudaError_t launch_split_merge(const SplitLaunch& L, const float2* ml, float2* o
 cudaError_t launch_split_finish(const SplitLaunch& L, int dtype, const void* in, void* out, const float2* ml,
                                 int64_t R, int64_t sr, int64_t ss, int64_t M, int N, int64_t ldi, int64_t ldo,
                                 cudaStream_t s);
+// Device address of the fixed scratch buffer (RS_SPLIT_NOALLOC_MAX_BYTES) of
+// rowsoftmax_split_fwd_noalloc on the current device (rs_split.cu).
+cudaError_t split_noalloc_scratch(void** ptr);
 
 }  // namespace rs

@@ -338,7 +338,34 @@ cudaError_t launch_finish_dt(const SplitLaunch& L, const void* in, void* out, co
     return launch_finish_vec<DT, 1>(L, in, out, ml, R, sr, ss, M, N, ldi, ldo, s);
 }
 
+// Scratch of rowsoftmax_split_fwd_noalloc: a fixed device buffer that every
+// GPU which loads this library holds until the process exits, for callers
+// that cannot allocate device memory.
+static __device__ __align__(256) unsigned char g_split_noalloc_scratch[RS_SPLIT_NOALLOC_MAX_BYTES];
+
 }  // namespace
+
+// The device address of the fixed scratch buffer on the current device.  The
+// name of a __device__ array in host code is only a host-side stand-in, so the
+// address is looked up with cudaGetSymbolAddress, once per device, with that
+// device current, and kept.
+cudaError_t split_noalloc_scratch(void** ptr) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_split_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
 
 cudaError_t launch_split_partial(const SplitLaunch& L, int dtype, const void* in, float2* ml, int64_t M, int N,
                                  int64_t ldi, int S, int B, cudaStream_t s) {
