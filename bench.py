@@ -678,6 +678,8 @@ SWEEP_CONFIGS = {
     "rows, one CTA per row group": {"path": 1},
     "rows, persistent": {"path": 1, "grid_limit": -1},
     "ring (bulk copies, persistent)": {"path": 4},
+    "rows, 128-thread CTAs": {"path": 1, "block_threads": 128},
+    "rows, 256-thread CTAs": {"path": 1, "block_threads": 256},
 }
 
 

@@ -33,20 +33,36 @@ namespace rs {
 namespace {
 
 constexpr int kSplitThreads = 256;  // threads per CTA of every kernel here
-constexpr int kPartialBatch = 4;    // units a thread loads before it reduces them
-constexpr int kFinishUnits = 4;     // units a lane of a finishing warp holds
+constexpr int kUnits = 8;           // 16-byte units a thread holds per pass (packed, unpacked one at a time)
 
-// A unit of a block, read so that it stays in L2 for a finish that follows
-// (the read-only path with the default eviction priority); -inf past n.
+// A unit's values as fp32: from the packed 16-byte word `raw` when it is a
+// whole unit of the block (u < full), else read element by element (the
+// ragged last unit), -inf past the block.  The block's reads use the
+// read-only path with the default eviction priority, so that they stay in L2
+// for a finish that follows.
 template <int DT, int VEC>
-__device__ __forceinline__ void load_unit_keep(const typename Traits<DT>::storage* row, int base, int n, float* v) {
+__device__ __forceinline__ void unit_values(const uint4& raw, const typename Traits<DT>::storage* x, int u, int full,
+                                            int len, float* f) {
     using T = Traits<DT>;
-    if (VEC == T::kVec && base + VEC <= n) {
-        T::unpack(__ldg(reinterpret_cast<const uint4*>(row + base)), v);
+    if (VEC == T::kVec && u < full) {
+        T::unpack(raw, f);
     } else {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) v[e] = base + e < n ? load_param1<DT>(row + base + e) : kNegInf;
+        for (int e = 0; e < VEC; ++e) {
+            const int j = u * VEC + e;
+            f[e] = j < len ? load_param1<DT>(x + j) : kNegInf;
+        }
     }
+}
+
+// Tree sum of a unit's values.
+template <int VEC>
+__device__ __forceinline__ float unit_sum(float (&f)[VEC]) {
+#pragma unroll
+    for (int h = VEC / 2; h > 0; h /= 2)
+#pragma unroll
+        for (int e = 0; e < h; ++e) f[e] += f[e + h];
+    return f[0];
 }
 
 // (m, l) absorbs (m2, l2): the online normaliser's step.
@@ -57,56 +73,21 @@ __device__ __forceinline__ void absorb(float& m, float& l, float m2, float l2) {
     m = mn;
 }
 
-// The merged pair of row r from its R pairs at ml[r * sr + s * ss], the same
-// in every lane of the warp.
-__device__ __forceinline__ float2 warp_merged_pair(const float2* ml, int64_t r, int64_t R, int64_t sr, int64_t ss,
-                                                   int lane) {
-    if (R == 1) return ml[r * sr];
-    float m = kNegInf, l = 0.0f;
-    for (int64_t s = lane; s < R; s += 32) {
-        const float2 p = ml[r * sr + s * ss];
-        absorb(m, l, p.x, p.y);
-    }
-    group_merge(m, l, 32);
-    return make_float2(m, l);
-}
-
-// Sum of a batch's values as a tree (short rounding chains).
-template <int B, int VEC>
-__device__ __forceinline__ float batch_sum(const float (&v)[B][VEC]) {
-    float u[B];
-#pragma unroll
-    for (int k = 0; k < B; ++k) {
-        float w[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) w[e] = v[k][e];
-#pragma unroll
-        for (int h = VEC / 2; h > 0; h /= 2)
-#pragma unroll
-            for (int e = 0; e < h; ++e) w[e] += w[e + h];
-        u[k] = w[0];
-    }
-#pragma unroll
-    for (int h = B / 2; h > 0; h /= 2)
-#pragma unroll
-        for (int k = 0; k < h; ++k) u[k] += u[k + h];
-    return u[0];
-}
-
 // One pair per (row, block) item: item q = r * S + b covers columns
-// [b * B, min(N, (b + 1) * B)) of row r and writes ml[q].  TPI threads serve
-// an item (256 / TPI items a CTA at a time); each thread takes units t,
-// t + TPI, ... of the item, kPartialBatch at a time, and keeps a running
-// (m, l): a batch's max raises m (rescaling l once), then the batch's exps,
-// summed as a tree, are added to l with compensated (Kahan) summation, so
-// that a thread's long run of batches adds no more than a few roundings.
+// [b * B, min(N, (b + 1) * B)) of row r and writes ml[q].  A group of TPI
+// threads serves an item (TPI from 4 lanes to 8 warps, by the item's width);
+// each thread takes units t, t + TPI, ... of the item, kUnits at a time: the
+// loads of a pass are issued together and kept packed, then the pass's max
+// raises the running m (rescaling l once) and its exponentials, summed as a
+// tree, are added to l with compensated (Kahan) summation.
 template <int DT, int VEC, int TPI>
 __global__ void __launch_bounds__(kSplitThreads)
 partial_kernel(const void* in_, float2* ml, int64_t M, int N, int64_t ldi, int S, int B) {
     using T = Traits<DT>;
     using St = typename T::storage;
     constexpr int kIpc = kSplitThreads / TPI;  // items a CTA serves at once
-    constexpr int kWpi = TPI / 32;             // warps of an item
+    constexpr int kWpi = TPI / 32;             // warps of an item (0: several items a warp)
+    constexpr int kWidth = TPI < 32 ? TPI : 32;
     const St* in = static_cast<const St*>(in_);
     __shared__ float2 part[2][kSplitThreads / 32];
 
@@ -128,41 +109,49 @@ partial_kernel(const void* in_, float2* ml, int64_t M, int N, int64_t ldi, int S
             const int len = c0 >= N ? 0 : (int)(c0 + B < N ? B : N - c0);
             const St* x = in + r * ldi + c0;
             const int units = (len + VEC - 1) / VEC;
-            for (int u0 = t; u0 < units; u0 += kPartialBatch * TPI) {
-                float v[kPartialBatch][VEC];
+            const int full = VEC == T::kVec ? len / VEC : 0;  // whole 16-byte units
+            for (int u0 = t; u0 < units; u0 += kUnits * TPI) {
+                uint4 raw[kUnits];
 #pragma unroll
-                for (int k = 0; k < kPartialBatch; ++k) {
+                for (int k = 0; k < kUnits; ++k) {
                     const int u = u0 + k * TPI;
-                    if (u < units) {
-                        load_unit_keep<DT, VEC>(x, u * VEC, len, v[k]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) v[k][e] = kNegInf;
-                    }
+                    raw[k] = u < full ? __ldg(reinterpret_cast<const uint4*>(x + u * VEC)) : make_uint4(0, 0, 0, 0);
                 }
                 float bm = kNegInf;
 #pragma unroll
-                for (int k = 0; k < kPartialBatch; ++k)
+                for (int k = 0; k < kUnits; ++k) {
+                    float f[VEC];
+                    unit_values<DT, VEC>(raw[k], x, u0 + k * TPI, full, len, f);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, v[k][e]);
+                    for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, f[e]);
+                }
                 if (bm > m) {
-                    const float f = rescale(m, bm);
-                    l *= f;
-                    comp *= f;
+                    const float fac = rescale(m, bm);
+                    l *= fac;
+                    comp *= fac;
                     m = bm;
                 }
                 const float ms = safe_max(m);
+                float us[kUnits];
 #pragma unroll
-                for (int k = 0; k < kPartialBatch; ++k)
+                for (int k = 0; k < kUnits; ++k) {
+                    float f[VEC];
+                    unit_values<DT, VEC>(raw[k], x, u0 + k * TPI, full, len, f);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) v[k][e] = exp_diff(v[k][e], ms);
-                const float y = batch_sum<kPartialBatch, VEC>(v) - comp;
+                    for (int e = 0; e < VEC; ++e) f[e] = exp_diff(f[e], ms);
+                    us[k] = unit_sum<VEC>(f);
+                }
+#pragma unroll
+                for (int h = kUnits / 2; h > 0; h /= 2)
+#pragma unroll
+                    for (int k = 0; k < h; ++k) us[k] += us[k + h];
+                const float y = us[0] - comp;
                 const float sum = l + y;
                 comp = (sum - l) - y;
                 l = sum;
             }
         }
-        group_merge(m, l, 32);
+        group_merge(m, l, kWidth);
         if constexpr (kWpi > 1) {
             float2* p = part[it & 1];
             if (lane == 0) p[warp] = make_float2(m, l);
@@ -215,49 +204,77 @@ merge_kernel(const float2* ml, float2* out, int64_t R, int64_t sr, int64_t ss, i
     allow_next_grid();
 }
 
-// y = exp(x - m) / l.  A warp item is 32 * kFinishUnits consecutive units of
-// one row (lane j holds units j, j + 32, ...); every warp merges its row's R
-// pairs itself (shuffles, no CTA barrier).
-template <int DT, int VEC>
+// y = exp(x - m) / l.  A group of G lanes (4 to 32, by the row's width)
+// serves one item, G * kUnits consecutive units of one row (lane j of the
+// group holds units j, j + G, ...); the group merges its row's R pairs itself
+// (G-lane butterflies, no CTA barrier), loads its units together, keeps them
+// packed, and scales and stores them one at a time.
+template <int DT, int VEC, int G>
 __global__ void __launch_bounds__(kSplitThreads)
 finish_kernel(const void* in_, void* out_, const float2* ml, int64_t R, int64_t sr, int64_t ss, int64_t M, int N,
               int64_t ldi, int64_t ldo) {
     using T = Traits<DT>;
     using St = typename T::storage;
+    constexpr int kGpw = 32 / G;  // groups a warp
     const St* in = static_cast<const St*>(in_);
     St* out = static_cast<St*>(out_);
     const int lane = threadIdx.x & 31;
+    const int t = lane % G;
     const int upr = (N + VEC - 1) / VEC;
-    const int cpr = (upr + 32 * kFinishUnits - 1) / (32 * kFinishUnits);  // warp items a row
+    const int full = VEC == T::kVec ? N / VEC : 0;
+    const int cpr = (upr + G * kUnits - 1) / (G * kUnits);  // items a row
     const int64_t items = M * (int64_t)cpr;
     const int64_t warps = (int64_t)gridDim.x * (kSplitThreads / 32);
     wait_prior_grid();
-    for (int64_t w = (int64_t)blockIdx.x * (kSplitThreads / 32) + (threadIdx.x >> 5); w < items; w += warps) {
-        const int64_t r = w / cpr;
-        const int c = (int)(w - r * cpr);
-        const float2 p = warp_merged_pair(ml, r, R, sr, ss, lane);
-        const float ms = safe_max(p.x);
-        const float inv = 1.0f / p.y;
+    for (int64_t wbase = ((int64_t)blockIdx.x * (kSplitThreads / 32) + (threadIdx.x >> 5)) * kGpw; wbase < items;
+         wbase += warps * kGpw) {
+        const int64_t gi = wbase + lane / G;
+        const bool active = gi < items;
+        const int64_t r = active ? gi / cpr : 0;
+        const int c = active ? (int)(gi - r * cpr) : 0;
+        float m = kNegInf, l = 0.0f;
+        if (R == 1) {
+            if (active) {
+                const float2 p = ml[r * sr];
+                m = p.x;
+                l = p.y;
+            }
+        } else {
+            if (active)
+                for (int64_t s = t; s < R; s += G) {
+                    const float2 p = ml[r * sr + s * ss];
+                    absorb(m, l, p.x, p.y);
+                }
+            group_merge(m, l, G);
+        }
+        const float ms = safe_max(m);
+        const float inv = 1.0f / l;
         const St* x = in + r * ldi;
         St* y = out + r * ldo;
-        const int ub = c * 32 * kFinishUnits + lane;
-        float v[kFinishUnits][VEC];
+        const int ub = c * G * kUnits + t;
+        uint4 raw[kUnits];
 #pragma unroll
-        for (int k = 0; k < kFinishUnits; ++k) {
-            const int u = ub + k * 32;
-            if (u < upr) {
-                load_unit<DT, VEC>(x, u * VEC, N, v[k]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] = kNegInf;
-            }
+        for (int k = 0; k < kUnits; ++k) {
+            const int u = ub + k * G;
+            raw[k] = active && u < full ? __ldcs(reinterpret_cast<const uint4*>(x + u * VEC)) : make_uint4(0, 0, 0, 0);
         }
+        if (!active) continue;
 #pragma unroll
-        for (int k = 0; k < kFinishUnits; ++k) {
+        for (int k = 0; k < kUnits; ++k) {
+            const int u = ub + k * G;
+            if (u >= upr) break;
+            float f[VEC];
+            if (VEC == T::kVec && u < full) {
+                T::unpack(raw[k], f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] = exp_diff(v[k][e], ms) * inv;
-            const int u = ub + k * 32;
-            if (u < upr) store_unit<DT, VEC>(y, u * VEC, N, v[k]);
+                for (int e = 0; e < VEC; ++e) f[e] = exp_diff(f[e], ms) * inv;
+                __stcs(reinterpret_cast<uint4*>(y + u * VEC), T::pack(f));
+            } else {
+                load_unit<DT, VEC>(x, u * VEC, N, f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) f[e] = exp_diff(f[e], ms) * inv;
+                store_unit<DT, VEC>(y, u * VEC, N, f);
+            }
         }
     }
     allow_next_grid();
@@ -293,26 +310,28 @@ unsigned grid_of(K kern, int64_t work, int sm_count) {
     return (unsigned)(work < cap ? (work < 1 ? 1 : work) : cap);
 }
 
+template <int DT, int VEC, int TPI>
+cudaError_t launch_partial_one(const SplitLaunch& L, const void* in, float2* ml, int64_t M, int N, int64_t ldi, int S,
+                               int B, cudaStream_t s) {
+    constexpr int kIpc = kSplitThreads / TPI;
+    const int64_t items = M * (int64_t)S;
+    return launch_kernel(partial_kernel<DT, VEC, TPI>, grid_of(partial_kernel<DT, VEC, TPI>, (items + kIpc - 1) / kIpc,
+                                                               L.sm_count),
+                         kSplitThreads, 0, s, 0, L.strict, in, ml, M, N, ldi, S, B);
+}
+
+// Threads an item: enough for one pass of kUnits units a thread, 4 to 256.
 template <int DT, int VEC>
 cudaError_t launch_partial_vec(const SplitLaunch& L, const void* in, float2* ml, int64_t M, int N, int64_t ldi, int S,
                                int B, cudaStream_t s) {
     const int units = (B + VEC - 1) / VEC;
-    const int64_t items = M * (int64_t)S;
-    if (units <= 256) {
-        return launch_kernel(partial_kernel<DT, VEC, 32>, grid_of(partial_kernel<DT, VEC, 32>, (items + 7) / 8, L.sm_count),
-                             kSplitThreads, 0, s, 0, L.strict, in, ml, M, N, ldi, S, B);
-    }
-    if (units <= 512) {
-        return launch_kernel(partial_kernel<DT, VEC, 64>, grid_of(partial_kernel<DT, VEC, 64>, (items + 3) / 4, L.sm_count),
-                             kSplitThreads, 0, s, 0, L.strict, in, ml, M, N, ldi, S, B);
-    }
-    if (units <= 1024) {
-        return launch_kernel(partial_kernel<DT, VEC, 128>, grid_of(partial_kernel<DT, VEC, 128>, (items + 1) / 2, L.sm_count),
-                             kSplitThreads, 0, s, 0, L.strict, in, ml, M, N, ldi, S, B);
-    }
-    return launch_kernel(partial_kernel<DT, VEC, 256>, grid_of(partial_kernel<DT, VEC, 256>, items, L.sm_count),
-                         kSplitThreads, 0, s,
-                         0, L.strict, in, ml, M, N, ldi, S, B);
+    if (units <= 4 * kUnits) return launch_partial_one<DT, VEC, 4>(L, in, ml, M, N, ldi, S, B, s);
+    if (units <= 8 * kUnits) return launch_partial_one<DT, VEC, 8>(L, in, ml, M, N, ldi, S, B, s);
+    if (units <= 16 * kUnits) return launch_partial_one<DT, VEC, 16>(L, in, ml, M, N, ldi, S, B, s);
+    if (units <= 32 * kUnits) return launch_partial_one<DT, VEC, 32>(L, in, ml, M, N, ldi, S, B, s);
+    if (units <= 64 * kUnits) return launch_partial_one<DT, VEC, 64>(L, in, ml, M, N, ldi, S, B, s);
+    if (units <= 128 * kUnits) return launch_partial_one<DT, VEC, 128>(L, in, ml, M, N, ldi, S, B, s);
+    return launch_partial_one<DT, VEC, 256>(L, in, ml, M, N, ldi, S, B, s);
 }
 
 template <int DT>
@@ -322,13 +341,26 @@ cudaError_t launch_partial_dt(const SplitLaunch& L, const void* in, float2* ml, 
     return launch_partial_vec<DT, 1>(L, in, ml, M, N, ldi, S, B, s);
 }
 
+template <int DT, int VEC, int G>
+cudaError_t launch_finish_one(const SplitLaunch& L, const void* in, void* out, const float2* ml, int64_t R, int64_t sr,
+                              int64_t ss, int64_t M, int N, int64_t ldi, int64_t ldo, cudaStream_t s) {
+    const int64_t upr = (N + VEC - 1) / VEC;
+    const int64_t items = M * ((upr + G * kUnits - 1) / (G * kUnits));
+    const int64_t per_cta = (kSplitThreads / 32) * (32 / G);
+    return launch_kernel(finish_kernel<DT, VEC, G>,
+                         grid_of(finish_kernel<DT, VEC, G>, (items + per_cta - 1) / per_cta, L.sm_count),
+                         kSplitThreads, 0, s, 0, L.strict, in, out, ml, R, sr, ss, M, N, ldi, ldo);
+}
+
+// Lanes an item: enough for one pass of kUnits units a lane over the row, 4 to 32.
 template <int DT, int VEC>
 cudaError_t launch_finish_vec(const SplitLaunch& L, const void* in, void* out, const float2* ml, int64_t R,
                               int64_t sr, int64_t ss, int64_t M, int N, int64_t ldi, int64_t ldo, cudaStream_t s) {
     const int64_t upr = (N + VEC - 1) / VEC;
-    const int64_t items = M * ((upr + 32 * kFinishUnits - 1) / (32 * kFinishUnits));
-    return launch_kernel(finish_kernel<DT, VEC>, grid_of(finish_kernel<DT, VEC>, (items + 7) / 8, L.sm_count),
-                         kSplitThreads, 0, s, 0, L.strict, in, out, ml, R, sr, ss, M, N, ldi, ldo);
+    if (upr <= 4 * kUnits) return launch_finish_one<DT, VEC, 4>(L, in, out, ml, R, sr, ss, M, N, ldi, ldo, s);
+    if (upr <= 8 * kUnits) return launch_finish_one<DT, VEC, 8>(L, in, out, ml, R, sr, ss, M, N, ldi, ldo, s);
+    if (upr <= 16 * kUnits) return launch_finish_one<DT, VEC, 16>(L, in, out, ml, R, sr, ss, M, N, ldi, ldo, s);
+    return launch_finish_one<DT, VEC, 32>(L, in, out, ml, R, sr, ss, M, N, ldi, ldo, s);
 }
 
 template <int DT>
