@@ -45,12 +45,18 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CSRC = os.path.join(ROOT, "memory_bound_row_gb300", "csrc")
 
 
+# Sources outside the kernels the benchmark lines time (the split-row kernels
+# have their own translation unit and their own --split measurements).
+TRAFFIC_HASH_EXCLUDES = ("rs_split.cu",)
+
+
 def kernel_source_hash() -> str:
-    """Hash of every CUDA/C++ source of the library: a committed ncu traffic
-    figure is only reported while the sources it was taken on are unchanged."""
+    """Hash of the CUDA/C++ sources of the library behind the benchmark lines
+    (every source but TRAFFIC_HASH_EXCLUDES): a committed ncu traffic figure is
+    only reported while the sources it was taken on are unchanged."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f.endswith((".cu", ".cuh", ".h")) and f not in TRAFFIC_HASH_EXCLUDES:
             with open(os.path.join(CSRC, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -923,7 +929,8 @@ def run_split(args):
     (2) the two steps of the vocabulary-parallel softmax on the bf16 causal
     scores split into two column shards of 1024: rowsoftmax_partial_fwd on a
     shard (bytes: its elements read, 8 a row written) and rowsoftmax_finish_fwd
-    with both shards' pairs (its elements read and written, the pairs read).
+    with both shards' pairs (its elements read and written, the pairs read) or
+    with the merged pairs, and rowsoftmax_fwd on the same strided elements.
     Every configuration is first checked against rowsoftmax_fwd on the same
     input (max |difference| within 2^-7 for 16-bit, 1e-6 for fp32); timings
     are graph-replayed launches over rotating buffers (more than 4x L2
@@ -1011,8 +1018,24 @@ def run_split(args):
         if r != rs.RS_OK:
             raise rs.RowSoftmaxError(r)
 
+    merged = rs.softmax_merge(pairs)
+    torch.cuda.synchronize()
+
+    def finish1(k):
+        r = lib.rowsoftmax_finish_fwd(xp[k % 2].data_ptr(), y[:, (k % 2) * half:].data_ptr(), merged.data_ptr(), 1,
+                                      M, half, N, N, code, h)
+        if r != rs.RS_OK:
+            raise rs.RowSoftmaxError(r)
+
+    def whole(k):  # the row softmax of the same strided elements, for comparison
+        r = lib.rowsoftmax_fwd(xp[k % 2].data_ptr(), y[:, (k % 2) * half:].data_ptr(), M, half, N, N, code, h)
+        if r != rs.RS_OK:
+            raise rs.RowSoftmaxError(r)
+
     for name, fn, nbytes in (("rowsoftmax_partial_fwd", partial, M * half * 2 + M * 8),
-                             ("rowsoftmax_finish_fwd (R = 2)", finish, M * half * 4 + 2 * M * 8)):
+                             ("rowsoftmax_finish_fwd (R = 2)", finish, M * half * 4 + 2 * M * 8),
+                             ("rowsoftmax_finish_fwd (R = 1, merged pairs)", finish1, M * half * 4 + M * 8),
+                             ("rowsoftmax_fwd on the same shard", whole, M * half * 4)):
         ms = graph_ms(fn, steps, stream)
         gbs = nbytes / (ms * 1e-3) / 1e9
         print(json.dumps({"split": "vocabulary-parallel steps, one of two column shards", "M": M, "N_shard": half,
