@@ -23,6 +23,9 @@
 // exponential the hardware base-2 one on (x - m) log2 e.
 #include <cuda_runtime.h>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include <mutex>
 
 #include "rs_common.cuh"
@@ -52,6 +55,24 @@ __device__ __forceinline__ void unit_values(const uint4& raw, const typename Tra
             const int j = u * VEC + e;
             f[e] = j < len ? load_param1<DT>(x + j) : kNegInf;
         }
+    }
+}
+
+// -inf in both halves of a packed pair of 16-bit values.
+template <int DT>
+constexpr uint32_t neg_inf_pair() { return DT == RS_BF16 ? 0xFF80FF80u : 0xFC00FC00u; }
+
+// Elementwise max of two packed pairs of 16-bit values (a NaN loses to the
+// other operand, as in fmaxf).
+template <int DT>
+__device__ __forceinline__ uint32_t hmax_pair(uint32_t a, uint32_t b) {
+    if constexpr (DT == RS_BF16) {
+        const __nv_bfloat162 r =
+            __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    } else {
+        const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
     }
 }
 
@@ -110,20 +131,49 @@ partial_kernel(const void* in_, float2* ml, int64_t M, int N, int64_t ldi, int S
             const St* x = in + r * ldi + c0;
             const int units = (len + VEC - 1) / VEC;
             const int full = VEC == T::kVec ? len / VEC : 0;  // whole 16-byte units
+            constexpr bool kPacked = VEC == T::kVec && DT != RS_F32;  // 16-bit words: the max on packed pairs
+            constexpr uint32_t kFillWord = kPacked ? neg_inf_pair<DT>() : 0u;
             for (int u0 = t; u0 < units; u0 += kUnits * TPI) {
                 uint4 raw[kUnits];
 #pragma unroll
                 for (int k = 0; k < kUnits; ++k) {
                     const int u = u0 + k * TPI;
-                    raw[k] = u < full ? __ldg(reinterpret_cast<const uint4*>(x + u * VEC)) : make_uint4(0, 0, 0, 0);
+                    raw[k] = u < full ? __ldg(reinterpret_cast<const uint4*>(x + u * VEC))
+                                      : make_uint4(kFillWord, kFillWord, kFillWord, kFillWord);
                 }
                 float bm = kNegInf;
+                if constexpr (kPacked) {
+                    // whole units on packed pairs (the others hold -inf), then the
+                    // item's ragged last unit, if this thread has it, element by element
+                    uint32_t acc = neg_inf_pair<DT>();
 #pragma unroll
-                for (int k = 0; k < kUnits; ++k) {
-                    float f[VEC];
-                    unit_values<DT, VEC>(raw[k], x, u0 + k * TPI, full, len, f);
+                    for (int k = 0; k < kUnits; ++k) {
+                        acc = hmax_pair<DT>(acc, raw[k].x);
+                        acc = hmax_pair<DT>(acc, raw[k].y);
+                        acc = hmax_pair<DT>(acc, raw[k].z);
+                        acc = hmax_pair<DT>(acc, raw[k].w);
+                    }
+                    float two[2];
+                    T::unpack2(acc, two);
+                    bm = fmaxf(two[0], two[1]);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, f[e]);
+                    for (int k = 0; k < kUnits; ++k) {
+                        const int u = u0 + k * TPI;
+                        if (u >= full && u < units) {
+                            float f[VEC];
+                            unit_values<DT, VEC>(raw[k], x, u, full, len, f);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, f[e]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kUnits; ++k) {
+                        float f[VEC];
+                        unit_values<DT, VEC>(raw[k], x, u0 + k * TPI, full, len, f);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) bm = fmaxf(bm, f[e]);
+                    }
                 }
                 if (bm > m) {
                     const float fac = rescale(m, bm);
