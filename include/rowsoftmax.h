@@ -105,8 +105,12 @@ typedef enum {
 typedef enum {
     RS_RING_AUTO = 0,
     RS_RING_REGISTERS = 1,  /* fp32 copies in registers: one exp per element */
-    RS_RING_REREAD = 2      /* re-read the staged row from shared memory in each pass: two exps per
+    RS_RING_REREAD = 2,     /* re-read the staged row from shared memory in each pass: two exps per
                                element, far fewer registers, more resident warps */
+    RS_RING_THREAD_COPIES = 3  /* the causal softmax on 16-bit rows (the default there): each thread
+                                  copies the units of its row that hold kept elements into the stage
+                                  with 16-byte asynchronous copies and holds them in registers as fp32;
+                                  the masked part is never copied; 2 or 3 stages */
 } rs_ring_values;
 
 /*
@@ -148,7 +152,7 @@ typedef struct {
     int block_threads;
     int cluster_size;     /* CTAs per row (1 for RS_PATH_ROWS / RS_PATH_RING) */
     int stages;           /* RS_PATH_CLUSTER: bulk-copy stages per CTA; RS_PATH_RING: ring depth */
-    int ring_values;      /* RS_PATH_RING: RS_RING_REGISTERS or RS_RING_REREAD */
+    int ring_values;      /* RS_PATH_RING: RS_RING_REGISTERS, RS_RING_REREAD or RS_RING_THREAD_COPIES */
     int64_t chunk_elems;  /* RS_PATH_CLUSTER / RS_PATH_STREAM: row slice per CTA */
     int64_t grid;         /* CTAs launched */
     size_t smem_bytes;    /* dynamic shared memory per CTA */
@@ -211,9 +215,10 @@ RS_API int rowsoftmax_plan(const void* in, const void* out, int64_t M, int64_t N
  *
  * elements: y[r][j] is the softmax of those L_r values for j < L_r and exactly
  * 0 for j >= L_r.  Elements at j >= L_r are never used (they may hold
- * anything, NaN included): the register rows and the clusters do not load
- * them, the ring stages whole rows and ignores them; every output element is
- * written.  For attention
+ * anything, NaN included): the register rows, the ring on 16-bit rows
+ * (RS_RING_THREAD_COPIES, the default there) and the clusters do not load
+ * them, the bulk-copy ring (forced RS_RING_REGISTERS) stages whole rows and
+ * ignores them; every output element is written.  For attention
  * scores [B, H, S_q, S_k] stored as (B*H*S_q) x S_k rows: period = S_q and
  * diag_offset = S_k - S_q.  L_r == 0 is an all -inf row: NaN.  Data model,
  * ownership, asynchrony and errors are those of rowsoftmax_fwd; period < 1 or

@@ -35,6 +35,7 @@ from ._abi import (  # noqa: F401
     RS_RING_AUTO,
     RS_RING_REGISTERS,
     RS_RING_REREAD,
+    RS_RING_THREAD_COPIES,
     rowsoftmax_causal_fwd,
     rowsoftmax_causal_fwd_ex,
     rowsoftmax_causal_plan,

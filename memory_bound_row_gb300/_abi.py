@@ -25,7 +25,7 @@ RS_ERR_NOT_DEVICE_MEMORY = 5
 RS_ERR_NO_PATH = 6
 # rs_path
 RS_PATH_AUTO, RS_PATH_ROWS, RS_PATH_CLUSTER, RS_PATH_STREAM, RS_PATH_RING = 0, 1, 2, 3, 4
-RS_RING_AUTO, RS_RING_REGISTERS, RS_RING_REREAD = 0, 1, 2
+RS_RING_AUTO, RS_RING_REGISTERS, RS_RING_REREAD, RS_RING_THREAD_COPIES = 0, 1, 2, 3
 # rs_op
 RS_OP_SOFTMAX, RS_OP_RMSNORM, RS_OP_LAYERNORM = 0, 1, 2
 PATH_NAMES = {RS_PATH_AUTO: "auto", RS_PATH_ROWS: "rows", RS_PATH_CLUSTER: "cluster", RS_PATH_STREAM: "stream",

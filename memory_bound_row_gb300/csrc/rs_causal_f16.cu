@@ -1,8 +1,11 @@
 // Softmax under a causal mask (rowsoftmax_causal_fwd) for f16 storage: the
 // register rows, the ring and the register-holding clusters instantiated
-// with OpSoftmaxCausal, which copy and read only each row's kept prefix.
+// with OpSoftmaxCausal, which copy and read only each row's kept prefix (the
+// ring by per-thread asynchronous copies, rs_ring_cp.cuh; the bulk-copy ring
+// when forced, which stages whole rows).
 #include "rs_hold.cuh"
 #include "rs_ring.cuh"
+#include "rs_ring_cp.cuh"
 #include "rs_rows.cuh"
 
 namespace rs {
@@ -19,6 +22,8 @@ cudaError_t launch_causal_f16(const rs_plan& p, const void* in, void* out, int64
             return cudaErrorInvalidConfiguration;
         case RS_PATH_RING:
             if (p.vec_elems != KV) return cudaErrorInvalidConfiguration;
+            if (p.ring_values == RS_RING_THREAD_COPIES)
+                return RingCpDispatch<RS_F16, OpSoftmaxCausal, RS_VPT_VEC_16>::go(p, in, out, M, N, ldi, ldo, s, a);
             return RingDispatch<RS_F16, OpSoftmaxCausal, RS_VPT_VEC_16>::go(p, in, out, M, N, ldi, ldo, s, a);
         case RS_PATH_CLUSTER:
             if (p.ring_values != RS_RING_REGISTERS) return cudaErrorInvalidConfiguration;

@@ -19,6 +19,7 @@ cudaError_t launch_causal_f32(const rs_plan& p, const void* in, void* out, int64
             return cudaErrorInvalidConfiguration;
         case RS_PATH_RING:
             if (p.vec_elems != KV) return cudaErrorInvalidConfiguration;
+            if (p.ring_values == RS_RING_THREAD_COPIES) return cudaErrorInvalidConfiguration;
             return RingDispatch<RS_F32, OpSoftmaxCausal, RS_VPT_VEC_F32>::go(p, in, out, M, N, ldi, ldo, s, a);
         case RS_PATH_CLUSTER:
             if (p.ring_values != RS_RING_REGISTERS) return cudaErrorInvalidConfiguration;

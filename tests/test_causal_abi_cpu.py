@@ -81,3 +81,24 @@ def test_remainder_by_direct_computation():
         for n in [0, 1, d - 1, d, d + 1, (1 << 32) - 1] + [rng.randrange(0, 1 << 32) for _ in range(50)]:
             if 0 <= n < (1 << 32):
                 assert (((c * n) & m64) * d) >> 64 == n % d, (n, d)
+
+
+def test_the_masked_ring_copies_only_the_kept_units_on_16bit_rows():
+    # bf16 causal scores: the ring with per-thread copies of the kept units by
+    # default; the bulk-copy ring (whole rows) when forced; neither elsewhere
+    rc, p = _plan(1 << 20, 2048, rs.RS_BF16, 2048)
+    assert rc == rs.RS_OK and p["path"] == rs.RS_PATH_RING and p["ring_values"] == rs.RS_RING_THREAD_COPIES
+    assert p["stages"] == 2 and p["smem_bytes"] == 2 * p["rows_per_cta"] * 2048 * 2
+    rc, p = _plan(1 << 20, 2048, rs.RS_BF16, 2048, opts={"path": rs.RS_PATH_RING, "ring_values": rs.RS_RING_REGISTERS})
+    assert rc == rs.RS_OK and p["ring_values"] == rs.RS_RING_REGISTERS
+    rc, p = _plan(4096, 2048, rs.RS_F16, 2048, opts={"path": rs.RS_PATH_RING, "stages": 3})
+    assert rc == rs.RS_OK and p["ring_values"] == rs.RS_RING_THREAD_COPIES and p["stages"] == 3
+    rc, p = _plan(4096, 2048, rs.RS_F16, 2048, opts={"path": rs.RS_PATH_RING, "stages": 4})  # copies: 2 or 3
+    assert rc == rs.RS_OK and p["ring_values"] == rs.RS_RING_REGISTERS
+    copies = {"ring_values": rs.RS_RING_THREAD_COPIES}
+    assert _plan(4096, 2048, rs.RS_F16, 2048, opts=dict(copies, path=rs.RS_PATH_RING, stages=4))[0] == rs.RS_ERR_NO_PATH
+    assert _plan(4096, 2048, rs.RS_F32, 2048, opts=dict(copies, path=rs.RS_PATH_RING))[0] == rs.RS_ERR_NO_PATH
+    assert _plan(64, 131072, rs.RS_F16, 64, opts=dict(copies, path=rs.RS_PATH_CLUSTER))[0] == rs.RS_ERR_NO_PATH
+    rc, _ = rs.rowsoftmax_plan(A, OUT, 4096, 2048, 2048, 2048, rs.RS_BF16, dict(copies, path=rs.RS_PATH_RING),
+                               gb300())
+    assert rc == rs.RS_ERR_NO_PATH  # the unmasked softmax stages whole rows

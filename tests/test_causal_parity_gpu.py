@@ -94,7 +94,9 @@ def _servable(x, period, offset, options):
 PATHS = {
     "auto": None,
     "rows": {"path": rs.RS_PATH_ROWS},
-    "ring": {"path": rs.RS_PATH_RING},
+    "ring": {"path": rs.RS_PATH_RING},  # 16-bit rows: per-thread copies of the kept units
+    "ring bulk": {"path": rs.RS_PATH_RING, "ring_values": rs.RS_RING_REGISTERS},  # whole rows, bulk copies
+    "ring copies 3": {"path": rs.RS_PATH_RING, "ring_values": rs.RS_RING_THREAD_COPIES, "stages": 3},
     "cluster": {"path": rs.RS_PATH_CLUSTER},
     "cluster3": {"path": rs.RS_PATH_CLUSTER, "cluster_size": 3},
 }
@@ -180,7 +182,7 @@ def test_kv_cache_offset_layout():
     compare(y, ref, "f16", "kv-cache layout")
 
 
-@pytest.mark.parametrize("path", ["rows", "ring", "cluster"])
+@pytest.mark.parametrize("path", ["rows", "ring", "ring bulk", "cluster"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_non_finite_values_in_the_kept_prefix(path, dtype):
     # A NaN or +inf inside the kept prefix makes the kept part NaN; the masked
