@@ -223,13 +223,15 @@ def compare_norm(y: torch.Tensor, ref: np.ndarray, x: torch.Tensor, op: str, wei
     return {"max_abs_err": st["max_abs_err"], "max_err_over_tol": st["max_err_over_tol"]}
 
 
-# Statistics of every all-rows check of this session (printed by conftest.py).
-REPORT: list[str] = []
+# Statistics of every all-rows check of this session (printed by conftest.py):
+# (group, line); group "workloads" (the benchmark workloads at full size) is
+# printed last.
+REPORT: list[tuple[str, str]] = []
 
 
 def check_all_rows(kind: str, x: torch.Tensor, y: torch.Tensor, n_cols: int, *, weight=None, bias=None,
                    eps: float = 0.0, period: int = 0, offset: int = 0, what: str = "",
-                   chunk_elems: int = 1 << 26, threads: int = 16) -> dict:
+                   chunk_elems: int = 1 << 26, threads: int = 16, group: str = "other") -> dict:
     """Every row of y (device, M x n_cols view) against the oracle on the same
     rows of x.  kind: "softmax" (softmax tolerances), "prefix" (the softmax
     under a causal mask: row r keeps min(n_cols, max(0, r mod period + 1 +
@@ -294,7 +296,7 @@ def check_all_rows(kind: str, x: torch.Tensor, y: torch.Tensor, n_cols: int, *, 
                 agg["max_abs_err"] = max(agg["max_abs_err"], st["max_abs_err"])
             agg["rows"] += r1 - r0
     assert agg["rows"] == M
-    REPORT.append(f"{what}: all {M} rows x {n_cols} checked against the oracle; "
-                  + ", ".join(f"{k} {v:.3e}" if isinstance(v, float) else f"{k} {v}" for k, v in agg.items()
-                              if k != "rows"))
+    REPORT.append((group, f"{what}: all {M} rows x {n_cols} checked against the oracle; "
+                   + ", ".join(f"{k} {v:.3e}" if isinstance(v, float) else f"{k} {v}" for k, v in agg.items()
+                               if k != "rows")))
     return agg

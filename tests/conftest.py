@@ -16,8 +16,16 @@ def pytest_terminal_summary(terminalreporter):
     # The all-rows parity checks of the full-size workloads record their
     # statistics (max error, row-sum error) here; print them even under -q.
     mod = sys.modules.get("_parity")
-    lines = getattr(mod, "REPORT", None) if mod else None
-    if lines:
-        terminalreporter.write_sep("-", "all-rows parity of the full-size workloads")
-        for line in lines:
+    entries = getattr(mod, "REPORT", None) if mod else None
+    if not entries:
+        return
+    other = [line for group, line in entries if group != "workloads"]
+    workloads = [line for group, line in entries if group == "workloads"]
+    if other:
+        terminalreporter.write_sep("-", "all-rows parity of the other large cases")
+        for line in other:
+            terminalreporter.write_line(line)
+    if workloads:
+        terminalreporter.write_sep("-", "all-rows parity of the benchmark workloads at full size")
+        for line in workloads:
             terminalreporter.write_line(line)

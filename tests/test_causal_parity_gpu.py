@@ -165,7 +165,8 @@ def test_causal_workload_full_size_equals_the_plain_softmax():
     # every row against the prefix oracle, with the masked part made NaN first
     # (the oracle never reads it either)
     _garbage(x, 2048, 0)
-    check_all_rows("prefix", x, masked, w.N, period=2048, offset=0, what="causal softmax bf16 1048576 x 2048")
+    check_all_rows("prefix", x, masked, w.N, period=2048, offset=0, what="causal softmax bf16 1048576 x 2048",
+                   group="workloads")
     again = _run(x, 2048, 0)
     assert torch.equal(plain.view(torch.int16), again.view(torch.int16))
     del x, plain, masked, again

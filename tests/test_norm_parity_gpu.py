@@ -422,7 +422,7 @@ def test_benchmark_shapes_full_size(op, name):
     eps = 1e-6 if op == "rms" else 1e-5
     y = _run(op, x[:, : w.N], wt, bs, eps=eps, out=out[:, : w.N])
     check_all_rows(op, x[:, : w.N], y, w.N, weight=wt, bias=bs if op == "ln" else None, eps=eps,
-                   what=f"{'RMSNorm' if op == 'rms' else 'LayerNorm'} {name}")
+                   what=f"{'RMSNorm' if op == 'rms' else 'LayerNorm'} {name}", group="workloads")
     assert bool(torch.isfinite(y).all())
     if w.ld > w.N:
         assert torch.equal(out[:, w.N:].view(torch.int32), pad_before.view(torch.int32))

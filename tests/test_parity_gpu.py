@@ -308,7 +308,7 @@ def test_benchmark_workloads_full_size(name):
     y = rs.softmax(x[:, : w.N], out=out[:, : w.N])
     torch.cuda.synchronize()
 
-    check_all_rows("softmax", x[:, : w.N], y, w.N, what=f"softmax {name}")
+    check_all_rows("softmax", x[:, : w.N], y, w.N, what=f"softmax {name}", group="workloads")
 
     assert bool(torch.isfinite(y).all())
     assert float(y.min()) >= 0.0 and float(y.max()) <= 1.0
