@@ -246,15 +246,19 @@ def run_reference(args, workloads):
         w = op_workload(op, name)
         fmt = w.dtype
         params = host_params(w) if op != "softmax" else None
-        probe_rows = min(w.M, max(cores, 8))
-        xs = W.generate(w, "cpu", 0, probe_rows)
+        # A probe of up to 1024 rows sizes the per-step sample: about a minute of
+        # oracle time for the whole run, at most 65536 rows a step.
+        probe_rows = min(w.M, 1024)
         store = lambda t: t.view(torch.int16).numpy().view(np.uint16) if fmt == "bf16" else t.numpy()
-        x_np = store(xs[:, : w.N].contiguous())
+        x_np = store(W.generate(w, "cpu", 0, probe_rows)[:, : w.N].contiguous())
+        oracle_op(op, x_np[: min(probe_rows, cores)], fmt, w.N, params, cores)  # first call: loads the oracle
         t = time.perf_counter()
         oracle_op(op, x_np, fmt, w.N, params, cores)
         per_row = (time.perf_counter() - t) / probe_rows
         budget = 60.0  # seconds for the whole run
-        rows_per_step = max(1, min(probe_rows, int(budget / max(1, args.steps + args.warmup) / per_row)))
+        rows_per_step = max(1, min(w.M, 65536, int(budget / max(1, args.steps + args.warmup) / per_row)))
+        if rows_per_step > probe_rows:
+            x_np = store(W.generate(w, "cpu", 0, rows_per_step)[:, : w.N].contiguous())
         sample = x_np[:rows_per_step]
         for _ in range(args.warmup):
             oracle_op(op, sample, fmt, w.N, params, cores)
