@@ -199,18 +199,26 @@ __device__ __forceinline__ float ex2_approx(float y) {
 // then scaled into base 2.
 __device__ __forceinline__ float exp_diff(float x, float ms) { return ex2_approx((x - ms) * kLog2e); }
 
-// The register-holding cluster kernel takes exponentials against a set's
-// offset: with m the set's max, o = rn(m * log2 e) and exp(x - m) taken as
-// 2^fma(x, log2 e, -o) -- one FMA and one ex2 an element.  Every value of
-// the set shares the rounding of o, which cancels when the set is
-// normalised, and sets merge with weights 2^(o_i - o) built from the same
-// rounded offsets, so the cancellation survives the merges.  (The row
-// kernels keep 2^((x - m) * log2 e), which measured faster there.)
-__device__ __forceinline__ float safe_offset(float o) { return o == kNegInf ? 0.0f : o; }
-__device__ __forceinline__ float exp_off(float x, float os) { return ex2_approx(fmaf(x, kLog2e, -os)); }
-// Weight of a partial sum taken against offset o when the merged offset is os.
-__device__ __forceinline__ float rescale_off(float o, float os) {
-    return o == kNegInf ? 0.0f : ex2_approx(o - os);
+// Exponentials against a rounded base-2 offset (the register-holding kernels):
+// with m a set's max, o = rn(m log2 e) and exp(x - m) taken as
+// 2^fma(x, log2 e, -o) -- one FMA and one ex2 an element.  The values come
+// out as exp(x - m) 2^r with r = m log2 e - o, the rounding residual of the
+// offset, shared by the set.  The set's sum times 2^-r is its plain sum of
+// exp(x - m), so sets merge as ordinary (m, l) pairs, and with M and L the
+// row's merged pair the set's values scale by exp(m - M) 2^-r / L
+// (rescale_res).  r is at most half a unit in the last place of o, which
+// stays below 1/2 only while |m| < 2^23 (|o| < 2^24); past that (and for an
+// infinite or NaN max) the set takes the difference form exp_diff, r = 0.
+constexpr float kOffsetFormLimit = 8388608.0f;  // 2^23
+__device__ __forceinline__ bool offset_form(float m) { return fabsf(m) < kOffsetFormLimit; }
+__device__ __forceinline__ float exp_off(float x, float o) { return ex2_approx(fmaf(x, kLog2e, -o)); }
+// The offset of a set with max m (offset_form(m) true) and its residual.
+__device__ __forceinline__ float offset_of(float m) { return m * kLog2e; }
+__device__ __forceinline__ float residual_of(float m, float o) { return fmaf(m, kLog2e, -o); }
+// Weight of a set with max m and residual r inside a row whose merged max is
+// ms (safe_max applied): exp(m - ms) 2^-r, 0 for a set with no mass.
+__device__ __forceinline__ float rescale_res(float m, float ms, float r) {
+    return m == kNegInf ? 0.0f : ex2_approx(fmaf(m - ms, kLog2e, -r));
 }
 
 // Weight of a partial sum taken against max m when the merged max is ms.
@@ -239,13 +247,6 @@ __device__ __forceinline__ void group_merge(float& m, float& l, int width) {
     const float mm = group_max(m, width);
     l = group_sum(l * rescale(m, safe_max(mm)), width);
     m = mm;
-}
-
-// group_merge for (offset, l) pairs: o = max_i o_i, l = sum_i l_i 2^(o_i - o).
-__device__ __forceinline__ void group_merge_off(float& o, float& l, int width) {
-    const float oo = group_max(o, width);
-    l = group_sum(l * rescale_off(o, safe_offset(oo)), width);
-    o = oo;
 }
 
 }  // namespace rs

@@ -15,11 +15,14 @@
 // distributed shared memory: every CTA pushes one pair of floats into a slot
 // of every CTA of its cluster (st.async, counted on the receivers' mbarrier)
 // and combines the cluster's pairs itself.  The pair of a slice is
-//   softmax    (o, l): its offset o = rn(m log2 e), m its max, and its sum
-//              of exp(x - m) taken as 2^fma(x, log2 e, -o); pairs merge with
+//   softmax    (m, l): its max and its sum of exp(x - m); pairs merge with
 //              the online normaliser of the mohakchugh.is-a.dev post ("How
-//              Flash Attention Uses Triton") in the base-2 domain:
-//              o = max o_c, l = sum l_c 2^(o_c - o);
+//              Flash Attention Uses Triton"): m = max m_c,
+//              l = sum l_c exp(m_c - m).  Each warp takes its exponentials
+//              as 2^fma(x, log2 e, -o) against its offset o = rn(m_w log2 e)
+//              while |m_w| < 2^23, and folds the offset's rounding residual r
+//              into its sum (times 2^-r) and into its final scale (rescale_res);
+//              past that magnitude it takes exp_diff;
 //   RMSNorm    (sum of x^2, 0): sums add;
 //   LayerNorm  (S_c, Q_c): the slice's sum and its sum of squared deviations
 //              from the slice's own mean mu_c = S_c / n_c; slices combine with
@@ -210,20 +213,33 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
         // This thread's contribution, reduced over the warp.
         float m = kNegInf;  // softmax: the warp's max
         float a0 = 0.0f;    // softmax: l; norms: sum of x^2 or sum of x
+        float res = 0.0f;   // softmax: the residual of the warp's offset
         if constexpr (kSoftmax) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) m = fmaxf(m, v[k][e]);
-            m = group_max(m, 32) * kLog2e;  // from here on the warp's offset
-            const float os = safe_offset(m);
+            m = group_max(m, 32);
+            if (offset_form(m)) {
+                const float o = offset_of(m);
+                res = residual_of(m, o);
 #pragma unroll
-            for (int k = 0; k < VPT; ++k)
+                for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    v[k][e] = exp_off(v[k][e], os);
-                    a0 += v[k][e];
-                }
+                    for (int e = 0; e < VEC; ++e) {
+                        v[k][e] = exp_off(v[k][e], o);
+                        a0 += v[k][e];
+                    }
+            } else {
+                const float ms = safe_max(m);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        v[k][e] = exp_diff(v[k][e], ms);
+                        a0 += v[k][e];
+                    }
+            }
         } else if constexpr (OP::kOp == RS_OP_RMSNORM) {
             a0 = thread_sum<VPT, VEC>(v, [](float acc, float x, int, int) { return fmaf(x, x, acc); });
         } else {
@@ -248,6 +264,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             m = q;
         }
         if constexpr (OP::kOp != RS_OP_LAYERNORM) a0 = group_sum(a0, 32);
+        if constexpr (kSoftmax) a0 *= ex2_approx(-res);  // the warp's plain sum of exp(x - m)
 
         // CTA merge of the warps' partials.  The barrier also ends every read
         // of the slot, which is then handed to the copy of a later row.
@@ -265,7 +282,7 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             pl = q.y;
         }
         if constexpr (kSoftmax) {
-            group_merge_off(pm, pl, pow2_ceil(nwarps));  // lanes 0..nwarps-1 hold the CTA's pair
+            group_merge(pm, pl, pow2_ceil(nwarps));  // lanes 0..nwarps-1 hold the CTA's pair
             pm = __shfl_sync(0xffffffffu, pm, 0);
             pl = __shfl_sync(0xffffffffu, pl, 0);
         } else if constexpr (OP::kOp == RS_OP_RMSNORM) {
@@ -327,10 +344,10 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
             qb = q.y;
         }
         if constexpr (kSoftmax) {
-            group_merge_off(qa, qb, pow2_ceil(cs));
+            group_merge(qa, qb, pow2_ceil(cs));
             qa = __shfl_sync(0xffffffffu, qa, 0);
             qb = __shfl_sync(0xffffffffu, qb, 0);
-            const float c = rescale_off(m, safe_offset(qa)) / qb;
+            const float c = rescale_res(m, safe_max(qa), res) / qb;
             __syncwarp();
             if (tid == 0 && received) mbar_arrive_expect_tx(&recv_bar[rb], pair_bytes);  // re-armed for row it + 2
             if (OP::kMasked && !isfinite(c)) {
