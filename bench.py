@@ -10,7 +10,7 @@ bias for LayerNorm) on the same shapes.  The default workload is the largest
 one, bf16 attention scores [16, 32, 2048, 2048] as 1048576 x 2048 rows
 (8.59 GB moved per step), timed with the plain rowsoftmax_fwd; the line also
 carries, under "all_configs", the device-timed figures of the other four
-workloads from the same run.  Rank 0 prints one JSON line per
+workloads and of rowsoftmax_causal_fwd on the same scores from the same run.  Rank 0 prints one JSON line per
 workload with achieved HBM GB/s (bytes = M * N * (in + out element size)),
 rows/s, the roofline fraction of the kernel against the measured HBM copy
 bandwidth, the end-to-end figure through the C ABI with host buffers, the
@@ -350,7 +350,7 @@ def pick_graph_launches(steps: int, nsets: int, est_ms: float) -> int:
     return max(pref or fit)
 
 
-def measure(args, name, ctx, full: bool):
+def measure(args, name, ctx, full: bool, causal_summary: bool = False):
     """Times K graph-replayed launches of the row operation on workload
     `name`.  Returns the JSON line (rank 0; None elsewhere).  With full=False
     only the device-timed figures are taken (no end-to-end leg, clocks or CPU
@@ -365,7 +365,7 @@ def measure(args, name, ctx, full: bool):
     lib, dev, world, rank, local, peak, peak_src, opts = (ctx[k] for k in (
         "lib", "dev", "world", "rank", "local", "peak", "peak_src", "opts"))
     op = args.op
-    causal = args.causal and full
+    causal = (args.causal and full) or causal_summary
     w = op_workload(op, name)
     if args.rows and full:
         w = W.Workload(w.name, w.dtype, min(args.rows, w.M), w.N, w.ld, w.seed, w.kind,
@@ -592,12 +592,16 @@ def measure(args, name, ctx, full: bool):
                    "min_ms_per_step": round(per_replay[0], 5),
                    "max_ms_per_step": round(per_replay[-1], 5)}
         if not full:
-            line = {"workload": name, "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms_per_step, 5),
+            line = {"workload": name + (" (rowsoftmax_causal_fwd)" if causal else ""), "value": round(value, 2),
+                    "unit": "GB/s", "ms_per_step": round(ms_per_step, 5),
                     "rows_per_s": round(world * w.M / (ms_per_step * 1e-3), 1), "frac": round(achieved / peak, 4),
                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                     "frac_of_same_run_copy": round(achieved / copy_gbs, 4), "same_run_copy_gbs": round(copy_gbs, 1),
                     "kernel": rs.PATH_NAMES[plan["path"]], "bytes_per_step": nbytes, "steps": args.steps,
                     "repeats": repeats}
+            if causal:  # the line's value counts M x N x 4 bytes; the least traffic the mask allows beside it
+                line["min_bytes_per_step"] = min_bytes
+                line["min_bytes_gbs"] = round(job_gbs(world, min_bytes, args.steps, total_ms), 2)
         else:
             line = {
                 "metric": OP_METRIC[op], "value": round(value, 2), "unit": "GB/s",
@@ -673,6 +677,9 @@ def run_ours(args, workloads):
             for other in W.ORDER:
                 if other != name:
                     others.append(measure(args, other, ctx, full=False))
+            if args.op == "softmax" and "causal" in W.WORKLOADS[name].kind:
+                # the mask-aware softmax on the same scores (never reads the masked part)
+                others.append(measure(args, name, ctx, full=False, causal_summary=True))
         line = measure(args, name, ctx, full=True)
         if rank == 0:
             if others:
