@@ -223,6 +223,36 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
         ro.vec_per_thread = 4;
     int rc = plan_rows(dtype, vec, M, units, ro, p, values != RS_RING_REREAD);
     if (rc != RS_OK) return rc;
+    // CTA sizes measured on the ring's 16-bit rows (graph-replayed, 2^18 to
+    // 2^20 rows, against the 256-thread CTAs planned above):
+    //  - softmax rows of one warp at 4 or more units a thread: 512 threads,
+    //    one CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048
+    //    +3.9 %, bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %;
+    //    softmax rows of 4 warps +0.3 %, of 8 warps -2 %: unchanged);
+    //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %);
+    //  - RMSNorm rows of 4 warps at 4 units a thread: 128 threads, one row a
+    //    CTA (bf16 4096 +6.1 %; its rows of one warp +0.7 % at 512, of 8
+    //    warps -7 % at 512: unchanged).
+    // Only with at least 64 rows an SM, so that every CTA loops over stages.
+    if (dtype != RS_F32 && values != RS_RING_REREAD && !o.block_threads && !o.threads_per_row &&
+        !o.vec_per_thread && M >= (int64_t)64 * dev.sm_count) {
+        const int tpr = p->threads_per_row, vpt = p->vec_per_thread;
+        int want = 0;
+        if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4)
+            want = 512;
+        else if (p->op == RS_OP_LAYERNORM && tpr == 32)
+            want = 128;
+        else if (p->op == RS_OP_RMSNORM && tpr == 128 && vpt <= 4)
+            want = 128;
+        if (want && want != p->block_threads) {
+            const rs_plan keep = *p;
+            rs_options rb = ro;
+            rb.block_threads = want;
+            if (plan_rows(dtype, vec, M, units, rb, p, true) != RS_OK || p->threads_per_row != tpr ||
+                p->vec_per_thread != vpt)
+                *p = keep;
+        }
+    }
     p->path = RS_PATH_RING;  // (the LayerNorm kind depends on the path)
     const int lkind = p->op == RS_OP_LAYERNORM ? rs::layernorm_merge_kind(*p, N, vec) : 0;
     const bool held = lkind == 3 || lkind == 4 || (p->op == RS_OP_RMSNORM && rs::rmsnorm_ring_held(*p, vec));

@@ -322,3 +322,24 @@ def test_ctypes_structs_match_the_c_header(cls):
     size, offsets = got
     assert ctypes.sizeof(cls) == size
     assert [getattr(cls, f).offset for f in fields] == offsets
+
+
+def test_ring_cta_sizes_for_16bit_rows():
+    # Measured CTA sizes of the ring on 16-bit rows (graph-replayed, 2^18 to
+    # 2^20 rows): softmax rows of one warp at 4 or more units a thread take
+    # 512-thread CTAs (one an SM, 16 rows a stage; bf16 2048 +3.3 %, bf16 1024
+    # +6.1 %), LayerNorm rows of one warp 128 threads; rows of 8 warps and
+    # problems of fewer than 64 rows an SM keep 256.
+    for N, vpt, per_sm in [(1024, 4, 2), (2048, 8, 1)]:  # 64 or 128 registers a thread
+        for dt in (rs.RS_BF16, rs.RS_F16):
+            p = _plan(1 << 20, N, dt)
+            assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"]) == (32, vpt)
+            assert p["block_threads"] == 512 and p["rows_per_cta"] == 16 and p["grid"] == per_sm * 152, (N, dt)
+    assert _plan(1 << 20, 2048, rs.RS_BF16, opts={"block_threads": 256})["block_threads"] == 256
+    assert _plan(64 * 152 - 1, 2048, rs.RS_BF16)["block_threads"] == 256  # few rows: unchanged
+    p = _plan(32768, 8192, rs.RS_BF16)
+    assert p["threads_per_row"] == 256 and p["block_threads"] == 256
+    rc, p = rs.rownorm_plan(rs.RS_OP_LAYERNORM, A, A + (1 << 40), A, A, 1 << 20, 2048, 2048, 2048, 1e-5,
+                            rs.RS_BF16, None, gb300())
+    assert rc == rs.RS_OK and p["path"] == rs.RS_PATH_RING and p["threads_per_row"] == 32
+    assert p["block_threads"] == 128

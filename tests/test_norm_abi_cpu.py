@@ -120,7 +120,7 @@ def test_layernorm_ring_stages_its_vectors_in_shared_memory():
     p = _plan(rs.RS_OP_LAYERNORM, 1 << 20, N, rs.RS_BF16, ld=2048, w=None, b=B)
     assert p["smem_bytes"] == stage * p["stages"] + 2048 * 2
     p = _plan(rs.RS_OP_RMSNORM, 1 << 20, N, rs.RS_BF16, ld=2048)
-    assert p["smem_bytes"] == stage * p["stages"]
+    assert p["smem_bytes"] == (N // 8) * 16 * p["rows_per_cta"] * p["stages"]
 
 
 @pytest.mark.parametrize("dtype", [rs.RS_F16, rs.RS_BF16])
@@ -138,13 +138,15 @@ def test_layernorm_rows_of_4_or_8_warps_hold_their_vectors_in_registers(dtype):
     # and a ragged row of the same size keeps the staged vectors
     p = _plan(rs.RS_OP_LAYERNORM, 32768, 2048, dtype, b=B)
     assert p["threads_per_row"] <= 32
-    # RMSNorm rows of 4 or more warps at 4 units a thread hold their weight too
-    # (2 CTAs an SM); the 12288-value rows' 384-thread CTAs read it from L1
+    # RMSNorm rows of 8 warps at 4 units a thread hold their weight too (2 CTAs
+    # an SM); the 12288-value rows' 384-thread CTAs read it from L1
     p = _plan(rs.RS_OP_RMSNORM, 32768, 8192, dtype)
     assert p["path"] == rs.RS_PATH_RING and p["smem_bytes"] == 8192 * 2 * p["rows_per_cta"] * p["stages"]
     assert p["threads_per_row"] == 256 and p["block_threads"] == 256 and p["grid"] == 2 * 152
+    # RMSNorm rows of 4 warps hold their weight in 128-thread CTAs, one row a CTA and 4
+    # CTAs an SM (measured 6.1 % faster than 2 rows a 256-thread CTA on bf16 4096)
     p = _plan(rs.RS_OP_RMSNORM, 32768, 4096, dtype)
-    assert p["threads_per_row"] == 128 and p["block_threads"] == 256 and p["grid"] == 2 * 152
+    assert p["threads_per_row"] == 128 and p["block_threads"] == 128 and p["grid"] == 4 * 152
     p = _plan(rs.RS_OP_RMSNORM, 32768, 12288, dtype)
     assert p["threads_per_row"] == 384 and p["grid"] == 2 * 152  # 64 registers, 384 threads: 2 CTAs by threads
     p = _plan(rs.RS_OP_LAYERNORM, 32768, 8184, dtype, ld=8192, b=B)
