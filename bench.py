@@ -504,9 +504,13 @@ def measure(args, name, ctx, full: bool, causal_summary: bool = False):
 
     ms_per_step = total_ms / args.steps
     nbytes = op_bytes(op, w)
-    if causal:  # the least traffic the mask allows: kept elements read, every element written
+    full_bytes = nbytes
+    if causal:
+        # The mask's line counts the least traffic it allows -- kept elements
+        # read, every element written -- the bytes the kernel must move; the
+        # plain softmax's M x N x (in + out) bytes are given beside it.
         kept = int(np.minimum(np.arange(w.M, dtype=np.int64) % w.N + 1, w.N).sum())
-        min_bytes = (kept + w.M * w.N) * w.elem_size
+        nbytes = (kept + w.M * w.N) * w.elem_size
     value = job_gbs(world, nbytes, args.steps, total_ms)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
 
@@ -599,9 +603,10 @@ def measure(args, name, ctx, full: bool, causal_summary: bool = False):
                     "frac_of_same_run_copy": round(achieved / copy_gbs, 4), "same_run_copy_gbs": round(copy_gbs, 1),
                     "kernel": rs.PATH_NAMES[plan["path"]], "bytes_per_step": nbytes, "steps": args.steps,
                     "repeats": repeats}
-            if causal:  # the line's value counts M x N x 4 bytes; the least traffic the mask allows beside it
-                line["min_bytes_per_step"] = min_bytes
-                line["min_bytes_gbs"] = round(job_gbs(world, min_bytes, args.steps, total_ms), 2)
+            if causal:  # value and frac count the least traffic the mask allows; the plain count beside it
+                line["bytes_counted"] = "kept elements read + all elements written"
+                line["full_bytes_per_step"] = full_bytes
+                line["full_bytes_gbs"] = round(job_gbs(world, full_bytes, args.steps, total_ms), 2)
         else:
             line = {
                 "metric": OP_METRIC[op], "value": round(value, 2), "unit": "GB/s",
@@ -636,9 +641,10 @@ def measure(args, name, ctx, full: bool, causal_summary: bool = False):
                 "e2e": e2e,
                 "gpu_launches": args.steps,
                 **({"causal": {"period": w.N, "diag_offset": 0,
-                               "value_counts": "M x N x (in + out) bytes, as the plain softmax line",
-                               "min_bytes_per_step": min_bytes,
-                               "min_bytes_gbs": round(job_gbs(world, min_bytes, args.steps, total_ms), 2),
+                               "value_counts": "the least traffic the mask allows: kept elements read, all "
+                                               "elements written (config.bytes_per_step)",
+                               "full_bytes_per_step": full_bytes,
+                               "full_bytes_gbs": round(job_gbs(world, full_bytes, args.steps, total_ms), 2),
                                "how": "rowsoftmax_causal_fwd: row r keeps (r mod N) + 1 elements, the masked part "
                                       "is not used and is written as 0"}} if causal else {}),
                 "timing": f"{replays} replays of a CUDA graph of {G} launches after one untimed replay; one event "
