@@ -223,35 +223,54 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
         ro.vec_per_thread = 4;
     int rc = plan_rows(dtype, vec, M, units, ro, p, values != RS_RING_REREAD);
     if (rc != RS_OK) return rc;
-    // CTA sizes measured on the ring's 16-bit rows (graph-replayed, 2^18 to
-    // 2^20 rows, against the 256-thread CTAs planned above):
+    // Shapes measured on the ring's 16-bit rows (graph-replayed, 2^15 to 2^20
+    // rows, against the plan above: 256-thread CTAs, two stages):
     //  - softmax rows of one warp at 4 or more units a thread: 512 threads,
     //    one CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048
-    //    +3.9 %, bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %;
-    //    softmax rows of 4 warps +0.3 %, of 8 warps -2 %: unchanged);
+    //    +3.9 %, bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %);
+    //  - softmax rows of 769 to 1024 units (bf16 8192): 4 warps a row at 8
+    //    units a thread in 512-thread CTAs, three stages (+7.8 %; 8 warps at 4
+    //    units measured within 1 % at any CTA size and stage count);
     //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %);
-    //  - RMSNorm rows of 4 warps at 4 units a thread: 128 threads, one row a
-    //    CTA (bf16 4096 +6.1 %; its rows of one warp +0.7 % at 512, of 8
-    //    warps -7 % at 512: unchanged).
-    // Only with at least 64 rows an SM, so that every CTA loops over stages.
+    //  - RMSNorm rows of one warp at 8 units: 512 threads (bf16 2048 +0.8 %);
+    //    of 4 warps at 4 units: 128 threads, one row a CTA (bf16 4096 +6.1 %);
+    //    of 8 warps at 4 units: four stages (bf16 8192 +8.3 %).
+    // Only with at least 64 rows an SM, so that every CTA loops over stages,
+    // and not for the causal mask's multi-warp rows (its copy ring serves rows
+    // of one warp best).
+    int def_stages = kRingDefaultStages;
     if (dtype != RS_F32 && values != RS_RING_REREAD && !o.block_threads && !o.threads_per_row &&
         !o.vec_per_thread && M >= (int64_t)64 * dev.sm_count) {
         const int tpr = p->threads_per_row, vpt = p->vec_per_thread;
-        int want = 0;
-        if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4)
-            want = 512;
-        else if (p->op == RS_OP_LAYERNORM && tpr == 32)
-            want = 128;
-        else if (p->op == RS_OP_RMSNORM && tpr == 128 && vpt <= 4)
-            want = 128;
-        if (want && want != p->block_threads) {
-            const rs_plan keep = *p;
-            rs_options rb = ro;
-            rb.block_threads = want;
-            if (plan_rows(dtype, vec, M, units, rb, p, true) != RS_OK || p->threads_per_row != tpr ||
-                p->vec_per_thread != vpt)
-                *p = keep;
+        rs_options rb = ro;
+        int stages_want = 0;
+        if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4) {
+            rb.block_threads = 512;
+        } else if (p->op == RS_OP_SOFTMAX && !p->masked && units > 768 && units <= 1024) {
+            rb.threads_per_row = 128;
+            rb.vec_per_thread = 8;
+            rb.block_threads = 512;
+            stages_want = 3;
+        } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
+            rb.block_threads = 128;
+        } else if (p->op == RS_OP_RMSNORM && tpr == 32 && vpt == 8) {
+            rb.block_threads = 512;
+        } else if (p->op == RS_OP_RMSNORM && tpr == 128 && vpt <= 4) {
+            rb.block_threads = 128;
+        } else if (p->op == RS_OP_RMSNORM && tpr == 256 && vpt <= 4) {
+            stages_want = 4;
         }
+        if (rb.block_threads && rb.block_threads != p->block_threads) {
+            const rs_plan keep = *p;
+            const int want_tpr = rb.threads_per_row ? rb.threads_per_row : tpr;
+            const int want_vpt = rb.vec_per_thread ? rb.vec_per_thread : vpt;
+            if (plan_rows(dtype, vec, M, units, rb, p, true) != RS_OK || p->threads_per_row != want_tpr ||
+                p->vec_per_thread != want_vpt) {
+                *p = keep;
+                stages_want = 0;
+            }
+        }
+        if (stages_want) def_stages = stages_want;
     }
     p->path = RS_PATH_RING;  // (the LayerNorm kind depends on the path)
     const int lkind = p->op == RS_OP_LAYERNORM ? rs::layernorm_merge_kind(*p, N, vec) : 0;
@@ -260,8 +279,12 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     const int64_t stage = slot * p->rows_per_cta;
     if (stage <= 0) return RS_ERR_NO_PATH;
     const int64_t max_dyn = (int64_t)dev.max_smem_per_block_optin - (int64_t)rs::kRingStaticSmem;
-    const int stages = o.stages ? o.stages : kRingDefaultStages;
-    const int64_t smem = stage * stages + (int64_t)(held ? 0 : nparams) * round_up(N, vec) * elem_size(dtype);
+    int stages = o.stages ? o.stages : def_stages;
+    int64_t smem = stage * stages + (int64_t)(held ? 0 : nparams) * round_up(N, vec) * elem_size(dtype);
+    if (!o.stages && stages > kRingDefaultStages && smem > max_dyn) {  // a measured stage count that does not fit
+        stages = kRingDefaultStages;
+        smem = stage * stages + (int64_t)(held ? 0 : nparams) * round_up(N, vec) * elem_size(dtype);
+    }
     if (smem > max_dyn || stage >= (1 << 20)) return RS_ERR_NO_PATH;  // mbarrier tx count < 2^20
     const int regs = values == RS_RING_REREAD ? rs::kRingRereadRegs
                      : held ? rs::kHeldRegs

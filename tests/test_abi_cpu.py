@@ -129,7 +129,7 @@ def test_plans_for_the_benchmark_workloads():
     assert p["path"] == rs.RS_PATH_ROWS and p["vec_elems"] == 4 and _covers(p, 5000)
     p = _plan(32768, 8192, rs.RS_BF16)
     assert p["path"] == rs.RS_PATH_RING and p["vec_elems"] == 8 and _covers(p, 8192)
-    assert p["ring_values"] == rs.RS_RING_REGISTERS and p["stages"] == 2
+    assert p["ring_values"] == rs.RS_RING_REGISTERS and p["stages"] == 3
     p = _plan(512, 131072, rs.RS_F16)
     assert p["path"] == rs.RS_PATH_CLUSTER and p["ring_values"] == rs.RS_RING_REGISTERS
     assert p["cluster_size"] >= 2 and _covers(p, 131072)
@@ -337,8 +337,15 @@ def test_ring_cta_sizes_for_16bit_rows():
             assert p["block_threads"] == 512 and p["rows_per_cta"] == 16 and p["grid"] == per_sm * 152, (N, dt)
     assert _plan(1 << 20, 2048, rs.RS_BF16, opts={"block_threads": 256})["block_threads"] == 256
     assert _plan(64 * 152 - 1, 2048, rs.RS_BF16)["block_threads"] == 256  # few rows: unchanged
+    # rows of 769 to 1024 units: 4 warps a row at 8 units a thread, 512-thread
+    # CTAs, three stages (bf16 8192 +7.8 %)
     p = _plan(32768, 8192, rs.RS_BF16)
-    assert p["threads_per_row"] == 256 and p["block_threads"] == 256
+    assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"], p["stages"]) == (128, 8, 512, 3)
+    assert p["rows_per_cta"] == 4 and p["grid"] == 152 and p["smem_bytes"] == 3 * 4 * 8192 * 2
+    p = _plan(32768, 6200, rs.RS_F16, ld=6208)
+    assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (128, 8, 512) and _covers(p, 6200)
+    p = _plan(32768, 6144, rs.RS_BF16)  # 768 units: unchanged
+    assert p["block_threads"] != 512 or p["threads_per_row"] != 128
     rc, p = rs.rownorm_plan(rs.RS_OP_LAYERNORM, A, A + (1 << 40), A, A, 1 << 20, 2048, 2048, 2048, 1e-5,
                             rs.RS_BF16, None, gb300())
     assert rc == rs.RS_OK and p["path"] == rs.RS_PATH_RING and p["threads_per_row"] == 32
