@@ -21,7 +21,15 @@
 // three stages (1.295 ms); three buffers with two groups in flight and the
 // refill issued as soon as a stage is loaded (1.238 ms); four (1.897 ms, one
 // CTA an SM); re-reading the stage in three passes with two exponentials a
-// kept element and 70 registers (1.513 ms).
+// kept element and 70 registers (1.513 ms); branches per slot that skip the
+// masked slots' loads and arithmetic (1.377 and 1.419 ms).
+// The rows of one warp are bound by instruction issue, not memory; three
+// changes that each issue fewer instructions a row, kept (in one call, every
+// step bitwise equal to the plain softmax of the same scores): the exponent's
+// subtraction and scaling and the final scaling in fp32 pairs (1215 -> 1132
+// us); the fill of the masked units selected on the 16-byte words before the
+// unpack (-> 1067 us); the scaling fused into the stores, the masked slots
+// selected to zero words after the rounding (-> 1033 us).
 #pragma once
 
 #include <mutex>
@@ -97,18 +105,18 @@ ring_cp_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64
         // Fully kept units from the stage, the rest the fill (-inf); then the
         // one unit that holds the end of the kept prefix (staged, or the row's
         // ragged tail read from global memory), if this thread has it.
+        // (The fill is selected on the 16-byte words, -inf pairs, before the
+        // unpack: one select a word rather than one move a value.)
         float v[VPT][VEC];
         const int keep = row_keep(args, active ? row : 0, N);
         const int whole_units = keep / VEC;
+        constexpr uint32_t kNegPair = DT == RS_BF16 ? 0xFF80FF80u : 0xFC00FC00u;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int u = t + k * tpr;
-            if (active && u < whole_units) {
-                T::unpack(*reinterpret_cast<const uint4*>(srow + (size_t)u * 16), v[k]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) v[k][e] = OP::kFill;
-            }
+            uint4 wv = make_uint4(kNegPair, kNegPair, kNegPair, kNegPair);
+            if (active && u < whole_units) wv = *reinterpret_cast<const uint4*>(srow + (size_t)u * 16);
+            T::unpack(wv, v[k]);
         }
         const int us = whole_units;
         if (active && keep % VEC && t <= us && us <= t + (VPT - 1) * tpr) {
@@ -125,12 +133,28 @@ ring_cp_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int64
                 }
             }
         }
-        OP::template apply<DT, VEC, VPT>(v, t, tpr, keep, false, GlobalParams{nullptr, nullptr, 0.0f, N, 0},
-                                         part[it & 1]);
+        const float c = OP::template reduce<DT, VEC, VPT>(v, tpr, keep, part[it & 1]);
         // The row's values have been used (the stage's reads are complete):
         // refill the stage with the group STAGES iterations ahead, then store.
         issue(s, g + (int64_t)STAGES * gridDim.x);
-        if (active) store_row_units<DT, VEC, VPT>(out + row * ldo, t, tpr, N, v);
+        if (active) {
+            S* yr = out + row * ldo;
+            if (isfinite(c) && (t + (VPT - 1) * tpr + 1) * VEC <= N) {
+                // Scale, round, and store each unit; the slots past the prefix
+                // are selected to zero words after the rounding.
+                const int kk = (keep + tpr * VEC - 1) / (tpr * VEC);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    unit_mul<VEC>(v[k], c);
+                    uint4 w = T::pack(v[k]);
+                    if (k >= kk) w = make_uint4(0u, 0u, 0u, 0u);
+                    __stcs(reinterpret_cast<uint4*>(yr + (size_t)(t + k * tpr) * VEC), w);
+                }
+            } else {
+                OP::template finish<DT, VEC, VPT>(v, t, tpr, keep, c);
+                store_row_units<DT, VEC, VPT>(yr, t, tpr, N, v);
+            }
+        }
         if (++s == STAGES) s = 0;
     }
     cp_async_wait<0>();  // no copy outlives the CTA
