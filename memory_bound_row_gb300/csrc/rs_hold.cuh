@@ -392,11 +392,8 @@ wide_hold_kernel(const void* in_, void* out_, int64_t M, int N, int64_t ldi, int
                 float w[VEC], b[VEC];
                 prm.template w_unit<DT, VEC>(base, w);
                 if constexpr (OP::kOp == RS_OP_LAYERNORM) prm.template b_unit<DT, VEC>(base, b);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    if constexpr (OP::kOp == RS_OP_RMSNORM) v[k][e] = v[k][e] * r * w[e];
-                    else v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
-                }
+                if constexpr (OP::kOp == RS_OP_RMSNORM) unit_rms<VEC>(v[k], r, w);
+                else unit_ln<VEC>(v[k], r, nmr, w, b);
             }
         }
 

@@ -256,6 +256,12 @@ struct SharedParams {
     __device__ __forceinline__ void b_unit_k(int, int base, float* f) const { b_unit<DT2, VEC>(base, f); }
 };
 
+// Whether a row operation's weight and bias already sit in registers (then the
+// LayerNorm epilogue stays scalar: packing held vectors into register pairs
+// measured 10 % slower on bf16 32768 x 8192, by spills).
+template <typename P> struct ParamsInRegisters { static constexpr bool value = false; };
+template <int VPT, int VEC> struct ParamsInRegisters<HeldParams<VPT, VEC>> { static constexpr bool value = true; };
+
 // Copies the elements [c0, c0 + len) of a parameter vector into shared memory
 // `dst`, padded with `pad` up to `padded` elements (all threads of the CTA;
 // the caller synchronises before reading).  A null source stages nothing.
@@ -306,6 +312,45 @@ __device__ __forceinline__ void pair_mul(float& a, float& b, float c) {
         "mul.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
         : "+f"(a), "+f"(b) : "f"(c));
 }
+// The normalisations' epilogues on a unit, in fp32 pairs (each lane rounds
+// as the scalar expression does): RMSNorm (x r) w, LayerNorm
+// fma(fma(x, r, nmr), w, b) with nmr = -mean r.  Measured against the scalar
+// loops (same call): LayerNorm bf16 1048576 x 2048 +2.5 %, fp16 512 x 131072
+// +3.2 %, RMSNorm +0.9 to +1.8 %, the rest unchanged.
+__device__ __forceinline__ unsigned long long f2(float a, float b) {
+    unsigned long long p;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a), "f"(b));
+    return p;
+}
+__device__ __forceinline__ void f2_split(unsigned long long p, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p));
+}
+template <int VEC>
+__device__ __forceinline__ void unit_rms(float (&f)[VEC], float r, const float (&w)[VEC]) {
+    const unsigned long long rr = f2(r, r);
+#pragma unroll
+    for (int e = 0; e + 1 < VEC; e += 2) {
+        unsigned long long x = f2(f[e], f[e + 1]);
+        asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(rr));
+        asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(f2(w[e], w[e + 1])));
+        f2_split(x, f[e], f[e + 1]);
+    }
+    if constexpr (VEC % 2 != 0) f[VEC - 1] = f[VEC - 1] * r * w[VEC - 1];
+}
+template <int VEC>
+__device__ __forceinline__ void unit_ln(float (&f)[VEC], float r, float nmr, const float (&w)[VEC],
+                                        const float (&b)[VEC]) {
+    const unsigned long long rr = f2(r, r), nn = f2(nmr, nmr);
+#pragma unroll
+    for (int e = 0; e + 1 < VEC; e += 2) {
+        unsigned long long x = f2(f[e], f[e + 1]);
+        asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x) : "l"(rr), "l"(nn));
+        asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x) : "l"(f2(w[e], w[e + 1])), "l"(f2(b[e], b[e + 1])));
+        f2_split(x, f[e], f[e + 1]);
+    }
+    if constexpr (VEC % 2 != 0) f[VEC - 1] = fmaf(fmaf(f[VEC - 1], r, nmr), w[VEC - 1], b[VEC - 1]);
+}
+
 // A unit's values through exp_diff, and times c, in pairs (an odd last value alone).
 template <int VEC>
 __device__ __forceinline__ void unit_exp_diff(float (&f)[VEC], float ms) {
@@ -424,8 +469,7 @@ struct OpRmsNorm {
         for (int k = 0; k < VPT; ++k) {
             float w[VEC];
             a.template w_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, w);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] = v[k][e] * r * w[e];
+            unit_rms<VEC>(v[k], r, w);
         }
     }
 };
@@ -463,8 +507,12 @@ struct OpLayerNorm {
             float w[VEC], b[VEC];
             a.template w_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, w);
             a.template b_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, b);
+            if constexpr (ParamsInRegisters<P>::value) {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
+                for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
+            } else {
+                unit_ln<VEC>(v[k], r, nmr, w, b);
+            }
         }
     }
 };
@@ -529,8 +577,12 @@ __device__ __forceinline__ void layernorm_out(float (&v)[VPT][VEC], int t, int t
         float w[VEC], b[VEC];
         a.template w_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, w);
         a.template b_unit_k<DT, VEC>(k, (t + k * tpr) * VEC, b);
+        if constexpr (ParamsInRegisters<P>::value) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
+            for (int e = 0; e < VEC; ++e) v[k][e] = fmaf(fmaf(v[k][e], r, nmr), w[e], b[e]);
+        } else {
+            unit_ln<VEC>(v[k], r, nmr, w, b);
+        }
     }
 }
 
