@@ -193,6 +193,17 @@ int64_t ctas_per_sm(const rs_device_info& dev, int block, size_t smem, int regs_
     return n < 1 ? 1 : n;
 }
 
+// 16-bit softmax rows of 769 to 4096 16-byte units that the ring serves at 8
+// units a thread (measured faster than the 4-unit ring shape and than the
+// clusters from 8192 to 32768 values), given enough rows that every CTA loops
+// over its stages (4 row groups an SM at least).
+bool wide16_ring(int64_t units, int64_t M, int sm_count) {
+    if (units <= 768 || units > 4096) return false;
+    const int64_t t8 = round_up(ceil_div(units, 8), 32);
+    const int64_t rows_per_cta = t8 <= 256 ? 512 / t8 : 1;
+    return M >= rows_per_cta * 4 * (int64_t)sm_count;
+}
+
 // RS_PATH_RING.  `nparams` parameter vectors (LayerNorm's weight and bias)
 // are staged in shared memory after the stages, padded to whole units, unless
 // the plan takes a held-parameter instance (vectors in registers).
@@ -223,44 +234,55 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
         ro.vec_per_thread = 4;
     int rc = plan_rows(dtype, vec, M, units, ro, p, values != RS_RING_REREAD);
     if (rc != RS_OK) return rc;
-    // Shapes measured on the ring's 16-bit rows (graph-replayed, 2^15 to 2^20
-    // rows, against the plan above: 256-thread CTAs, two stages):
+    // Shapes measured on the ring's 16-bit rows (graph-replayed, 2^13 to 2^20
+    // rows, against the plan above: 256-thread CTAs, two stages, and against
+    // the clusters where they were planned):
     //  - softmax rows of one warp at 4 or more units a thread: 512 threads,
     //    one CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048
     //    +3.9 %, bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %);
-    //  - softmax rows of 769 to 1024 units (bf16 8192): 4 warps a row at 8
-    //    units a thread in 512-thread CTAs, three stages (+7.8 %; 8 warps at 4
-    //    units measured within 1 % at any CTA size and stage count);
-    //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %);
+    //  - softmax rows of 769 to 4096 units (wide16_ring): 8 units a thread,
+    //    512-thread CTAs where a row takes at most 256 threads (else one row a
+    //    CTA), three stages (bf16 8192 +7.8 %, 12288 +12.9 %, 16384 +12.1 %
+    //    against the clusters, 20480 +4.4 %, 24576 +3.5 %, 28672 +16 %,
+    //    32768 +8.3 %);
+    //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %); of 1537 to
+    //    2048 units: 8 units a thread, 512-thread CTAs (bf16 16384 +24 %);
     //  - RMSNorm rows of one warp at 8 units: 512 threads (bf16 2048 +0.8 %);
     //    of 4 warps at 4 units: 128 threads, one row a CTA (bf16 4096 +6.1 %);
     //    of 8 warps at 4 units: four stages (bf16 8192 +8.3 %).
-    // Only with at least 64 rows an SM, so that every CTA loops over stages,
-    // and not for the causal mask's multi-warp rows (its copy ring serves rows
-    // of one warp best).
+    // Not for the causal mask's multi-warp rows (its copy ring serves rows of
+    // one warp best).
     int def_stages = kRingDefaultStages;
     if (dtype != RS_F32 && values != RS_RING_REREAD && !o.block_threads && !o.threads_per_row &&
-        !o.vec_per_thread && M >= (int64_t)64 * dev.sm_count) {
+        !o.vec_per_thread) {
         const int tpr = p->threads_per_row, vpt = p->vec_per_thread;
+        const bool many_rows = M >= (int64_t)64 * dev.sm_count;  // every CTA loops over stages
         rs_options rb = ro;
         int stages_want = 0;
-        if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4) {
-            rb.block_threads = 512;
-        } else if (p->op == RS_OP_SOFTMAX && !p->masked && units > 768 && units <= 1024) {
-            rb.threads_per_row = 128;
+        if (p->op == RS_OP_SOFTMAX && !p->masked && wide16_ring(units, M, dev.sm_count)) {
+            const int t8 = (int)round_up(ceil_div(units, 8), 32);
+            rb.threads_per_row = t8;
             rb.vec_per_thread = 8;
-            rb.block_threads = 512;
+            rb.block_threads = t8 <= 256 ? (512 / t8) * t8 : t8;
             stages_want = 3;
-        } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
-            rb.block_threads = 128;
-        } else if (p->op == RS_OP_RMSNORM && tpr == 32 && vpt == 8) {
-            rb.block_threads = 512;
-        } else if (p->op == RS_OP_RMSNORM && tpr == 128 && vpt <= 4) {
-            rb.block_threads = 128;
-        } else if (p->op == RS_OP_RMSNORM && tpr == 256 && vpt <= 4) {
-            stages_want = 4;
+        } else if (many_rows) {
+            if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4) {
+                rb.block_threads = 512;
+            } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
+                rb.block_threads = 128;
+            } else if (p->op == RS_OP_LAYERNORM && units > 1536 && units <= 2048) {
+                rb.threads_per_row = 256;
+                rb.vec_per_thread = 8;
+                rb.block_threads = 512;
+            } else if (p->op == RS_OP_RMSNORM && tpr == 32 && vpt == 8) {
+                rb.block_threads = 512;
+            } else if (p->op == RS_OP_RMSNORM && tpr == 128 && vpt <= 4) {
+                rb.block_threads = 128;
+            } else if (p->op == RS_OP_RMSNORM && tpr == 256 && vpt <= 4) {
+                stages_want = 4;
+            }
         }
-        if (rb.block_threads && rb.block_threads != p->block_threads) {
+        if (rb.block_threads && (rb.block_threads != p->block_threads || rb.threads_per_row || rb.vec_per_thread)) {
             const rs_plan keep = *p;
             const int want_tpr = rb.threads_per_row ? rb.threads_per_row : tpr;
             const int want_vpt = rb.vec_per_thread ? rb.vec_per_thread : vpt;
@@ -544,7 +566,8 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         // kClusterThinValues values a thread: 3278 -> 5327 GB/s on 40 KB rows;
         // with fuller cluster shapes the clusters measured as fast or faster).
         bool ring = dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes &&
-                    (norm || N * es < kRowsMaxRowBytes);
+                    (norm || N * es < kRowsMaxRowBytes ||
+                     (!masked && wide16_ring(units, M, dev->sm_count)));
         if (!ring && !norm && dtype != RS_F32 && vec_ok && N * es < kRingMaxRowBytesSoftmax16) {
             rs_plan cp = *p;
             ring = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, &cp) != RS_OK ||

@@ -109,15 +109,27 @@ def _covers(plan, N):
     return plan["cluster_size"] * plan["chunk_elems"] >= N
 
 
-def test_wide_16bit_softmax_rows_take_the_ring_where_clusters_spread_thin():
-    # 16-bit softmax rows of 32-64 KB take the ring when the cluster plan would
-    # hold at most 16 values a thread, and keep well-filled clusters otherwise.
-    p = _plan(8192, 20480, rs.RS_BF16)  # the fill rule's cluster: 5 CTAs of 2 units a thread
-    assert p["path"] == rs.RS_PATH_RING and _covers(p, 20480)
-    for N in (16384, 24576, 28672, 32768):
-        p = _plan(8192, N, rs.RS_BF16)
-        assert p["path"] == rs.RS_PATH_CLUSTER and p["vec_per_thread"] * 8 > 16, N
-    assert _plan(4096, 40960, rs.RS_F16)["path"] == rs.RS_PATH_CLUSTER  # over 64 KB
+def test_wide_16bit_softmax_rows_take_the_ring_at_8_units_a_thread():
+    # 16-bit softmax rows of 769 to 4096 units (6145 to 32768 values) take the
+    # ring at 8 units a thread, 512-thread CTAs where a row takes at most 256
+    # threads, three stages (measured faster than the 4-unit ring and than the
+    # clusters at every N from 8192 to 32768); given 4 row groups an SM.
+    for N, tpr, block in [(12288, 192, 384), (16384, 256, 512), (20480, 320, 320), (24576, 384, 384),
+                          (28672, 448, 448), (32768, 512, 512)]:
+        p = _plan((1 << 28) // N, N, rs.RS_BF16)
+        assert p["path"] == rs.RS_PATH_RING and _covers(p, N), N
+        assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"], p["stages"]) == (tpr, 8, block, 3), N
+        assert p["smem_bytes"] == 3 * (block // tpr) * N * 2
+    # ragged widths round the threads up to whole warps
+    p = _plan(8192, 10000, rs.RS_F16, ld=10000)
+    assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (160, 8, 480) and _covers(p, 10000)
+    # few rows: the clusters as before (each CTA would not loop over its stages)
+    assert _plan(64, 32768, rs.RS_BF16)["path"] == rs.RS_PATH_CLUSTER
+    assert _plan(4096, 40960, rs.RS_F16)["path"] == rs.RS_PATH_CLUSTER  # over 4096 units
+    # the causal mask keeps its plans (the copy ring serves rows of one warp best)
+    rc, p = rs.rowsoftmax_causal_plan(A, A + (1 << 40), 8192, 32768, 32768, 32768, 32768, 0, rs.RS_BF16, None,
+                                      gb300())
+    assert rc == rs.RS_OK and p["path"] == rs.RS_PATH_CLUSTER
 
 
 def test_plans_for_the_benchmark_workloads():

@@ -99,6 +99,26 @@ def test_auto_path_wide_16bit_rows(dtype, N):
     _check(x, _run(x, out=out), what=f"auto wide {dtype} N={N}")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [6200, 10000, 12288, 16384, 24576, 32768])
+def test_wide_16bit_rows_on_the_8_unit_ring(dtype, N):
+    # Where the planner puts wide 16-bit softmax rows given enough rows: the
+    # ring at 8 units a thread, several rows a 512-thread CTA where they fit,
+    # three stages; a ragged last row group; every row against the oracle.
+    units = -(-N // 8)
+    tpr = -(-(-(-units // 8)) // 32) * 32
+    rows_per_cta = 512 // tpr if tpr <= 256 else 1
+    M = rows_per_cta * 4 * 152 + 37
+    x, out = _aligned(M, N, dtype, kind="normal_spike", seed=N + 7)
+    rc, dev = rs.rowsoftmax_device_info()
+    rc, plan = rs.rowsoftmax_plan(x.data_ptr(), out.data_ptr(), M, N, x.stride(0), out.stride(0),
+                                  rs.dtype_code(x.dtype), None, dev)
+    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_RING
+    assert (plan["threads_per_row"], plan["vec_per_thread"], plan["stages"]) == (tpr, 8, 3)
+    y = _run(x, out=out)
+    check_all_rows("softmax", x, y, N, what=f"8-unit ring {dtype} {M}x{N}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("tpr,vpt", [(1, 1), (2, 2), (4, 3), (8, 5), (16, 8), (32, 1), (32, 6), (64, 4), (96, 2),
                                      (256, 2), (512, 1), (1024, 1), (160, 8)])
