@@ -193,15 +193,47 @@ int64_t ctas_per_sm(const rs_device_info& dev, int block, size_t smem, int regs_
     return n < 1 ? 1 : n;
 }
 
-// 16-bit softmax rows of 769 to 4096 16-byte units that the ring serves at 8
-// units a thread (measured faster than the 4-unit ring shape and than the
-// clusters from 8192 to 32768 values), given enough rows that every CTA loops
-// over its stages (4 row groups an SM at least).
-bool wide16_ring(int64_t units, int64_t M, int sm_count) {
-    if (units <= 768 || units > 4096) return false;
-    const int64_t t8 = round_up(ceil_div(units, 8), 32);
-    const int64_t rows_per_cta = t8 <= 256 ? 512 / t8 : 1;
-    return M >= rows_per_cta * 4 * (int64_t)sm_count;
+// Ring shapes measured for 16-bit softmax rows of 257 to 4096 16-byte units
+// (bf16, 2^28 / N to 2^29 / N rows, graph-replayed, against the 4-unit shape
+// planned otherwise and, from 16384 values, the clusters):
+//  - a multiple of 256 units: 8 units a thread, 512-thread CTAs where a row
+//    takes at most 256 threads (else one row a CTA), three stages (N = 4096
+//    +9 %, 6144 +8 %, 8192 +7.8 %, 12288 +13 %, 16384 +12 %, 20480 +4.4 %,
+//    24576 +3.5 %, 28672 +16 %, 32768 +8.3 %);
+//  - else 6 or 5 units a thread where they fill whole warps exactly: one row
+//    a CTA, two stages (2560 +34 %, 4608 +25 %, 5120 +7.6 %; 3072 -1 %);
+//  - else 8 units a thread on whole warps: rows of up to 768 units one row a
+//    CTA and two stages (3584 +10 %, 5632 +17 %), wider rows as the first case.
+// Given 4 row groups an SM at least, so that every CTA loops over its stages.
+struct RingShape {
+    int tpr, vpt, block, stages;
+};
+bool ring16_softmax_shape(int64_t units, int64_t M, int sm_count, RingShape* shape) {
+    if (units <= 256 || units > 4096) return false;
+    RingShape r{};
+    if (units % 256 == 0) {
+        r.tpr = (int)(units / 8);
+        r.vpt = 8;
+        r.stages = 3;
+        r.block = r.tpr <= 256 ? (512 / r.tpr) * r.tpr : r.tpr;
+    } else if (units % 6 == 0 && (units / 6) % 32 == 0) {
+        r = {(int)(units / 6), 6, (int)(units / 6), 2};
+    } else if (units % 5 == 0 && (units / 5) % 32 == 0) {
+        r = {(int)(units / 5), 5, (int)(units / 5), 2};
+    } else {
+        r.tpr = (int)round_up(ceil_div(units, 8), 32);
+        r.vpt = 8;
+        if (units <= 768) {
+            r.block = r.tpr;
+            r.stages = 2;
+        } else {
+            r.block = r.tpr <= 256 ? (512 / r.tpr) * r.tpr : r.tpr;
+            r.stages = 3;
+        }
+    }
+    if (M < (int64_t)(r.block / r.tpr) * 4 * sm_count) return false;
+    *shape = r;
+    return true;
 }
 
 // RS_PATH_RING.  `nparams` parameter vectors (LayerNorm's weight and bias)
@@ -240,11 +272,7 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     //  - softmax rows of one warp at 4 or more units a thread: 512 threads,
     //    one CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048
     //    +3.9 %, bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %);
-    //  - softmax rows of 769 to 4096 units (wide16_ring): 8 units a thread,
-    //    512-thread CTAs where a row takes at most 256 threads (else one row a
-    //    CTA), three stages (bf16 8192 +7.8 %, 12288 +12.9 %, 16384 +12.1 %
-    //    against the clusters, 20480 +4.4 %, 24576 +3.5 %, 28672 +16 %,
-    //    32768 +8.3 %);
+    //  - softmax rows of 257 to 4096 units: ring16_softmax_shape;
     //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %); of 1537 to
     //    2048 units: 8 units a thread, 512-thread CTAs (bf16 16384 +24 %);
     //  - RMSNorm rows of one warp at 8 units: 512 threads (bf16 2048 +0.8 %);
@@ -259,12 +287,12 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
         const bool many_rows = M >= (int64_t)64 * dev.sm_count;  // every CTA loops over stages
         rs_options rb = ro;
         int stages_want = 0;
-        if (p->op == RS_OP_SOFTMAX && !p->masked && wide16_ring(units, M, dev.sm_count)) {
-            const int t8 = (int)round_up(ceil_div(units, 8), 32);
-            rb.threads_per_row = t8;
-            rb.vec_per_thread = 8;
-            rb.block_threads = t8 <= 256 ? (512 / t8) * t8 : t8;
-            stages_want = 3;
+        RingShape shape{};
+        if (p->op == RS_OP_SOFTMAX && !p->masked && ring16_softmax_shape(units, M, dev.sm_count, &shape)) {
+            rb.threads_per_row = shape.tpr;
+            rb.vec_per_thread = shape.vpt;
+            rb.block_threads = shape.block;
+            stages_want = shape.stages;
         } else if (many_rows) {
             if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4) {
                 rb.block_threads = 512;
@@ -282,7 +310,8 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
                 stages_want = 4;
             }
         }
-        if (rb.block_threads && (rb.block_threads != p->block_threads || rb.threads_per_row || rb.vec_per_thread)) {
+        if (rb.block_threads &&
+            (rb.block_threads != p->block_threads || rb.threads_per_row != tpr || rb.vec_per_thread != vpt)) {
             const rs_plan keep = *p;
             const int want_tpr = rb.threads_per_row ? rb.threads_per_row : tpr;
             const int want_vpt = rb.vec_per_thread ? rb.vec_per_thread : vpt;
@@ -565,9 +594,10 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         // 64 KB where the cluster plan would spread a row thin (at most
         // kClusterThinValues values a thread: 3278 -> 5327 GB/s on 40 KB rows;
         // with fuller cluster shapes the clusters measured as fast or faster).
+        RingShape shape16{};
         bool ring = dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes &&
                     (norm || N * es < kRowsMaxRowBytes ||
-                     (!masked && wide16_ring(units, M, dev->sm_count)));
+                     (!masked && ring16_softmax_shape(units, M, dev->sm_count, &shape16)));
         if (!ring && !norm && dtype != RS_F32 && vec_ok && N * es < kRingMaxRowBytesSoftmax16) {
             rs_plan cp = *p;
             ring = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, &cp) != RS_OK ||

@@ -109,11 +109,12 @@ def _covers(plan, N):
     return plan["cluster_size"] * plan["chunk_elems"] >= N
 
 
-def test_wide_16bit_softmax_rows_take_the_ring_at_8_units_a_thread():
-    # 16-bit softmax rows of 769 to 4096 units (6145 to 32768 values) take the
-    # ring at 8 units a thread, 512-thread CTAs where a row takes at most 256
-    # threads, three stages (measured faster than the 4-unit ring and than the
-    # clusters at every N from 8192 to 32768); given 4 row groups an SM.
+def test_16bit_softmax_rows_take_the_measured_ring_shapes():
+    # 16-bit softmax rows of 257 to 4096 units take the ring shapes measured
+    # fastest; those of 769 units or more at 8 units a thread, 512-thread CTAs
+    # where a row takes at most 256 threads, three stages (faster than the
+    # 4-unit ring and than the clusters at every N from 8192 to 32768); given
+    # 4 row groups an SM.
     for N, tpr, block in [(12288, 192, 384), (16384, 256, 512), (20480, 320, 320), (24576, 384, 384),
                           (28672, 448, 448), (32768, 512, 512)]:
         p = _plan((1 << 28) // N, N, rs.RS_BF16)
@@ -123,6 +124,16 @@ def test_wide_16bit_softmax_rows_take_the_ring_at_8_units_a_thread():
     # ragged widths round the threads up to whole warps
     p = _plan(8192, 10000, rs.RS_F16, ld=10000)
     assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (160, 8, 480) and _covers(p, 10000)
+    # narrower rows (257 to 768 units): 8 units a thread on a multiple of 256
+    # units, else 6 or 5 units where they fill whole warps exactly (one row a
+    # CTA, two stages), else 8 units on whole warps, one row a CTA
+    for N, shape in [(4096, (64, 8, 512, 3)), (6144, (96, 8, 480, 3)), (2560, (64, 5, 64, 2)),
+                     (3072, (64, 6, 64, 2)), (4608, (96, 6, 96, 2)), (5120, (128, 5, 128, 2)),
+                     (3584, (64, 8, 64, 2)), (5632, (96, 8, 96, 2))]:
+        p = _plan((1 << 29) // N, N, rs.RS_BF16)
+        assert p["path"] == rs.RS_PATH_RING and _covers(p, N), N
+        assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"], p["stages"]) == shape, N
+    assert _plan(1 << 20, 2048, rs.RS_BF16)["vec_per_thread"] == 8  # rows of one warp: their own rule
     # few rows: the clusters as before (each CTA would not loop over its stages)
     assert _plan(64, 32768, rs.RS_BF16)["path"] == rs.RS_PATH_CLUSTER
     assert _plan(4096, 40960, rs.RS_F16)["path"] == rs.RS_PATH_CLUSTER  # over 4096 units

@@ -99,24 +99,29 @@ def test_auto_path_wide_16bit_rows(dtype, N):
     _check(x, _run(x, out=out), what=f"auto wide {dtype} N={N}")
 
 
+# (threads a row, units a thread, threads a CTA, stages) the planner gives
+# 16-bit softmax rows of 257 to 4096 units given enough rows.
+RING16_SHAPES = {2560: (64, 5, 64, 2), 3584: (64, 8, 64, 2), 4096: (64, 8, 512, 3), 4608: (96, 6, 96, 2),
+                 5120: (128, 5, 128, 2), 6200: (128, 8, 512, 3), 10000: (160, 8, 480, 3), 12288: (192, 8, 384, 3),
+                 16384: (256, 8, 512, 3), 24576: (384, 8, 384, 3), 32768: (512, 8, 512, 3)}
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("N", [6200, 10000, 12288, 16384, 24576, 32768])
-def test_wide_16bit_rows_on_the_8_unit_ring(dtype, N):
-    # Where the planner puts wide 16-bit softmax rows given enough rows: the
-    # ring at 8 units a thread, several rows a 512-thread CTA where they fit,
-    # three stages; a ragged last row group; every row against the oracle.
-    units = -(-N // 8)
-    tpr = -(-(-(-units // 8)) // 32) * 32
-    rows_per_cta = 512 // tpr if tpr <= 256 else 1
-    M = rows_per_cta * 4 * 152 + 37
+@pytest.mark.parametrize("N", list(RING16_SHAPES))
+def test_16bit_softmax_rows_on_the_measured_ring_shapes(dtype, N):
+    # Where the planner puts 16-bit softmax rows of 2560 to 32768 values given
+    # enough rows: the ring shapes measured fastest (5, 6 or 8 units a thread);
+    # a ragged last row group; every row against the oracle.
+    tpr, vpt, block, stages = RING16_SHAPES[N]
+    M = (block // tpr) * 4 * 152 + 37
     x, out = _aligned(M, N, dtype, kind="normal_spike", seed=N + 7)
     rc, dev = rs.rowsoftmax_device_info()
     rc, plan = rs.rowsoftmax_plan(x.data_ptr(), out.data_ptr(), M, N, x.stride(0), out.stride(0),
                                   rs.dtype_code(x.dtype), None, dev)
     assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_RING
-    assert (plan["threads_per_row"], plan["vec_per_thread"], plan["stages"]) == (tpr, 8, 3)
+    assert (plan["threads_per_row"], plan["vec_per_thread"], plan["block_threads"], plan["stages"]) == RING16_SHAPES[N]
     y = _run(x, out=out)
-    check_all_rows("softmax", x, y, N, what=f"8-unit ring {dtype} {M}x{N}")
+    check_all_rows("softmax", x, y, N, what=f"ring shape {dtype} {M}x{N}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
