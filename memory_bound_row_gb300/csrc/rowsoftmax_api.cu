@@ -273,11 +273,15 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     //    one CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048
     //    +3.9 %, bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %);
     //  - softmax rows of 257 to 4096 units: ring16_softmax_shape;
-    //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %); of 1537 to
-    //    2048 units: 8 units a thread, 512-thread CTAs (bf16 16384 +24 %);
+    //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %); of 257 to
+    //    768 units that 6 (else 4) units a thread fill on whole warps exactly:
+    //    that shape, one row a CTA (bf16 3072 +4 %, 4096 +8 %, 4608 +13 %, 5120
+    //    +45 %, 6144 +14 %); of 1537 to 2048 units: 8 units a thread,
+    //    512-thread CTAs (bf16 16384 +24 %);
     //  - RMSNorm rows of one warp at 8 units: 512 threads (bf16 2048 +0.8 %);
     //    of 4 warps at 4 units: 128 threads, one row a CTA (bf16 4096 +6.1 %);
-    //    of 8 warps at 4 units: four stages (bf16 8192 +8.3 %).
+    //    of 5 to 7 warps at 4 units: three stages (4608 +4 %, 5120 +3 %, 6144
+    //    +8 %); of 8 warps at 4 units: four stages (bf16 8192 +8.3 %).
     // Not for the causal mask's multi-warp rows (its copy ring serves rows of
     // one warp best).
     int def_stages = kRingDefaultStages;
@@ -298,6 +302,12 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
                 rb.block_threads = 512;
             } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
                 rb.block_threads = 128;
+            } else if (p->op == RS_OP_LAYERNORM && units > 256 && units <= 768 &&
+                       ((units % 6 == 0 && (units / 6) % 32 == 0) || (units % 4 == 0 && (units / 4) % 32 == 0))) {
+                const int v = units % 6 == 0 && (units / 6) % 32 == 0 ? 6 : 4;
+                rb.threads_per_row = (int)(units / v);
+                rb.vec_per_thread = v;
+                rb.block_threads = (int)(units / v);
             } else if (p->op == RS_OP_LAYERNORM && units > 1536 && units <= 2048) {
                 rb.threads_per_row = 256;
                 rb.vec_per_thread = 8;
@@ -308,6 +318,8 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
                 rb.block_threads = 128;
             } else if (p->op == RS_OP_RMSNORM && tpr == 256 && vpt <= 4) {
                 stages_want = 4;
+            } else if (p->op == RS_OP_RMSNORM && tpr > 128 && tpr < 256 && vpt <= 4) {
+                stages_want = 3;
             }
         }
         if (rb.block_threads &&

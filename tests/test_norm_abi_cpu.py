@@ -129,10 +129,11 @@ def test_layernorm_rows_of_4_or_8_warps_hold_their_vectors_in_registers(dtype):
     # instance with weight and bias in registers: 256-thread CTAs, 128
     # registers a thread, so the persistent grid is 2 CTAs an SM, and nothing
     # is staged in shared memory beside the ring stages.
-    for N, tpr in [(4096, 128), (8192, 256)]:
+    # (4096-value rows: one row a 128-thread CTA, 4 CTAs an SM, measured 8 % faster)
+    for N, tpr, block, grid in [(4096, 128, 128, 4 * 152), (8192, 256, 256, 2 * 152)]:
         p = _plan(rs.RS_OP_LAYERNORM, 32768, N, dtype, b=B)
         assert p["path"] == rs.RS_PATH_RING and p["vec_per_thread"] == 4 and p["threads_per_row"] == tpr
-        assert p["block_threads"] == 256 and p["grid"] == 2 * 152
+        assert p["block_threads"] == block and p["grid"] == grid
         assert p["smem_bytes"] == (N // 8) * 16 * p["rows_per_cta"] * p["stages"]
     # rows of 2 warps keep one warp a row (measured faster), RMSNorm keeps its plan,
     # and a ragged row of the same size keeps the staged vectors
@@ -237,3 +238,16 @@ def test_layernorm_16bit_rows_of_2048_units_take_8_units_a_thread():
     assert p["path"] == rs.RS_PATH_RING
     assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (256, 8, 512)
     assert _plan(rs.RS_OP_LAYERNORM, 1024, 16384, rs.RS_BF16, b=B)["vec_per_thread"] == 4
+
+
+def test_16bit_norm_rows_of_257_to_768_units():
+    # LayerNorm rows that 6 (else 4) units a thread fill on whole warps exactly
+    # take that shape, one row a CTA; RMSNorm rows of 5 to 7 warps at 4 units a
+    # thread take three stages (bf16, measured against the previous plans).
+    for N, shape in [(3072, (64, 6, 64)), (4096, (128, 4, 128)), (4608, (96, 6, 96)), (5120, (160, 4, 160)),
+                     (6144, (128, 6, 128))]:
+        p = _plan(rs.RS_OP_LAYERNORM, (1 << 29) // N, N, rs.RS_BF16, b=B)
+        assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == shape
+    for N in (4608, 5120, 6144):
+        p = _plan(rs.RS_OP_RMSNORM, (1 << 29) // N, N, rs.RS_BF16)
+        assert p["vec_per_thread"] == 4 and 128 < p["threads_per_row"] < 256 and p["stages"] == 3, N
