@@ -798,14 +798,19 @@ def run_sweep_n(args):
         torch.cuda.empty_cache()
 
 
-WIDE_SWEEP_N = [8192, 12288, 16384, 20480, 24576, 28672, 32768, 40960, 49152, 65536]
-WIDE_SWEEP_CONFIGS = {"auto": None, "ring": {"path": 4}, "cluster": {"path": 2}}
+WIDE_SWEEP_N = [2560, 3072, 3584, 4096, 4608, 5120, 5632, 6144, 8192, 12288, 16384, 20480, 24576, 28672, 32768,
+                40960, 49152, 65536]
+# "ring4": the ring at 4 units a thread, the shape planned before the measured
+# shapes of the planner (rs_options forcing the units a thread).
+WIDE_SWEEP_CONFIGS = {"auto": None, "ring": {"path": 4}, "ring4": {"path": 4, "vec_per_thread": 4},
+                      "cluster": {"path": 2}}
 
 
 def run_sweep_wide(args):
-    """Wide 16-bit rows (N = 8192..65536, M = 2^28 / N: 512 MB a tensor) for
+    """16-bit rows of 2560..65536 values (M = 2^28 / N: 512 MB a tensor) for
     the --op row operation, through the planner's choice, the bulk-copy ring
-    and the register-holding clusters, where each has a plan.  Every point is
+    (the planner's ring shape, and at 4 units a thread) and the
+    register-holding clusters, where each has a plan.  Every point is
     checked first on 16 sampled rows against the operation evaluated by torch
     in fp64 on the decoded inputs (softmax also: row sums within 1e-2), and the
     configurations against each other; then timed as graph-replayed launches
@@ -904,7 +909,8 @@ def run_sweep_wide(args):
             gbs = nbytes / (ms * 1e-3) / 1e9
             print(json.dumps({"sweep": f"{dt} wide rows, M = 2^28 / N", "op": op, "N": N, "M": M, "config": name,
                               "kernel": rs.PATH_NAMES[plan["path"]], "cluster": plan["cluster_size"],
-                              "threads": plan["block_threads"], "units_a_thread": plan["vec_per_thread"],
+                              "threads": plan["block_threads"], "threads_per_row": plan["threads_per_row"],
+                              "units_a_thread": plan["vec_per_thread"], "stages": plan["stages"],
                               "grid": plan["grid"], "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
                               "frac": round(gbs / peak, 4), "max_rel_err": round(err, 6)}), flush=True)
             del graph
@@ -1085,7 +1091,7 @@ def main():
                     help="instead of the benchmark line: the fp32 M=4096, N=256..12672 sweep of the row softmax, "
                          "one JSON line per (N, kernel configuration)")
     ap.add_argument("--sweep-wide", action="store_true",
-                    help="instead of the benchmark line: wide 16-bit rows (N = 8192..65536) of the --op row "
+                    help="instead of the benchmark line: 16-bit rows (N = 2560..65536) of the --op row "
                          "operation through the planner's choice, the ring and the clusters")
     ap.add_argument("--sweep-dtype", choices=["bf16", "f16"], default="bf16")
     ap.add_argument("--split", action="store_true",
