@@ -196,30 +196,39 @@ int64_t ctas_per_sm(const rs_device_info& dev, int block, size_t smem, int regs_
 // Ring shapes measured for 16-bit softmax rows of 257 to 4096 16-byte units
 // (bf16, 2^28 / N to 2^29 / N rows, graph-replayed, against the 4-unit shape
 // planned otherwise and, from 16384 values, the clusters):
-//  - a multiple of 256 units: 8 units a thread, 512-thread CTAs where a row
-//    takes at most 256 threads (else one row a CTA), three stages (N = 4096
-//    +9 %, 6144 +8 %, 8192 +7.8 %, 12288 +13 %, 16384 +12 %, 20480 +4.4 %,
-//    24576 +3.5 %, 28672 +16 %, 32768 +8.3 %);
-//  - else 6 or 5 units a thread where they fill whole warps exactly: one row
-//    a CTA, two stages (2560 +34 %, 4608 +25 %, 5120 +7.6 %; 3072 -1 %);
+//  - a multiple of 256 units: 8 units a thread, three stages (N = 4096 +9 %,
+//    6144 +8 %, 8192 +7.8 %, 12288 +13 %, 16384 +12 %, 20480 +4.4 %, 24576
+//    +3.5 %, 28672 +16 %, 32768 +8.3 %); several rows a CTA where they fill
+//    448 to 512 threads (4096, 6144, 8192, 16384), else one row a CTA (12288:
+//    two rows in 384 threads measured 7 % slower);
+//  - else 5 units a thread where they fill whole warps exactly, or 6 where
+//    they do and 4 do not: one row a CTA, two stages (2560 +34 %, 4608 +25 %,
+//    5120 +7.6 %; 6 units at 3072, where 4 fill exactly, -1 to -4 %);
 //  - else 8 units a thread on whole warps: rows of up to 768 units one row a
 //    CTA and two stages (3584 +10 %, 5632 +17 %), wider rows as the first case.
 // Given 4 row groups an SM at least, so that every CTA loops over its stages.
 struct RingShape {
     int tpr, vpt, block, stages;
 };
+int ring16_block(int tpr) {
+    const int filled = (512 / tpr) * tpr;
+    return tpr <= 256 && filled >= 448 ? filled : tpr;
+}
 bool ring16_softmax_shape(int64_t units, int64_t M, int sm_count, RingShape* shape) {
     if (units <= 256 || units > 4096) return false;
+    const auto exact = [units](int v) { return units % v == 0 && (units / v) % 32 == 0; };
     RingShape r{};
     if (units % 256 == 0) {
         r.tpr = (int)(units / 8);
         r.vpt = 8;
         r.stages = 3;
-        r.block = r.tpr <= 256 ? (512 / r.tpr) * r.tpr : r.tpr;
-    } else if (units % 6 == 0 && (units / 6) % 32 == 0) {
-        r = {(int)(units / 6), 6, (int)(units / 6), 2};
-    } else if (units % 5 == 0 && (units / 5) % 32 == 0) {
+        r.block = ring16_block(r.tpr);
+    } else if (exact(5)) {
         r = {(int)(units / 5), 5, (int)(units / 5), 2};
+    } else if (exact(6) && !exact(4)) {
+        r = {(int)(units / 6), 6, (int)(units / 6), 2};
+    } else if (exact(4) && units <= 768) {
+        return false;  // the planned 4-unit shape
     } else {
         r.tpr = (int)round_up(ceil_div(units, 8), 32);
         r.vpt = 8;
@@ -227,7 +236,7 @@ bool ring16_softmax_shape(int64_t units, int64_t M, int sm_count, RingShape* sha
             r.block = r.tpr;
             r.stages = 2;
         } else {
-            r.block = r.tpr <= 256 ? (512 / r.tpr) * r.tpr : r.tpr;
+            r.block = ring16_block(r.tpr);
             r.stages = 3;
         }
     }
@@ -276,8 +285,9 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %); of 257 to
     //    768 units that 6 (else 4) units a thread fill on whole warps exactly:
     //    that shape, one row a CTA (bf16 3072 +4 %, 4096 +8 %, 4608 +13 %, 5120
-    //    +45 %, 6144 +14 %); of 1537 to 2048 units: 8 units a thread,
-    //    512-thread CTAs (bf16 16384 +24 %);
+    //    +45 %, 6144 +14 %), the others 4 units a thread (2560 +8 %, 3584 +3 %,
+    //    5632 +24 %); of 1537 to 2048 units: 8 units a thread, 512-thread CTAs
+    //    (bf16 16384 +24 %);
     //  - RMSNorm rows of one warp at 8 units: 512 threads (bf16 2048 +0.8 %);
     //    of 4 warps at 4 units: 128 threads, one row a CTA (bf16 4096 +6.1 %);
     //    of 5 to 7 warps at 4 units: three stages (4608 +4 %, 5120 +3 %, 6144
@@ -302,12 +312,13 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
                 rb.block_threads = 512;
             } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
                 rb.block_threads = 128;
-            } else if (p->op == RS_OP_LAYERNORM && units > 256 && units <= 768 &&
-                       ((units % 6 == 0 && (units / 6) % 32 == 0) || (units % 4 == 0 && (units / 4) % 32 == 0))) {
-                const int v = units % 6 == 0 && (units / 6) % 32 == 0 ? 6 : 4;
-                rb.threads_per_row = (int)(units / v);
+            } else if (p->op == RS_OP_LAYERNORM && units > 256 && units <= 768) {
+                const bool e6 = units % 6 == 0 && (units / 6) % 32 == 0;
+                const bool e4 = units % 4 == 0 && (units / 4) % 32 == 0;
+                const int v = e6 ? 6 : 4;
+                rb.threads_per_row = (int)round_up(ceil_div(units, v), 32);
                 rb.vec_per_thread = v;
-                rb.block_threads = (int)(units / v);
+                rb.block_threads = e6 || e4 ? rb.threads_per_row : 0;  // else the planned CTA size
             } else if (p->op == RS_OP_LAYERNORM && units > 1536 && units <= 2048) {
                 rb.threads_per_row = 256;
                 rb.vec_per_thread = 8;
@@ -322,8 +333,8 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
                 stages_want = 3;
             }
         }
-        if (rb.block_threads &&
-            (rb.block_threads != p->block_threads || rb.threads_per_row != tpr || rb.vec_per_thread != vpt)) {
+        if ((rb.block_threads && rb.block_threads != p->block_threads) ||
+            (rb.threads_per_row && rb.threads_per_row != tpr) || (rb.vec_per_thread && rb.vec_per_thread != vpt)) {
             const rs_plan keep = *p;
             const int want_tpr = rb.threads_per_row ? rb.threads_per_row : tpr;
             const int want_vpt = rb.vec_per_thread ? rb.vec_per_thread : vpt;

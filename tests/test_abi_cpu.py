@@ -115,7 +115,7 @@ def test_16bit_softmax_rows_take_the_measured_ring_shapes():
     # where a row takes at most 256 threads, three stages (faster than the
     # 4-unit ring and than the clusters at every N from 8192 to 32768); given
     # 4 row groups an SM.
-    for N, tpr, block in [(12288, 192, 384), (16384, 256, 512), (20480, 320, 320), (24576, 384, 384),
+    for N, tpr, block in [(12288, 192, 192), (16384, 256, 512), (20480, 320, 320), (24576, 384, 384),
                           (28672, 448, 448), (32768, 512, 512)]:
         p = _plan((1 << 28) // N, N, rs.RS_BF16)
         assert p["path"] == rs.RS_PATH_RING and _covers(p, N), N
@@ -125,10 +125,12 @@ def test_16bit_softmax_rows_take_the_measured_ring_shapes():
     p = _plan(8192, 10000, rs.RS_F16, ld=10000)
     assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (160, 8, 480) and _covers(p, 10000)
     # narrower rows (257 to 768 units): 8 units a thread on a multiple of 256
-    # units, else 6 or 5 units where they fill whole warps exactly (one row a
-    # CTA, two stages), else 8 units on whole warps, one row a CTA
+    # units, else 5 units where they fill whole warps exactly, or 6 where they
+    # do and 4 do not (one row a CTA, two stages), rows that 4 units fill
+    # exactly their planned 4-unit shape, else 8 units on whole warps, one row
+    # a CTA
     for N, shape in [(4096, (64, 8, 512, 3)), (6144, (96, 8, 480, 3)), (2560, (64, 5, 64, 2)),
-                     (3072, (64, 6, 64, 2)), (4608, (96, 6, 96, 2)), (5120, (128, 5, 128, 2)),
+                     (3072, (96, 4, 192, 2)), (4608, (96, 6, 96, 2)), (5120, (128, 5, 128, 2)),
                      (3584, (64, 8, 64, 2)), (5632, (96, 8, 96, 2))]:
         p = _plan((1 << 29) // N, N, rs.RS_BF16)
         assert p["path"] == rs.RS_PATH_RING and _covers(p, N), N

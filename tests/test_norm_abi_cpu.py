@@ -251,3 +251,7 @@ def test_16bit_norm_rows_of_257_to_768_units():
     for N in (4608, 5120, 6144):
         p = _plan(rs.RS_OP_RMSNORM, (1 << 29) // N, N, rs.RS_BF16)
         assert p["vec_per_thread"] == 4 and 128 < p["threads_per_row"] < 256 and p["stages"] == 3, N
+    # LayerNorm rows that neither fills exactly: 4 units a thread, the planned CTA size
+    for N, tpr in [(2560, 96), (3584, 128), (5632, 192)]:
+        p = _plan(rs.RS_OP_LAYERNORM, (1 << 29) // N, N, rs.RS_BF16, b=B)
+        assert (p["threads_per_row"], p["vec_per_thread"]) == (tpr, 4), N

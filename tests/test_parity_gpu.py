@@ -102,7 +102,7 @@ def test_auto_path_wide_16bit_rows(dtype, N):
 # (threads a row, units a thread, threads a CTA, stages) the planner gives
 # 16-bit softmax rows of 257 to 4096 units given enough rows.
 RING16_SHAPES = {2560: (64, 5, 64, 2), 3584: (64, 8, 64, 2), 4096: (64, 8, 512, 3), 4608: (96, 6, 96, 2),
-                 5120: (128, 5, 128, 2), 6200: (128, 8, 512, 3), 10000: (160, 8, 480, 3), 12288: (192, 8, 384, 3),
+                 5120: (128, 5, 128, 2), 6200: (128, 8, 512, 3), 10000: (160, 8, 480, 3), 12288: (192, 8, 192, 3),
                  16384: (256, 8, 512, 3), 24576: (384, 8, 384, 3), 32768: (512, 8, 512, 3)}
 
 
