@@ -403,6 +403,27 @@ def test_nonzero_stream():
     _check("ln", x, y, w, b, what="side stream")
 
 
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [2560, 3072, 3584, 4608, 5120, 5632, 6144, 16384, 4100])
+def test_16bit_norm_rows_on_the_measured_ring_shapes(op, dtype, N):
+    # The planner's measured ring shapes for 16-bit norm rows take effect from
+    # 64 rows an SM: LayerNorm rows of 257 to 768 units at 6 or 4 units a
+    # thread (one row a CTA where they fill exactly), of 1537 to 2048 units at 8
+    # units in 512-thread CTAs, RMSNorm rows of 5 to 7 warps with three stages;
+    # a ragged width; every row against the oracle.
+    M = 64 * 152 + 5
+    x, out = _aligned(M, N, dtype, seed=N + 11)
+    wt, bs = _params(N, dtype, seed=N)
+    ok, plan = _servable(op, x, wt, bs, None)
+    assert ok and plan["path"] == rs.RS_PATH_RING
+    y = _run(op, x, wt, bs, out=out)
+    check_all_rows(op, x, y, N, weight=wt, bias=bs if op == "ln" else None, eps=EPS[op],
+                   what=f"ring shape {'RMSNorm' if op == 'rms' else 'LayerNorm'} {dtype} {M}x{N}")
+    del x, y, out
+    torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------------------
 # The benchmark shapes at full size, in the launch configuration the
 # benchmark times (auto plan, weight and bias present).

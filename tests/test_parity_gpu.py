@@ -124,6 +124,22 @@ def test_16bit_softmax_rows_on_the_measured_ring_shapes(dtype, N):
     check_all_rows("softmax", x, y, N, what=f"ring shape {dtype} {M}x{N}")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [2561, 4100, 6150, 9999, 20000, 32767])
+def test_16bit_softmax_ragged_rows_on_the_ring_shapes(dtype, N):
+    # Ragged widths (a partial last 16-byte unit, read from global memory by
+    # the ring) with enough rows for the planner's measured shapes; every row
+    # against the oracle.
+    M = 8 * 4 * 152 + 5
+    x, out = _aligned(M, N, dtype, kind="normal_spike", seed=N + 3)
+    rc, dev = rs.rowsoftmax_device_info()
+    rc, plan = rs.rowsoftmax_plan(x.data_ptr(), out.data_ptr(), M, N, x.stride(0), out.stride(0),
+                                  rs.dtype_code(x.dtype), None, dev)
+    assert rc == rs.RS_OK and plan["path"] == rs.RS_PATH_RING and plan["vec_per_thread"] >= 5
+    y = _run(x, out=out)
+    check_all_rows("softmax", x, y, N, what=f"ragged ring shape {dtype} {M}x{N}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("tpr,vpt", [(1, 1), (2, 2), (4, 3), (8, 5), (16, 8), (32, 1), (32, 6), (64, 4), (96, 2),
                                      (256, 2), (512, 1), (1024, 1), (160, 8)])
