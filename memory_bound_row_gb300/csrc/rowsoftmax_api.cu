@@ -245,6 +245,15 @@ bool ring16_softmax_shape(int64_t units, int64_t M, int sm_count, RingShape* sha
     return true;
 }
 
+// The causal mask's 16-bit rows of 257 to 4096 units (2049 to 32768 values)
+// on its copy ring: 8 units a thread on whole warps, one row a CTA, two
+// stages (bf16, period = N, 2^28 / N rows, against the 4-unit shape and the
+// clusters planned otherwise: 4096 +36 %, 6000 +19 %, 6144 +33 %, 8192 +31 %,
+// 12288 +17 %, 16384 +21 %, 32768 +22 %), given 4 rows an SM at least.
+bool causal16_ring(int64_t units, int64_t M, int sm_count) {
+    return units > 256 && units <= 4096 && M >= 4 * (int64_t)sm_count;
+}
+
 // RS_PATH_RING.  `nparams` parameter vectors (LayerNorm's weight and bias)
 // are staged in shared memory after the stages, padded to whole units, unless
 // the plan takes a held-parameter instance (vectors in registers).
@@ -292,8 +301,7 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     //    of 4 warps at 4 units: 128 threads, one row a CTA (bf16 4096 +6.1 %);
     //    of 5 to 7 warps at 4 units: three stages (4608 +4 %, 5120 +3 %, 6144
     //    +8 %); of 8 warps at 4 units: four stages (bf16 8192 +8.3 %).
-    // Not for the causal mask's multi-warp rows (its copy ring serves rows of
-    // one warp best).
+    //  - the causal mask's rows of 257 to 4096 units: causal16_ring.
     int def_stages = kRingDefaultStages;
     if (dtype != RS_F32 && values != RS_RING_REREAD && !o.block_threads && !o.threads_per_row &&
         !o.vec_per_thread) {
@@ -307,6 +315,11 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
             rb.vec_per_thread = shape.vpt;
             rb.block_threads = shape.block;
             stages_want = shape.stages;
+        } else if (p->op == RS_OP_SOFTMAX && p->masked && causal16_ring(units, M, dev.sm_count)) {
+            rb.threads_per_row = (int)round_up(ceil_div(units, 8), 32);
+            rb.vec_per_thread = 8;
+            rb.block_threads = rb.threads_per_row;
+            stages_want = 2;
         } else if (many_rows) {
             if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4) {
                 rb.block_threads = 512;
@@ -620,7 +633,8 @@ int validate_and_plan_op(int op, const void* in, const void* out, const void* w,
         RingShape shape16{};
         bool ring = dtype != RS_F32 && vec_ok && N * es >= kRingMinRowBytes &&
                     (norm || N * es < kRowsMaxRowBytes ||
-                     (!masked && ring16_softmax_shape(units, M, dev->sm_count, &shape16)));
+                     (!masked && ring16_softmax_shape(units, M, dev->sm_count, &shape16)) ||
+                     (masked && causal16_ring(units, M, dev->sm_count)));
         if (!ring && !norm && dtype != RS_F32 && vec_ok && N * es < kRingMaxRowBytesSoftmax16) {
             rs_plan cp = *p;
             ring = plan_wide(dtype, RS_PATH_CLUSTER, vec, M, N, o, *dev, &cp) != RS_OK ||

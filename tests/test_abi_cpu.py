@@ -139,10 +139,13 @@ def test_16bit_softmax_rows_take_the_measured_ring_shapes():
     # few rows: the clusters as before (each CTA would not loop over its stages)
     assert _plan(64, 32768, rs.RS_BF16)["path"] == rs.RS_PATH_CLUSTER
     assert _plan(4096, 40960, rs.RS_F16)["path"] == rs.RS_PATH_CLUSTER  # over 4096 units
-    # the causal mask keeps its plans (the copy ring serves rows of one warp best)
-    rc, p = rs.rowsoftmax_causal_plan(A, A + (1 << 40), 8192, 32768, 32768, 32768, 32768, 0, rs.RS_BF16, None,
-                                      gb300())
-    assert rc == rs.RS_OK and p["path"] == rs.RS_PATH_CLUSTER
+    # the causal mask's rows of 257 to 4096 units take its copy ring at 8 units a
+    # thread, one row a CTA, two stages (measured +17 to +36 % from 4096 to 32768)
+    for N in (4096, 6000, 16384, 32768):
+        rc, p = rs.rowsoftmax_causal_plan(A, A + (1 << 40), 8192, N, N, N, N, 0, rs.RS_BF16, None, gb300())
+        tpr = -(-(-(-N // 8) // 8) // 32) * 32
+        assert rc == rs.RS_OK and p["path"] == rs.RS_PATH_RING and p["ring_values"] == rs.RS_RING_THREAD_COPIES
+        assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"], p["stages"]) == (tpr, 8, tpr, 2), N
 
 
 def test_plans_for_the_benchmark_workloads():

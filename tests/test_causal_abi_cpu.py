@@ -42,7 +42,9 @@ def test_shape_errors_match_the_softmax():
 
 
 def test_masked_rows_use_the_same_kernels_as_the_plain_softmax():
-    for M, N, dt in [(1 << 20, 2048, rs.RS_BF16), (8192, 5000, rs.RS_F32), (4096, 4096, rs.RS_F16),
+    # (16-bit rows of 2049 to 32768 values have their own measured shape on the
+    # causal copy ring: test_abi_cpu.py)
+    for M, N, dt in [(1 << 20, 2048, rs.RS_BF16), (8192, 5000, rs.RS_F32), (4096, 2048, rs.RS_F16),
                      (512, 131072, rs.RS_F16)]:
         rc, plain = rs.rowsoftmax_plan(A, OUT, M, N, N, N, dt, None, gb300())
         rc2, masked = _plan(M, N, dt, period=2048)

@@ -183,6 +183,29 @@ def test_kv_cache_offset_layout():
     compare(y, ref, "f16", "kv-cache layout")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [2050, 4096, 6000, 12288, 32768])
+@pytest.mark.parametrize("mask", ["period N", "period 97"])
+def test_causal_16bit_rows_of_2049_to_32768_values_on_the_copy_ring(dtype, N, mask):
+    # The planner's measured shape for the causal mask's 16-bit rows of 257 to
+    # 4096 units: its copy ring at 8 units a thread, one row a CTA; NaN written
+    # into the masked part; every row against the oracle.
+    M = 4 * 152 + 37
+    period, offset = (N, 0) if mask == "period N" else (97, N // 2)
+    x, out = _aligned(M, N, dtype, seed=N + 17)
+    assert _servable(x, period, offset, None)
+    rc, dev = rs.rowsoftmax_device_info()
+    rc, plan = rs.rowsoftmax_causal_plan(x.data_ptr(), out.data_ptr(), M, N, x.stride(0), out.stride(0), period,
+                                         offset, rs.dtype_code(x.dtype), None, dev)
+    assert plan["path"] == rs.RS_PATH_RING and plan["ring_values"] == rs.RS_RING_THREAD_COPIES
+    assert plan["vec_per_thread"] == 8 and plan["block_threads"] == plan["threads_per_row"]
+    xc = x.clone()
+    _garbage(x, period, offset)
+    y = _run(x, period, offset, out=out)
+    check_all_rows("prefix", xc, y, N, period=period, offset=offset,
+                   what=f"causal copy ring {dtype} {M}x{N} {mask}")
+
+
 @pytest.mark.parametrize("path", ["rows", "ring", "ring bulk", "cluster"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_non_finite_values_in_the_kept_prefix(path, dtype):
