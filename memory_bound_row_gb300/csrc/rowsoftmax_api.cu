@@ -254,6 +254,24 @@ bool causal16_ring(int64_t units, int64_t M, int sm_count) {
     return units > 256 && units <= 4096 && M >= 4 * (int64_t)sm_count;
 }
 
+// The causal mask's 16-bit rows of 32 to 256 units (256 to 2048 values) on
+// its copy ring: the fewest lanes (a power of two, at least 4) that hold the
+// row at up to 8 units a thread, 512-thread CTAs, two stages (bf16, period =
+// N, 2^28 / N rows, against the 4-unit shape planned otherwise: 256 +21 %, 512
+// +27 %, 768 +37 %, 1024 +25 %; 1280, 1536 and 2048 keep 32 lanes), given 4
+// row groups an SM.
+bool causal16_narrow(int64_t units, int64_t M, int sm_count, int* tpr, int* vpt) {
+    if (units < 32 || units > 256) return false;
+    int t = 4;
+    while (t * 8 < units) t <<= 1;
+    const int64_t need = ceil_div(units, t);
+    const int v = need <= 2 ? 2 : need <= 3 ? 3 : need <= 4 ? 4 : need <= 5 ? 5 : need <= 6 ? 6 : 8;
+    if (M < (int64_t)(512 / t) * 4 * sm_count) return false;
+    *tpr = t;
+    *vpt = v;
+    return true;
+}
+
 // RS_PATH_RING.  `nparams` parameter vectors (LayerNorm's weight and bias)
 // are staged in shared memory after the stages, padded to whole units, unless
 // the plan takes a held-parameter instance (vectors in registers).
@@ -287,9 +305,14 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     // Shapes measured on the ring's 16-bit rows (graph-replayed, 2^13 to 2^20
     // rows, against the plan above: 256-thread CTAs, two stages, and against
     // the clusters where they were planned):
-    //  - softmax rows of one warp at 4 or more units a thread: 512 threads,
-    //    one CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048
-    //    +3.9 %, bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %);
+    //  - softmax rows of one warp at 4 or 8 units a thread: 512 threads, one
+    //    CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048 +3.9 %,
+    //    bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %; at 5 or 6
+    //    units, 1280 and 1536 values, 256-thread CTAs measured 12 and 4 %
+    //    faster); rows that 16 lanes fill exactly at 4, 5, 6 or 8 units on 16
+    //    lanes, 512-thread CTAs at 4 or 8 units, else 256 (bf16 512 +9 %, 768
+    //    +2.9 %, 1024 +6 % over 32 lanes);
+    //  - the causal mask's rows of 32 to 256 units: causal16_narrow;
     //  - softmax rows of 257 to 4096 units: ring16_softmax_shape;
     //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %); of 257 to
     //    768 units that 6 (else 4) units a thread fill on whole warps exactly:
@@ -320,8 +343,17 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
             rb.vec_per_thread = 8;
             rb.block_threads = rb.threads_per_row;
             stages_want = 2;
+        } else if (p->op == RS_OP_SOFTMAX && p->masked &&
+                   causal16_narrow(units, M, dev.sm_count, &rb.threads_per_row, &rb.vec_per_thread)) {
+            rb.block_threads = 512;
+            stages_want = 2;
         } else if (many_rows) {
-            if (p->op == RS_OP_SOFTMAX && tpr == 32 && vpt >= 4) {
+            if (p->op == RS_OP_SOFTMAX && !p->masked && units % 16 == 0 && units >= 64 && units <= 128 &&
+                units != 112) {
+                rb.threads_per_row = 16;
+                rb.vec_per_thread = (int)(units / 16);
+                rb.block_threads = rb.vec_per_thread == 4 || rb.vec_per_thread == 8 ? 512 : 256;
+            } else if (p->op == RS_OP_SOFTMAX && tpr == 32 && (vpt == 4 || vpt == 8)) {
                 rb.block_threads = 512;
             } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
                 rb.block_threads = 128;

@@ -354,15 +354,27 @@ def test_ctypes_structs_match_the_c_header(cls):
 
 def test_ring_cta_sizes_for_16bit_rows():
     # Measured CTA sizes of the ring on 16-bit rows (graph-replayed, 2^18 to
-    # 2^20 rows): softmax rows of one warp at 4 or more units a thread take
-    # 512-thread CTAs (one an SM, 16 rows a stage; bf16 2048 +3.3 %, bf16 1024
-    # +6.1 %), LayerNorm rows of one warp 128 threads; rows of 8 warps and
+    # 2^20 rows): softmax rows of one warp at 4 or 8 units a thread take
+    # 512-thread CTAs (one an SM, 16 rows a stage; bf16 2048 +3.3 %), rows of
+    # 64 or 128 units 16 lanes in 512-thread CTAs (bf16 512 +9 %, 1024 +6 %),
+    # rows of one warp at 5 or 6 units 256 threads (1280: 512 threads measured
+    # 12 % slower); LayerNorm rows of one warp 128 threads; rows of 8 warps and
     # problems of fewer than 64 rows an SM keep 256.
-    for N, vpt, per_sm in [(1024, 4, 2), (2048, 8, 1)]:  # 64 or 128 registers a thread
+    for N, tpr, vpt, rows_per_cta in [(512, 16, 4, 32), (1024, 16, 8, 32), (2048, 32, 8, 16)]:
         for dt in (rs.RS_BF16, rs.RS_F16):
             p = _plan(1 << 20, N, dt)
-            assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"]) == (32, vpt)
-            assert p["block_threads"] == 512 and p["rows_per_cta"] == 16 and p["grid"] == per_sm * 152, (N, dt)
+            assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"]) == (tpr, vpt)
+            assert p["block_threads"] == 512 and p["rows_per_cta"] == rows_per_cta and p["grid"] % 152 == 0, (N, dt)
+    for N in (1280, 1536):
+        assert _plan(1 << 20, N, rs.RS_BF16)["block_threads"] == 256
+    p = _plan(1 << 20, 768, rs.RS_BF16)  # 16 lanes at 6 units: 256-thread CTAs (+2.9 % over 32 lanes x 3)
+    assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (16, 6, 256)
+    # the causal mask's rows of 32 to 256 units: the fewest lanes that hold the
+    # row at up to 8 units a thread, 512-thread CTAs (bf16 512 +27 %, 1024 +25 %)
+    for N, tpr, vpt in [(256, 4, 8), (512, 8, 8), (768, 16, 6), (1024, 16, 8), (1280, 32, 5), (2048, 32, 8)]:
+        rc, p = rs.rowsoftmax_causal_plan(A, A + (1 << 40), 1 << 20, N, N, N, N, 0, rs.RS_BF16, None, gb300())
+        assert rc == rs.RS_OK and p["ring_values"] == rs.RS_RING_THREAD_COPIES
+        assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (tpr, vpt, 512), N
     assert _plan(1 << 20, 2048, rs.RS_BF16, opts={"block_threads": 256})["block_threads"] == 256
     assert _plan(64 * 152 - 1, 2048, rs.RS_BF16)["block_threads"] == 256  # few rows: unchanged
     # rows of 769 to 1024 units: 4 warps a row at 8 units a thread, 512-thread

@@ -184,6 +184,25 @@ def test_kv_cache_offset_layout():
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N,tpr", [(256, 4), (300, 8), (512, 8), (768, 16), (1024, 16)])
+def test_causal_narrow_16bit_rows_on_few_lanes(dtype, N, tpr):
+    # The causal mask's rows of 32 to 256 units: the fewest lanes that hold the
+    # row at up to 8 units a thread, 512-thread CTAs, enough rows for the rule;
+    # NaN in the masked part; every row against the oracle.
+    M = (512 // tpr) * 4 * 152 + 37
+    x, out = _aligned(M, N, dtype, seed=N + 19)
+    rc, dev = rs.rowsoftmax_device_info()
+    rc, plan = rs.rowsoftmax_causal_plan(x.data_ptr(), out.data_ptr(), M, N, x.stride(0), out.stride(0), N, 0,
+                                         rs.dtype_code(x.dtype), None, dev)
+    assert rc == rs.RS_OK and plan["ring_values"] == rs.RS_RING_THREAD_COPIES
+    assert plan["threads_per_row"] == tpr and plan["block_threads"] == 512
+    xc = x.clone()
+    _garbage(x, N, 0)
+    y = _run(x, N, 0, out=out)
+    check_all_rows("prefix", xc, y, N, period=N, offset=0, what=f"causal narrow rows {dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("N", [2050, 4096, 6000, 12288, 32768])
 @pytest.mark.parametrize("mask", ["period N", "period 97"])
 def test_causal_16bit_rows_of_2049_to_32768_values_on_the_copy_ring(dtype, N, mask):

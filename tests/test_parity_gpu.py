@@ -125,6 +125,21 @@ def test_16bit_softmax_rows_on_the_measured_ring_shapes(dtype, N):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [512, 768, 1024])
+def test_16bit_softmax_rows_of_64_to_128_units_on_16_lanes(dtype, N):
+    # Rows that 16 lanes fill exactly (64, 96, 128 units) on 16 lanes, two rows
+    # a warp, given enough rows; every row against the oracle.
+    M = 32 * 4 * 152 + 37
+    x, out = _aligned(M, N, dtype, kind="normal_spike", seed=N + 5)
+    rc, dev = rs.rowsoftmax_device_info()
+    rc, plan = rs.rowsoftmax_plan(x.data_ptr(), out.data_ptr(), M, N, x.stride(0), out.stride(0),
+                                  rs.dtype_code(x.dtype), None, dev)
+    assert rc == rs.RS_OK and plan["threads_per_row"] == 16
+    y = _run(x, out=out)
+    check_all_rows("softmax", x, y, N, what=f"16-lane rows {dtype} {M}x{N}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("N", [2561, 4100, 6150, 9999, 20000, 32767])
 def test_16bit_softmax_ragged_rows_on_the_ring_shapes(dtype, N):
     # Ragged widths (a partial last 16-byte unit, read from global memory by
