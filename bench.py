@@ -798,8 +798,8 @@ def run_sweep_n(args):
         torch.cuda.empty_cache()
 
 
-WIDE_SWEEP_N = [2560, 3072, 3584, 4096, 4608, 5120, 5632, 6144, 8192, 12288, 16384, 20480, 24576, 28672, 32768,
-                40960, 49152, 65536]
+WIDE_SWEEP_N = [256, 512, 768, 1024, 1280, 1536, 2048, 2560, 3072, 3584, 4096, 4608, 5120, 5632, 6144, 8192, 12288,
+                16384, 20480, 24576, 28672, 32768, 40960, 49152, 65536]
 # "ring4": the ring at 4 units a thread, the shape planned before the measured
 # shapes of the planner (rs_options forcing the units a thread).
 WIDE_SWEEP_CONFIGS = {"auto": None, "ring": {"path": 4}, "ring4": {"path": 4, "vec_per_thread": 4},
@@ -807,14 +807,18 @@ WIDE_SWEEP_CONFIGS = {"auto": None, "ring": {"path": 4}, "ring4": {"path": 4, "v
 
 
 def run_sweep_wide(args):
-    """16-bit rows of 2560..65536 values (M = 2^28 / N: 512 MB a tensor) for
+    """16-bit rows of 256..65536 values (M = 2^28 / N: 512 MB a tensor) for
     the --op row operation, through the planner's choice, the bulk-copy ring
     (the planner's ring shape, and at 4 units a thread) and the
-    register-holding clusters, where each has a plan.  Every point is
-    checked first on 16 sampled rows against the operation evaluated by torch
-    in fp64 on the decoded inputs (softmax also: row sums within 1e-2), and the
-    configurations against each other; then timed as graph-replayed launches
-    over rotating buffers.  One JSON line per (N, configuration)."""
+    register-holding clusters, where each has a plan; with --causal, the
+    softmax under a causal mask of period N (row r keeps r mod N + 1 values;
+    GB/s then count the kept values read and all values written).  Every
+    point is checked first on 16 sampled rows against the operation evaluated
+    by torch in fp64 on the decoded inputs (softmax also: row sums within
+    1e-2), and the configurations against each other; then timed as
+    graph-replayed launches over rotating buffers.  One JSON line per (N,
+    configuration)."""
+    import numpy as np
     import torch
 
     import memory_bound_row_gb300 as rs
@@ -826,6 +830,7 @@ def run_sweep_wide(args):
     peak, _ = measured_peaks()
     rc, info = rs.rowsoftmax_device_info()
     op, dt = args.op, args.sweep_dtype
+    causal = args.causal and op == "softmax"
     code = {"f16": rs.RS_F16, "bf16": rs.RS_BF16}[dt]
     tol = {"f16": 2.0 ** -9, "bf16": 2.0 ** -6}[dt]  # a few units in the last place of the output
     for N in WIDE_SWEEP_N:
@@ -839,7 +844,11 @@ def run_sweep_wide(args):
         ys = [torch.empty_like(x0) for _ in range(nsets)]
         rows = torch.linspace(0, M - 1, 16, device=dev).long()
         xr = x0[rows].double()
-        if op == "softmax":
+        if causal:  # row r keeps its first r mod N + 1 values, the rest is 0
+            keep = (rows % N + 1)[:, None]
+            cols = torch.arange(N, device=dev)[None, :]
+            ref = torch.softmax(xr.masked_fill(cols >= keep, -math.inf), dim=1)
+        elif op == "softmax":
             ref = torch.softmax(xr, dim=1)
         elif op == "rmsnorm":
             ref = xr * torch.rsqrt((xr * xr).mean(dim=1, keepdim=True) + OP_EPS[op]) * wt.double()
@@ -851,7 +860,10 @@ def run_sweep_wide(args):
         first = None
         for name, opts in WIDE_SWEEP_CONFIGS.items():
             copts = rs._abi._opts(opts)
-            if op == "softmax":
+            if causal:
+                rc, plan = rs.rowsoftmax_causal_plan(xs[0].data_ptr(), ys[0].data_ptr(), M, N, N, N, N, 0, code,
+                                                     opts, info)
+            elif op == "softmax":
                 rc, plan = rs.rowsoftmax_plan(xs[0].data_ptr(), ys[0].data_ptr(), M, N, N, N, code, opts, info)
             else:
                 rc, plan = rs.rownorm_plan(OP_CODES[op], xs[0].data_ptr(), ys[0].data_ptr(), wt.data_ptr(),
@@ -864,7 +876,10 @@ def run_sweep_wide(args):
             pb = bs.data_ptr() if op == "layernorm" else None
 
             def call(k):
-                if op == "softmax":
+                if causal:
+                    r = lib.rowsoftmax_causal_fwd_ex(xs[k % nsets].data_ptr(), ys[k % nsets].data_ptr(), M, N, N, N,
+                                                     N, 0, code, h, copts)
+                elif op == "softmax":
                     r = lib.rowsoftmax_fwd_ex(xs[k % nsets].data_ptr(), ys[k % nsets].data_ptr(), M, N, N, N, code,
                                               h, copts)
                 else:
@@ -906,8 +921,12 @@ def run_sweep_wide(args):
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / (reps * G)
             nbytes = 2 * M * N * 2 + {"softmax": 0, "rmsnorm": 1, "layernorm": 2}[op] * N * 2
+            if causal:  # kept values read, all written
+                kept = int(np.minimum(np.arange(M, dtype=np.int64) % N + 1, N).sum())
+                nbytes = (kept + M * N) * 2
             gbs = nbytes / (ms * 1e-3) / 1e9
-            print(json.dumps({"sweep": f"{dt} wide rows, M = 2^28 / N", "op": op, "N": N, "M": M, "config": name,
+            print(json.dumps({"sweep": f"{dt} rows, M = 2^28 / N" + (", causal mask of period N" if causal else ""),
+                              "op": op, "N": N, "M": M, "config": name,
                               "kernel": rs.PATH_NAMES[plan["path"]], "cluster": plan["cluster_size"],
                               "threads": plan["block_threads"], "threads_per_row": plan["threads_per_row"],
                               "units_a_thread": plan["vec_per_thread"], "stages": plan["stages"],
@@ -1091,8 +1110,9 @@ def main():
                     help="instead of the benchmark line: the fp32 M=4096, N=256..12672 sweep of the row softmax, "
                          "one JSON line per (N, kernel configuration)")
     ap.add_argument("--sweep-wide", action="store_true",
-                    help="instead of the benchmark line: 16-bit rows (N = 2560..65536) of the --op row "
-                         "operation through the planner's choice, the ring and the clusters")
+                    help="instead of the benchmark line: 16-bit rows (N = 256..65536) of the --op row "
+                         "operation through the planner's choice, the ring and the clusters (with --causal: the "
+                         "causal softmax, mask period N)")
     ap.add_argument("--sweep-dtype", choices=["bf16", "f16"], default="bf16")
     ap.add_argument("--split", action="store_true",
                     help="instead of the benchmark line: the split-row softmax (few wide rows through "
