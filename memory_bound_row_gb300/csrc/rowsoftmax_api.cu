@@ -246,10 +246,11 @@ bool ring16_softmax_shape(int64_t units, int64_t M, int sm_count, RingShape* sha
 }
 
 // The causal mask's 16-bit rows of 257 to 4096 units (2049 to 32768 values)
-// on its copy ring: 8 units a thread on whole warps, one row a CTA, two
-// stages (bf16, period = N, 2^28 / N rows, against the 4-unit shape and the
-// clusters planned otherwise: 4096 +36 %, 6000 +19 %, 6144 +33 %, 8192 +31 %,
-// 12288 +17 %, 16384 +21 %, 32768 +22 %), given 4 rows an SM at least.
+// on its copy ring: 8 units a thread on whole warps (or 5 or 6 where they
+// fill whole warps exactly and 8 do not), one row a CTA, two stages (bf16,
+// period = N, 2^28 / N rows, against the 4-unit shape and the clusters
+// planned otherwise: 4096 +36 %, 6000 +19 %, 6144 +33 %, 8192 +31 %, 12288
+// +17 %, 16384 +21 %, 32768 +22 %), given 4 rows an SM at least.
 bool causal16_ring(int64_t units, int64_t M, int sm_count) {
     return units > 256 && units <= 4096 && M >= 4 * (int64_t)sm_count;
 }
@@ -314,7 +315,9 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
     //    +2.9 %, 1024 +6 % over 32 lanes);
     //  - the causal mask's rows of 32 to 256 units: causal16_narrow;
     //  - softmax rows of 257 to 4096 units: ring16_softmax_shape;
-    //  - LayerNorm rows of one warp: 128 threads (bf16 2048 +5.8 %); of 257 to
+    //  - LayerNorm rows of 32 to 128 units: about 4 units a thread on the
+    //    fewest lanes that hold them; rows of one warp: 128 threads (bf16 2048
+    //    +5.8 %); of 257 to
     //    768 units that 6 (else 4) units a thread fill on whole warps exactly:
     //    that shape, one row a CTA (bf16 3072 +4 %, 4096 +8 %, 4608 +13 %, 5120
     //    +45 %, 6144 +14 %), the others 4 units a thread (2560 +8 %, 3584 +3 %,
@@ -339,8 +342,13 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
             rb.block_threads = shape.block;
             stages_want = shape.stages;
         } else if (p->op == RS_OP_SOFTMAX && p->masked && causal16_ring(units, M, dev.sm_count)) {
-            rb.threads_per_row = (int)round_up(ceil_div(units, 8), 32);
-            rb.vec_per_thread = 8;
+            // 8 units a thread where they fill whole warps exactly, else 5 or 6
+            // where those do (2560 +47 %, 3072 +35 %, 4608 +34 %, 5120 +15 %
+            // over 8 units on rounded-up warps), else 8 on whole warps
+            const auto exact = [units](int v) { return units % v == 0 && (units / v) % 32 == 0; };
+            const int v = exact(8) ? 8 : exact(5) ? 5 : exact(6) ? 6 : 8;
+            rb.threads_per_row = (int)round_up(ceil_div(units, v), 32);
+            rb.vec_per_thread = v;
             rb.block_threads = rb.threads_per_row;
             stages_want = 2;
         } else if (p->op == RS_OP_SOFTMAX && p->masked &&
@@ -355,6 +363,14 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
                 rb.block_threads = rb.vec_per_thread == 4 || rb.vec_per_thread == 8 ? 512 : 256;
             } else if (p->op == RS_OP_SOFTMAX && tpr == 32 && (vpt == 4 || vpt == 8)) {
                 rb.block_threads = 512;
+            } else if (p->op == RS_OP_LAYERNORM && units >= 32 && units <= 128) {
+                // about 4 units a thread on the fewest lanes that hold the row
+                // (256 +24 %, 512 +11 %, 768 +12 %, 1024 +2.8 % over 8 units)
+                int t = 8;
+                while (t < 32 && t * 4 < units) t <<= 1;
+                rb.threads_per_row = t;
+                rb.vec_per_thread = (int)ceil_div(units, t);
+                rb.block_threads = 256;
             } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
                 rb.block_threads = 128;
             } else if (p->op == RS_OP_LAYERNORM && units > 256 && units <= 768) {

@@ -203,7 +203,7 @@ def test_causal_narrow_16bit_rows_on_few_lanes(dtype, N, tpr):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("N", [2050, 4096, 6000, 12288, 32768])
+@pytest.mark.parametrize("N", [2050, 2560, 3072, 4096, 4608, 5120, 6000, 12288, 32768])
 @pytest.mark.parametrize("mask", ["period N", "period 97"])
 def test_causal_16bit_rows_of_2049_to_32768_values_on_the_copy_ring(dtype, N, mask):
     # The planner's measured shape for the causal mask's 16-bit rows of 257 to
@@ -217,7 +217,7 @@ def test_causal_16bit_rows_of_2049_to_32768_values_on_the_copy_ring(dtype, N, ma
     rc, plan = rs.rowsoftmax_causal_plan(x.data_ptr(), out.data_ptr(), M, N, x.stride(0), out.stride(0), period,
                                          offset, rs.dtype_code(x.dtype), None, dev)
     assert plan["path"] == rs.RS_PATH_RING and plan["ring_values"] == rs.RS_RING_THREAD_COPIES
-    assert plan["vec_per_thread"] == 8 and plan["block_threads"] == plan["threads_per_row"]
+    assert plan["vec_per_thread"] in (5, 6, 8) and plan["block_threads"] == plan["threads_per_row"]
     xc = x.clone()
     _garbage(x, period, offset)
     y = _run(x, period, offset, out=out)

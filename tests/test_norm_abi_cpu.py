@@ -255,3 +255,11 @@ def test_16bit_norm_rows_of_257_to_768_units():
     for N, tpr in [(2560, 96), (3584, 128), (5632, 192)]:
         p = _plan(rs.RS_OP_LAYERNORM, (1 << 29) // N, N, rs.RS_BF16, b=B)
         assert (p["threads_per_row"], p["vec_per_thread"]) == (tpr, 4), N
+
+
+def test_16bit_layernorm_rows_of_32_to_128_units_hold_about_4_units_a_thread():
+    # the fewest lanes (8 to 32) that hold the row at about 4 units a thread
+    # (bf16 256 +24 %, 512 +11 %, 768 +12 %, 1024 +2.8 % over 8 units a thread)
+    for N, tpr, vpt in [(256, 8, 4), (512, 16, 4), (768, 32, 3), (1024, 32, 4)]:
+        p = _plan(rs.RS_OP_LAYERNORM, (1 << 28) // N, N, rs.RS_BF16, b=B)
+        assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"]) == (tpr, vpt), N
