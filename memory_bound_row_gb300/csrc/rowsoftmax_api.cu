@@ -273,6 +273,106 @@ bool causal16_narrow(int64_t units, int64_t M, int sm_count, int* tpr, int* vpt)
     return true;
 }
 
+// Shapes measured for the ring's 16-bit rows, against the first-guess plan
+// (about 32 values a thread, 256-thread CTAs, two stages) and, where they
+// were planned, the clusters: bf16 rows, 2^13 to 2^20 of them, graph-replayed
+// in one call, every shape checked against the oracle first.  `want` gets the
+// threads a row, units a thread, CTA size and stages to take (0: as planned);
+// false where the first guess stands.
+//
+// softmax      rows of one warp at 4 or 8 units a thread: 512-thread CTAs
+//              (2048 values +3.3 %; at 5 or 6 units 256-thread CTAs measured
+//              4-12 % faster); rows that 16 lanes fill exactly at 4-8 units:
+//              16 lanes, 512-thread CTAs at 4 or 8 units, else 256 (512 +9 %,
+//              768 +2.9 %, 1024 +6 %); rows of 257 to 4096 units:
+//              ring16_softmax_shape (+4 to +34 % from 2560 to 32768 values);
+// causal mask  rows of 32 to 256 units: causal16_narrow (+21 to +37 %); of 257
+//              to 4096 units: its copy ring at 8 units a thread (5 or 6 where
+//              they fill whole warps exactly and 8 do not), one row a CTA, two
+//              stages (+15 to +47 % from 2560 to 32768 values);
+// LayerNorm    rows of 32 to 128 units: about 4 units a thread on the fewest
+//              lanes that hold them (+3 to +24 %); rows of one warp: 128-thread
+//              CTAs (2048 +5.8 %); 257 to 768 units: 6 (else 4) units a thread,
+//              one row a CTA where they fill whole warps exactly, else 4 units
+//              (+3 to +45 %); 1537 to 2048 units: 8 units a thread, 512-thread
+//              CTAs (16384 +24 %);
+// RMSNorm      rows of one warp at 8 units: 512-thread CTAs (+0.8 %); 4 warps at
+//              4 units: one row a 128-thread CTA (4096 +6.1 %); 5 to 7 warps at
+//              4 units: three stages (+3 to +8 %); 8 warps at 4 units: four
+//              stages (8192 +8.3 %).
+// The rules other than the causal and the wide softmax ones apply from 64
+// rows an SM, so that every CTA loops over its stages.
+struct ShapeWant {
+    int tpr, vpt, block, stages;
+};
+bool measured_ring_shape(const rs_plan& p, int64_t units, int64_t M, int sm_count, ShapeWant* w) {
+    const int tpr = p.threads_per_row, vpt = p.vec_per_thread;
+    const auto fills = [units](int lanes, int v) { return units % v == 0 && (units / v) % lanes == 0; };
+    *w = ShapeWant{0, 0, 0, 0};
+    if (p.op == RS_OP_SOFTMAX && !p.masked) {
+        RingShape r{};
+        if (ring16_softmax_shape(units, M, sm_count, &r)) {
+            *w = ShapeWant{r.tpr, r.vpt, r.block, r.stages};
+            return true;
+        }
+    } else if (p.op == RS_OP_SOFTMAX && causal16_ring(units, M, sm_count)) {
+        const int v = fills(32, 8) ? 8 : fills(32, 5) ? 5 : fills(32, 6) ? 6 : 8;
+        const int t = (int)round_up(ceil_div(units, v), 32);
+        *w = ShapeWant{t, v, t, 2};
+        return true;
+    } else if (p.op == RS_OP_SOFTMAX) {
+        int t = 0, v = 0;
+        if (causal16_narrow(units, M, sm_count, &t, &v)) {
+            *w = ShapeWant{t, v, 512, 2};
+            return true;
+        }
+    }
+    if (M < (int64_t)64 * sm_count) return false;
+    if (p.op == RS_OP_SOFTMAX) {
+        const int v16 = !p.masked && units >= 64 && units <= 128 && units % 16 == 0 ? (int)(units / 16) : 0;
+        if (v16 == 4 || v16 == 5 || v16 == 6 || v16 == 8) {
+            *w = ShapeWant{16, v16, v16 == 4 || v16 == 8 ? 512 : 256, 0};
+            return true;
+        }
+        if (tpr == 32 && (vpt == 4 || vpt == 8)) {
+            *w = ShapeWant{0, 0, 512, 0};
+            return true;
+        }
+        return false;
+    }
+    if (p.op == RS_OP_LAYERNORM) {
+        if (units >= 32 && units <= 128) {
+            int t = 8;
+            while (t < 32 && t * 4 < units) t <<= 1;
+            *w = ShapeWant{t, (int)ceil_div(units, t), 256, 0};
+            return true;
+        }
+        if (tpr == 32) {
+            *w = ShapeWant{0, 0, 128, 0};
+            return true;
+        }
+        if (units > 256 && units <= 768) {
+            const bool e6 = fills(32, 6), e4 = fills(32, 4);
+            const int v = e6 ? 6 : 4;
+            const int t = (int)round_up(ceil_div(units, v), 32);
+            *w = ShapeWant{t, v, e6 || e4 ? t : 0, 0};
+            return true;
+        }
+        if (units > 1536 && units <= 2048) {
+            *w = ShapeWant{256, 8, 512, 0};
+            return true;
+        }
+        return false;
+    }
+    // RMSNorm
+    if (tpr == 32 && vpt == 8) *w = ShapeWant{0, 0, 512, 0};
+    else if (tpr == 128 && vpt <= 4) *w = ShapeWant{0, 0, 128, 0};
+    else if (tpr == 256 && vpt <= 4) *w = ShapeWant{0, 0, 0, 4};
+    else if (tpr > 128 && tpr < 256 && vpt <= 4) *w = ShapeWant{0, 0, 0, 3};
+    else return false;
+    return true;
+}
+
 // RS_PATH_RING.  `nparams` parameter vectors (LayerNorm's weight and bias)
 // are staged in shared memory after the stages, padded to whole units, unless
 // the plan takes a held-parameter instance (vectors in registers).
@@ -303,109 +403,28 @@ int plan_ring(int dtype, int vec, int64_t M, int64_t N, int64_t units, const rs_
         ro.vec_per_thread = 4;
     int rc = plan_rows(dtype, vec, M, units, ro, p, values != RS_RING_REREAD);
     if (rc != RS_OK) return rc;
-    // Shapes measured on the ring's 16-bit rows (graph-replayed, 2^13 to 2^20
-    // rows, against the plan above: 256-thread CTAs, two stages, and against
-    // the clusters where they were planned):
-    //  - softmax rows of one warp at 4 or 8 units a thread: 512 threads, one
-    //    CTA an SM with 16 rows a stage (bf16 2048 +3.3 %, fp16 2048 +3.9 %,
-    //    bf16 1024 +6.1 %, the causal copy ring on bf16 2048 +0.6 %; at 5 or 6
-    //    units, 1280 and 1536 values, 256-thread CTAs measured 12 and 4 %
-    //    faster); rows that 16 lanes fill exactly at 4, 5, 6 or 8 units on 16
-    //    lanes, 512-thread CTAs at 4 or 8 units, else 256 (bf16 512 +9 %, 768
-    //    +2.9 %, 1024 +6 % over 32 lanes);
-    //  - the causal mask's rows of 32 to 256 units: causal16_narrow;
-    //  - softmax rows of 257 to 4096 units: ring16_softmax_shape;
-    //  - LayerNorm rows of 32 to 128 units: about 4 units a thread on the
-    //    fewest lanes that hold them; rows of one warp: 128 threads (bf16 2048
-    //    +5.8 %); of 257 to
-    //    768 units that 6 (else 4) units a thread fill on whole warps exactly:
-    //    that shape, one row a CTA (bf16 3072 +4 %, 4096 +8 %, 4608 +13 %, 5120
-    //    +45 %, 6144 +14 %), the others 4 units a thread (2560 +8 %, 3584 +3 %,
-    //    5632 +24 %); of 1537 to 2048 units: 8 units a thread, 512-thread CTAs
-    //    (bf16 16384 +24 %);
-    //  - RMSNorm rows of one warp at 8 units: 512 threads (bf16 2048 +0.8 %);
-    //    of 4 warps at 4 units: 128 threads, one row a CTA (bf16 4096 +6.1 %);
-    //    of 5 to 7 warps at 4 units: three stages (4608 +4 %, 5120 +3 %, 6144
-    //    +8 %); of 8 warps at 4 units: four stages (bf16 8192 +8.3 %).
-    //  - the causal mask's rows of 257 to 4096 units: causal16_ring.
+    // The shapes measured for 16-bit rows (measured_ring_shape), unless the
+    // caller forced one.
     int def_stages = kRingDefaultStages;
+    ShapeWant want{};
     if (dtype != RS_F32 && values != RS_RING_REREAD && !o.block_threads && !o.threads_per_row &&
-        !o.vec_per_thread) {
+        !o.vec_per_thread && measured_ring_shape(*p, units, M, dev.sm_count, &want)) {
         const int tpr = p->threads_per_row, vpt = p->vec_per_thread;
-        const bool many_rows = M >= (int64_t)64 * dev.sm_count;  // every CTA loops over stages
         rs_options rb = ro;
-        int stages_want = 0;
-        RingShape shape{};
-        if (p->op == RS_OP_SOFTMAX && !p->masked && ring16_softmax_shape(units, M, dev.sm_count, &shape)) {
-            rb.threads_per_row = shape.tpr;
-            rb.vec_per_thread = shape.vpt;
-            rb.block_threads = shape.block;
-            stages_want = shape.stages;
-        } else if (p->op == RS_OP_SOFTMAX && p->masked && causal16_ring(units, M, dev.sm_count)) {
-            // 8 units a thread where they fill whole warps exactly, else 5 or 6
-            // where those do (2560 +47 %, 3072 +35 %, 4608 +34 %, 5120 +15 %
-            // over 8 units on rounded-up warps), else 8 on whole warps
-            const auto exact = [units](int v) { return units % v == 0 && (units / v) % 32 == 0; };
-            const int v = exact(8) ? 8 : exact(5) ? 5 : exact(6) ? 6 : 8;
-            rb.threads_per_row = (int)round_up(ceil_div(units, v), 32);
-            rb.vec_per_thread = v;
-            rb.block_threads = rb.threads_per_row;
-            stages_want = 2;
-        } else if (p->op == RS_OP_SOFTMAX && p->masked &&
-                   causal16_narrow(units, M, dev.sm_count, &rb.threads_per_row, &rb.vec_per_thread)) {
-            rb.block_threads = 512;
-            stages_want = 2;
-        } else if (many_rows) {
-            if (p->op == RS_OP_SOFTMAX && !p->masked && units % 16 == 0 && units >= 64 && units <= 128 &&
-                units != 112) {
-                rb.threads_per_row = 16;
-                rb.vec_per_thread = (int)(units / 16);
-                rb.block_threads = rb.vec_per_thread == 4 || rb.vec_per_thread == 8 ? 512 : 256;
-            } else if (p->op == RS_OP_SOFTMAX && tpr == 32 && (vpt == 4 || vpt == 8)) {
-                rb.block_threads = 512;
-            } else if (p->op == RS_OP_LAYERNORM && units >= 32 && units <= 128) {
-                // about 4 units a thread on the fewest lanes that hold the row
-                // (256 +24 %, 512 +11 %, 768 +12 %, 1024 +2.8 % over 8 units)
-                int t = 8;
-                while (t < 32 && t * 4 < units) t <<= 1;
-                rb.threads_per_row = t;
-                rb.vec_per_thread = (int)ceil_div(units, t);
-                rb.block_threads = 256;
-            } else if (p->op == RS_OP_LAYERNORM && tpr == 32) {
-                rb.block_threads = 128;
-            } else if (p->op == RS_OP_LAYERNORM && units > 256 && units <= 768) {
-                const bool e6 = units % 6 == 0 && (units / 6) % 32 == 0;
-                const bool e4 = units % 4 == 0 && (units / 4) % 32 == 0;
-                const int v = e6 ? 6 : 4;
-                rb.threads_per_row = (int)round_up(ceil_div(units, v), 32);
-                rb.vec_per_thread = v;
-                rb.block_threads = e6 || e4 ? rb.threads_per_row : 0;  // else the planned CTA size
-            } else if (p->op == RS_OP_LAYERNORM && units > 1536 && units <= 2048) {
-                rb.threads_per_row = 256;
-                rb.vec_per_thread = 8;
-                rb.block_threads = 512;
-            } else if (p->op == RS_OP_RMSNORM && tpr == 32 && vpt == 8) {
-                rb.block_threads = 512;
-            } else if (p->op == RS_OP_RMSNORM && tpr == 128 && vpt <= 4) {
-                rb.block_threads = 128;
-            } else if (p->op == RS_OP_RMSNORM && tpr == 256 && vpt <= 4) {
-                stages_want = 4;
-            } else if (p->op == RS_OP_RMSNORM && tpr > 128 && tpr < 256 && vpt <= 4) {
-                stages_want = 3;
-            }
-        }
-        if ((rb.block_threads && rb.block_threads != p->block_threads) ||
-            (rb.threads_per_row && rb.threads_per_row != tpr) || (rb.vec_per_thread && rb.vec_per_thread != vpt)) {
+        if (want.tpr) rb.threads_per_row = want.tpr;
+        if (want.vpt) rb.vec_per_thread = want.vpt;
+        if (want.block) rb.block_threads = want.block;
+        bool ok = true;
+        if ((want.block && want.block != p->block_threads) || (want.tpr && want.tpr != tpr) ||
+            (want.vpt && want.vpt != vpt)) {
             const rs_plan keep = *p;
-            const int want_tpr = rb.threads_per_row ? rb.threads_per_row : tpr;
-            const int want_vpt = rb.vec_per_thread ? rb.vec_per_thread : vpt;
-            if (plan_rows(dtype, vec, M, units, rb, p, true) != RS_OK || p->threads_per_row != want_tpr ||
-                p->vec_per_thread != want_vpt) {
+            if (plan_rows(dtype, vec, M, units, rb, p, true) != RS_OK ||
+                p->threads_per_row != (want.tpr ? want.tpr : tpr) || p->vec_per_thread != (want.vpt ? want.vpt : vpt)) {
                 *p = keep;
-                stages_want = 0;
+                ok = false;
             }
         }
-        if (stages_want) def_stages = stages_want;
+        if (ok && want.stages) def_stages = want.stages;
     }
     p->path = RS_PATH_RING;  // (the LayerNorm kind depends on the path)
     const int lkind = p->op == RS_OP_LAYERNORM ? rs::layernorm_merge_kind(*p, N, vec) : 0;
