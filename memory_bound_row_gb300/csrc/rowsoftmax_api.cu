@@ -288,18 +288,26 @@ bool causal16_narrow(int64_t units, int64_t M, int sm_count, int* tpr, int* vpt)
 //              ring16_softmax_shape (+4 to +34 % from 2560 to 32768 values);
 // causal mask  rows of 32 to 256 units: causal16_narrow (+21 to +37 %); of 257
 //              to 4096 units: its copy ring at 8 units a thread (5 or 6 where
-//              they fill whole warps exactly and 8 do not), one row a CTA, two
+//              they fill whole warps exactly and 8 do not; 5 or 6 where they
+//              fill 16 warps exactly: 20480 +5.7 %, 24576 +1.9 % against 8
+//              units, 10240 -18 %, 12288 -0.6 % at 8 warps), one row a CTA, two
 //              stages (+15 to +47 % from 2560 to 32768 values);
 // LayerNorm    rows of 32 to 128 units: about 4 units a thread on the fewest
 //              lanes that hold them (+3 to +24 %); rows of one warp: 128-thread
 //              CTAs (2048 +5.8 %); 257 to 768 units: 6 (else 4) units a thread,
 //              one row a CTA where they fill whole warps exactly, else 4 units
-//              (+3 to +45 %); 1537 to 2048 units: 8 units a thread, 512-thread
-//              CTAs (16384 +24 %);
+//              (+3 to +45 %); 1536 and 3072 units: 6 units a thread on 8 or
+//              16 warps, one row a CTA (12288 +9.1 %, 24576 +8.6 %; on 6, 9, 10,
+//              12 and 14 warps -4 to -19 %); 1537 to 2048 units: 8 units a
+//              thread, 512-thread CTAs (16384 +24 %);
 // RMSNorm      rows of one warp at 8 units: 512-thread CTAs (+0.8 %); 4 warps at
 //              4 units: one row a 128-thread CTA (4096 +6.1 %); 5 to 7 warps at
 //              4 units: three stages (+3 to +8 %); 8 warps at 4 units: four
-//              stages (8192 +8.3 %).
+//              stages (8192 +8.3 %); 2049 to 3072 units that 6 units a thread
+//              fill whole warps exactly: 6 units, one row a CTA (18432 +6.9 %,
+//              21504 +9.9 %, 24576 +11.1 % against 4 units on 18 to 24 warps;
+//              at 1536 to 1920 units, where 4 units take at most 15 warps, -1
+//              to -25 %).
 // The rules other than the causal and the wide softmax ones apply from 64
 // rows an SM, so that every CTA loops over its stages.
 struct ShapeWant {
@@ -316,7 +324,7 @@ bool measured_ring_shape(const rs_plan& p, int64_t units, int64_t M, int sm_coun
             return true;
         }
     } else if (p.op == RS_OP_SOFTMAX && causal16_ring(units, M, sm_count)) {
-        const int v = fills(32, 8) ? 8 : fills(32, 5) ? 5 : fills(32, 6) ? 6 : 8;
+        const int v = fills(512, 5) ? 5 : fills(512, 6) ? 6 : fills(32, 8) ? 8 : fills(32, 5) ? 5 : fills(32, 6) ? 6 : 8;
         const int t = (int)round_up(ceil_div(units, v), 32);
         *w = ShapeWant{t, v, t, 2};
         return true;
@@ -358,6 +366,10 @@ bool measured_ring_shape(const rs_plan& p, int64_t units, int64_t M, int sm_coun
             *w = ShapeWant{t, v, e6 || e4 ? t : 0, 0};
             return true;
         }
+        if (units >= 1536 && units <= 3072 && fills(256, 6)) {
+            *w = ShapeWant{(int)(units / 6), 6, (int)(units / 6), 0};
+            return true;
+        }
         if (units > 1536 && units <= 2048) {
             *w = ShapeWant{256, 8, 512, 0};
             return true;
@@ -365,7 +377,8 @@ bool measured_ring_shape(const rs_plan& p, int64_t units, int64_t M, int sm_coun
         return false;
     }
     // RMSNorm
-    if (tpr == 32 && vpt == 8) *w = ShapeWant{0, 0, 512, 0};
+    if (units > 2048 && units <= 3072 && fills(32, 6)) *w = ShapeWant{(int)(units / 6), 6, (int)(units / 6), 0};
+    else if (tpr == 32 && vpt == 8) *w = ShapeWant{0, 0, 512, 0};
     else if (tpr == 128 && vpt <= 4) *w = ShapeWant{0, 0, 128, 0};
     else if (tpr == 256 && vpt <= 4) *w = ShapeWant{0, 0, 0, 4};
     else if (tpr > 128 && tpr < 256 && vpt <= 4) *w = ShapeWant{0, 0, 0, 3};

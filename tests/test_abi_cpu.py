@@ -151,6 +151,11 @@ def test_16bit_softmax_rows_take_the_measured_ring_shapes():
     for N, tpr, vpt in [(2560, 64, 5), (3072, 64, 6), (4608, 96, 6), (5120, 128, 5)]:
         rc, p = rs.rowsoftmax_causal_plan(A, A + (1 << 40), 8192, N, N, N, N, 0, rs.RS_BF16, None, gb300())
         assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (tpr, vpt, tpr), N
+    # and 5 or 6 where they fill 16 warps exactly, before 8 on 10 or 12 warps
+    # (20480 +5.7 %, 24576 +1.9 %); 8 warps keep 8 units (10240 -18 %, 12288 -0.6 %)
+    for N, tpr, vpt in [(20480, 512, 5), (24576, 512, 6), (10240, 160, 8), (12288, 192, 8)]:
+        rc, p = rs.rowsoftmax_causal_plan(A, A + (1 << 40), 8192, N, N, N, N, 0, rs.RS_F16, None, gb300())
+        assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"], p["stages"]) == (tpr, vpt, tpr, 2), N
 
 
 def test_plans_for_the_benchmark_workloads():

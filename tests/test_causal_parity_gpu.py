@@ -203,12 +203,13 @@ def test_causal_narrow_16bit_rows_on_few_lanes(dtype, N, tpr):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("N", [2050, 2560, 3072, 4096, 4608, 5120, 6000, 12288, 32768])
+@pytest.mark.parametrize("N", [2050, 2560, 3072, 4096, 4608, 5120, 6000, 12288, 20480, 24576, 32768])
 @pytest.mark.parametrize("mask", ["period N", "period 97"])
 def test_causal_16bit_rows_of_2049_to_32768_values_on_the_copy_ring(dtype, N, mask):
     # The planner's measured shape for the causal mask's 16-bit rows of 257 to
-    # 4096 units: its copy ring at 8 units a thread, one row a CTA; NaN written
-    # into the masked part; every row against the oracle.
+    # 4096 units: its copy ring at 8 units a thread (5 or 6 where they fill
+    # whole warps exactly and 8 do not, or where they fill 16 warps), one row a
+    # CTA; NaN written into the masked part; every row against the oracle.
     M = 4 * 152 + 37
     period, offset = (N, 0) if mask == "period N" else (97, N // 2)
     x, out = _aligned(M, N, dtype, seed=N + 17)

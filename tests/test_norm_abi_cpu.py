@@ -257,6 +257,25 @@ def test_16bit_norm_rows_of_257_to_768_units():
         assert (p["threads_per_row"], p["vec_per_thread"]) == (tpr, 4), N
 
 
+def test_16bit_norm_rows_that_6_units_fill_exactly_on_wide_rows():
+    # LayerNorm rows of 1536 and 3072 units: 6 units a thread on 8 or 16 warps,
+    # one row a CTA (bf16 12288 +9.1 %, 24576 +8.6 %); RMSNorm rows of 2049 to
+    # 3072 units that 6 units fill on whole warps: 6 units, one row a CTA
+    # (18432 +6.9 %, 21504 +9.9 %, 24576 +11.1 %); rows of other widths, and
+    # fewer rows than 64 an SM, keep the plan.
+    for op, N, tpr in [(rs.RS_OP_LAYERNORM, 12288, 256), (rs.RS_OP_LAYERNORM, 24576, 512),
+                       (rs.RS_OP_RMSNORM, 18432, 384), (rs.RS_OP_RMSNORM, 21504, 448), (rs.RS_OP_RMSNORM, 24576, 512)]:
+        for dt in (rs.RS_F16, rs.RS_BF16):
+            p = _plan(op, (1 << 28) // N, N, dt, b=B if op == rs.RS_OP_LAYERNORM else None)
+            assert p["path"] == rs.RS_PATH_RING and p["stages"] == 2, (op, N)
+            assert (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == (tpr, 6, tpr), (op, N)
+    for op, N, shape in [(rs.RS_OP_LAYERNORM, 18432, (576, 4)), (rs.RS_OP_LAYERNORM, 9216, (288, 4)),
+                         (rs.RS_OP_RMSNORM, 12288, (384, 4)), (rs.RS_OP_RMSNORM, 15360, (480, 4))]:
+        p = _plan(op, (1 << 28) // N, N, rs.RS_BF16, b=B if op == rs.RS_OP_LAYERNORM else None)
+        assert (p["threads_per_row"], p["vec_per_thread"]) == shape, (op, N)
+    assert _plan(rs.RS_OP_RMSNORM, 1024, 24576, rs.RS_BF16)["vec_per_thread"] == 4
+
+
 def test_16bit_layernorm_rows_of_32_to_128_units_hold_about_4_units_a_thread():
     # the fewest lanes (8 to 32) that hold the row at about 4 units a thread
     # (bf16 256 +24 %, 512 +11 %, 768 +12 %, 1024 +2.8 % over 8 units a thread)

@@ -405,13 +405,15 @@ def test_nonzero_stream():
 
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("N", [256, 512, 768, 1024, 2560, 3072, 3584, 4608, 5120, 5632, 6144, 16384, 4100])
+@pytest.mark.parametrize("N", [256, 512, 768, 1024, 2560, 3072, 3584, 4608, 5120, 5632, 6144, 12288, 16384, 18432,
+                               24576, 4100])
 def test_16bit_norm_rows_on_the_measured_ring_shapes(op, dtype, N):
     # The planner's measured ring shapes for 16-bit norm rows take effect from
     # 64 rows an SM: LayerNorm rows of 257 to 768 units at 6 or 4 units a
-    # thread (one row a CTA where they fill exactly), of 1537 to 2048 units at 8
-    # units in 512-thread CTAs, RMSNorm rows of 5 to 7 warps with three stages;
-    # a ragged width; every row against the oracle.
+    # thread (one row a CTA where they fill exactly), of 1536 and 3072 units at
+    # 6 units, of 1537 to 2048 units at 8 units in 512-thread CTAs, RMSNorm rows
+    # of 5 to 7 warps with three stages, of 2049 to 3072 units at 6 units a
+    # thread; a ragged width; every row against the oracle.
     M = 64 * 152 + 5
     x, out = _aligned(M, N, dtype, seed=N + 11)
     wt, bs = _params(N, dtype, seed=N)
