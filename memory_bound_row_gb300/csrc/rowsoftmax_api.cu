@@ -294,12 +294,15 @@ bool causal16_narrow(int64_t units, int64_t M, int sm_count, int* tpr, int* vpt)
 //              stages (+15 to +47 % from 2560 to 32768 values);
 // LayerNorm    rows of 32 to 128 units: about 4 units a thread on the fewest
 //              lanes that hold them (+3 to +24 %); rows of one warp: 128-thread
-//              CTAs (2048 +5.8 %); 257 to 768 units: 6 (else 4) units a thread,
-//              one row a CTA where they fill whole warps exactly, else 4 units
-//              (+3 to +45 %); 1536 and 3072 units: 6 units a thread on 8 or
-//              16 warps, one row a CTA (12288 +9.1 %, 24576 +8.6 %; on 6, 9, 10,
-//              12 and 14 warps -4 to -19 %); 1537 to 2048 units: 8 units a
-//              thread, 512-thread CTAs (16384 +24 %);
+//              CTAs (2048 +5.8 %); 257 to 768 units: 6 (else 5, else 4) units
+//              a thread, one row a CTA where they fill whole warps exactly (at
+//              5 units at least 128 threads a CTA), else 4 units (+3 to +45 %;
+//              5 units: 2560 +40 %, 5120 +12 %); 1536 and 3072 units: 6 units a
+//              thread on 8 or 16 warps, one row a CTA (12288 +9.1 %, 24576
+//              +8.6 %; on 6, 9, 10, 12 and 14 warps -4 to -19 %); 1537 to 2048
+//              units: 8 units a thread, 512-thread CTAs (16384 +24 %); other
+//              rows of 769 to 2560 units that 5 units fill exactly: 5 units,
+//              one row a CTA (10240 +13 %, 20480 +12 %);
 // RMSNorm      rows of one warp at 8 units: 512-thread CTAs (+0.8 %); 4 warps at
 //              4 units: one row a 128-thread CTA (4096 +6.1 %); 5 to 7 warps at
 //              4 units: three stages (+3 to +8 %); 8 warps at 4 units: four
@@ -307,7 +310,11 @@ bool causal16_narrow(int64_t units, int64_t M, int sm_count, int* tpr, int* vpt)
 //              fill whole warps exactly: 6 units, one row a CTA (18432 +6.9 %,
 //              21504 +9.9 %, 24576 +11.1 % against 4 units on 18 to 24 warps;
 //              at 1536 to 1920 units, where 4 units take at most 15 warps, -1
-//              to -25 %).
+//              to -25 %); other rows of 129 to 2560 units that 5 units fill on
+//              whole warps and 4 units do not within 512 threads: 5 units, one
+//              row a CTA, 128-thread CTAs for rows of one warp (1280 +31 %,
+//              2560 +21 %, 20480 +12 %; where 4 units fill 5 or 10 warps, 5120
+//              and 10240, 5 units measured 8 and 2.5 % slower).
 // The rules other than the causal and the wide softmax ones apply from 64
 // rows an SM, so that every CTA loops over its stages.
 struct ShapeWant {
@@ -360,10 +367,10 @@ bool measured_ring_shape(const rs_plan& p, int64_t units, int64_t M, int sm_coun
             return true;
         }
         if (units > 256 && units <= 768) {
-            const bool e6 = fills(32, 6), e4 = fills(32, 4);
-            const int v = e6 ? 6 : 4;
+            const bool e6 = fills(32, 6), e5 = fills(32, 5), e4 = fills(32, 4);
+            const int v = e6 ? 6 : e5 ? 5 : 4;
             const int t = (int)round_up(ceil_div(units, v), 32);
-            *w = ShapeWant{t, v, e6 || e4 ? t : 0, 0};
+            *w = ShapeWant{t, v, v == 5 ? (t < 128 ? 128 / t * t : t) : e6 || e4 ? t : 0, 0};
             return true;
         }
         if (units >= 1536 && units <= 3072 && fills(256, 6)) {
@@ -374,10 +381,17 @@ bool measured_ring_shape(const rs_plan& p, int64_t units, int64_t M, int sm_coun
             *w = ShapeWant{256, 8, 512, 0};
             return true;
         }
+        if (units > 768 && units <= 2560 && fills(32, 5)) {
+            *w = ShapeWant{(int)(units / 5), 5, (int)(units / 5), 0};
+            return true;
+        }
         return false;
     }
     // RMSNorm
+    const bool e4 = fills(32, 4) && units / 4 <= 512;
     if (units > 2048 && units <= 3072 && fills(32, 6)) *w = ShapeWant{(int)(units / 6), 6, (int)(units / 6), 0};
+    else if (units > 128 && units <= 2560 && fills(32, 5) && !e4)
+        *w = ShapeWant{(int)(units / 5), 5, units == 160 ? 128 : (int)(units / 5), 0};
     else if (tpr == 32 && vpt == 8) *w = ShapeWant{0, 0, 512, 0};
     else if (tpr == 128 && vpt <= 4) *w = ShapeWant{0, 0, 128, 0};
     else if (tpr == 256 && vpt <= 4) *w = ShapeWant{0, 0, 0, 4};

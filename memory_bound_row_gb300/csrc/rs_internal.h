@@ -22,7 +22,7 @@ constexpr int kVptVec16[] = {RS_VPT_VEC_16};
 constexpr int kVptScalar[] = {RS_VPT_SCALAR};
 
 // The normalisations (RMSNorm, LayerNorm) are instantiated for fewer counts.
-#define RS_VPT_NORM_VEC 1, 2, 3, 4, 6, 8
+#define RS_VPT_NORM_VEC 1, 2, 3, 4, 5, 6, 8
 #define RS_VPT_NORM_SCALAR 1, 2, 4, 8, 16
 constexpr int kVptNormVec[] = {RS_VPT_NORM_VEC};
 constexpr int kVptNormScalar[] = {RS_VPT_NORM_SCALAR};

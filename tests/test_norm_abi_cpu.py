@@ -12,7 +12,7 @@ A = 1 << 20            # 16-byte aligned fake addresses; validation fails before
 OUT = A + (1 << 40)
 W = A + (1 << 41)
 B = A + (1 << 42)
-NORM_VPT_VEC = {1, 2, 3, 4, 6, 8}
+NORM_VPT_VEC = {1, 2, 3, 4, 5, 6, 8}
 NORM_VPT_SCALAR = {1, 2, 4, 8, 16}
 
 
@@ -241,20 +241,42 @@ def test_layernorm_16bit_rows_of_2048_units_take_8_units_a_thread():
 
 
 def test_16bit_norm_rows_of_257_to_768_units():
-    # LayerNorm rows that 6 (else 4) units a thread fill on whole warps exactly
-    # take that shape, one row a CTA; RMSNorm rows of 5 to 7 warps at 4 units a
-    # thread take three stages (bf16, measured against the previous plans).
-    for N, shape in [(3072, (64, 6, 64)), (4096, (128, 4, 128)), (4608, (96, 6, 96)), (5120, (160, 4, 160)),
-                     (6144, (128, 6, 128))]:
+    # LayerNorm rows that 6 (else 5, else 4) units a thread fill on whole warps
+    # exactly take that shape, one row a CTA (at 5 units at least 128 threads a
+    # CTA); RMSNorm rows of 5 to 7 warps at 4 units a thread take three stages
+    # (bf16, measured against the previous plans).
+    for N, shape in [(2560, (64, 5, 128)), (3072, (64, 6, 64)), (4096, (128, 4, 128)), (4608, (96, 6, 96)),
+                     (5120, (128, 5, 128)), (6144, (128, 6, 128))]:
         p = _plan(rs.RS_OP_LAYERNORM, (1 << 29) // N, N, rs.RS_BF16, b=B)
         assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == shape
     for N in (4608, 5120, 6144):
         p = _plan(rs.RS_OP_RMSNORM, (1 << 29) // N, N, rs.RS_BF16)
         assert p["vec_per_thread"] == 4 and 128 < p["threads_per_row"] < 256 and p["stages"] == 3, N
-    # LayerNorm rows that neither fills exactly: 4 units a thread, the planned CTA size
-    for N, tpr in [(2560, 96), (3584, 128), (5632, 192)]:
+    # LayerNorm rows that none fills exactly: 4 units a thread, the planned CTA size
+    for N, tpr in [(3584, 128), (5632, 192)]:
         p = _plan(rs.RS_OP_LAYERNORM, (1 << 29) // N, N, rs.RS_BF16, b=B)
         assert (p["threads_per_row"], p["vec_per_thread"]) == (tpr, 4), N
+
+
+def test_16bit_norm_rows_that_5_units_fill_exactly():
+    # 5 units a thread where they fill whole warps exactly (bf16, against the
+    # previous plans): LayerNorm from 257 units, one row a CTA (5120 +12 %,
+    # 10240 +13 %, 20480 +12 %; 2560 two rows a 128-thread CTA, +40 %);
+    # RMSNorm where 4 units do not fill whole warps within 512 threads (1280
+    # in 128-thread CTAs +31 %, 2560 +21 %, 20480 +12 %; at 5120 and 10240,
+    # where 4 units fill 5 and 10 warps, 5 units measured 8 and 2.5 % slower).
+    for dt in (rs.RS_F16, rs.RS_BF16):
+        for N, shape in [(10240, (256, 5, 256)), (20480, (512, 5, 512))]:
+            p = _plan(rs.RS_OP_LAYERNORM, (1 << 28) // N, N, dt, b=B)
+            assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == shape
+        for N, shape in [(1280, (32, 5, 128)), (2560, (64, 5, 64)), (20480, (512, 5, 512)), (5120, (160, 4, 160)),
+                         (10240, (320, 4, 320))]:
+            p = _plan(rs.RS_OP_RMSNORM, (1 << 28) // N, N, dt)
+            assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"], p["block_threads"]) == shape
+    # rows that need exactly 5 units a thread at the first-guess lane count take
+    # 5 (the instance list has no gap there): fp32 register rows of 1280 values
+    p = _plan(rs.RS_OP_RMSNORM, 100000, 1280, rs.RS_F32)
+    assert p["path"] == rs.RS_PATH_ROWS and (p["threads_per_row"], p["vec_per_thread"]) == (64, 5)
 
 
 def test_16bit_norm_rows_that_6_units_fill_exactly_on_wide_rows():

@@ -118,7 +118,7 @@ def test_optional_weight_and_bias(op, dtype, weight, bias, N):
 
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("tpr,vpt", [(1, 1), (2, 2), (4, 3), (8, 6), (16, 8), (32, 1), (32, 6), (64, 4), (96, 2),
+@pytest.mark.parametrize("tpr,vpt", [(1, 1), (2, 2), (4, 3), (8, 6), (16, 8), (32, 1), (32, 5), (32, 6), (64, 4), (96, 2),
                                      (128, 8), (256, 3), (1024, 1)])
 @pytest.mark.parametrize("grid_limit", [0, 3])
 def test_rows_path_thread_shapes(op, dtype, tpr, vpt, grid_limit):
@@ -133,6 +133,23 @@ def test_rows_path_thread_shapes(op, dtype, tpr, vpt, grid_limit):
         pytest.skip("register budget of this shape")
     y = _run(op, x, w, b, out=out, options=opts)
     _check(op, x, y, w, b, what=f"{op} rows tpr={tpr} vpt={vpt}")
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("N", [300, 640, 1280])
+def test_fp32_rows_that_need_5_units_a_thread(op, N):
+    # fp32 rows of 75, 160 and 320 units on 16, 32 and 64 lanes take 5 units a
+    # thread on the register rows (a thread of 16 rows a CTA, 8 and 4 rows);
+    # many rows, so that every CTA of the grid serves its rows; every row
+    # against the oracle.
+    M = 20011
+    x, out = _aligned(M, N, "f32", seed=N + 5)
+    wt, bs = _params(N, "f32", seed=N + 1)
+    ok, plan = _servable(op, x, wt, bs, None)
+    assert ok and plan["path"] == rs.RS_PATH_ROWS and plan["vec_per_thread"] == 5
+    y = _run(op, x, wt, bs, out=out)
+    check_all_rows(op, x, y, N, weight=wt, bias=bs if op == "ln" else None, eps=EPS[op],
+                   what=f"{'RMSNorm' if op == 'rms' else 'LayerNorm'} fp32 {M}x{N} at 5 units a thread")
 
 
 @pytest.mark.parametrize("op", OPS)
@@ -405,15 +422,16 @@ def test_nonzero_stream():
 
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("N", [256, 512, 768, 1024, 2560, 3072, 3584, 4608, 5120, 5632, 6144, 12288, 16384, 18432,
-                               24576, 4100])
+@pytest.mark.parametrize("N", [256, 512, 768, 1024, 1280, 2560, 3072, 3584, 4608, 5120, 5632, 6144, 10240, 12288,
+                               16384, 18432, 20480, 24576, 4100])
 def test_16bit_norm_rows_on_the_measured_ring_shapes(op, dtype, N):
     # The planner's measured ring shapes for 16-bit norm rows take effect from
     # 64 rows an SM: LayerNorm rows of 257 to 768 units at 6 or 4 units a
     # thread (one row a CTA where they fill exactly), of 1536 and 3072 units at
-    # 6 units, of 1537 to 2048 units at 8 units in 512-thread CTAs, RMSNorm rows
-    # of 5 to 7 warps with three stages, of 2049 to 3072 units at 6 units a
-    # thread; a ragged width; every row against the oracle.
+    # 6 units, of 1537 to 2048 units at 8 units in 512-thread CTAs, rows that 5
+    # units fill exactly at 5 units; RMSNorm rows of 5 to 7 warps with three
+    # stages, of 2049 to 3072 units at 6 units a thread, rows that 5 units fill
+    # and 4 do not at 5 units; a ragged width; every row against the oracle.
     M = 64 * 152 + 5
     x, out = _aligned(M, N, dtype, seed=N + 11)
     wt, bs = _params(N, dtype, seed=N)
