@@ -400,3 +400,28 @@ def test_ring_cta_sizes_for_16bit_rows():
                             rs.RS_BF16, None, gb300())
     assert rc == rs.RS_OK and p["path"] == rs.RS_PATH_RING and p["threads_per_row"] == 32
     assert p["block_threads"] == 128
+
+
+@pytest.mark.parametrize("dtype", [rs.RS_F16, rs.RS_BF16])
+@pytest.mark.parametrize("masked", [False, True])
+def test_measured_shapes_are_valid_plans_at_every_16bit_width(dtype, masked):
+    # Every multiple of 64 values from 256 to 32768 with enough rows for the
+    # measured shapes, plain and under a causal mask of period N: the plan
+    # covers the row with an instantiated unit count, its CTA holds whole rows
+    # within the block limit of that count, and its stages fit the opt-in
+    # shared memory.
+    instantiated = {1, 2, 3, 4, 5, 6, 8}
+    for N in range(256, 32768 + 1, 64):
+        M = max(64 * 152, (1 << 27) // N)
+        if masked:
+            rc, p = rs.rowsoftmax_causal_plan(A, A + (1 << 40), M, N, N, N, N, 0, dtype, None, gb300())
+            assert rc == rs.RS_OK, N
+        else:
+            p = _plan(M, N, dtype)
+        assert _covers(p, N), N
+        if p["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING):
+            assert p["vec_per_thread"] in instantiated, N
+            assert p["block_threads"] % p["threads_per_row"] == 0, N
+            limit = 1024 if p["vec_per_thread"] * p["vec_elems"] <= 32 else 512
+            assert p["block_threads"] <= limit, N
+            assert p["smem_bytes"] <= 232448 - 1024, N

@@ -304,3 +304,22 @@ def test_16bit_layernorm_rows_of_32_to_128_units_hold_about_4_units_a_thread():
     for N, tpr, vpt in [(256, 8, 4), (512, 16, 4), (768, 32, 3), (1024, 32, 4)]:
         p = _plan(rs.RS_OP_LAYERNORM, (1 << 28) // N, N, rs.RS_BF16, b=B)
         assert p["path"] == rs.RS_PATH_RING and (p["threads_per_row"], p["vec_per_thread"]) == (tpr, vpt), N
+
+
+@pytest.mark.parametrize("op", [rs.RS_OP_RMSNORM, rs.RS_OP_LAYERNORM])
+@pytest.mark.parametrize("dtype", [rs.RS_F16, rs.RS_BF16])
+def test_measured_shapes_are_valid_plans_at_every_16bit_width(op, dtype):
+    # Every multiple of 64 values from 256 to 32768 with enough rows for the
+    # measured shapes: the plan covers the row with an instantiated unit count,
+    # its CTA holds whole rows within the block limit of that count, and its
+    # stages fit the opt-in shared memory.
+    for N in range(256, 32768 + 1, 64):
+        M = max(64 * 152, (1 << 27) // N)
+        p = _plan(op, M, N, dtype, b=B if op == rs.RS_OP_LAYERNORM else None)
+        assert _covers(p, N), N
+        if p["path"] in (rs.RS_PATH_ROWS, rs.RS_PATH_RING):
+            assert p["vec_per_thread"] in NORM_VPT_VEC, N
+            assert p["block_threads"] % p["threads_per_row"] == 0, N
+            limit = 1024 if p["vec_per_thread"] * p["vec_elems"] <= 32 else 512
+            assert p["block_threads"] <= limit, N
+            assert p["smem_bytes"] <= 232448 - 1024, N
