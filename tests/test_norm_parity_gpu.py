@@ -422,8 +422,8 @@ def test_nonzero_stream():
 
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("N", [256, 512, 768, 1024, 1280, 2560, 3072, 3584, 4608, 5120, 5632, 6144, 10240, 12288,
-                               16384, 18432, 20480, 24576, 4100])
+@pytest.mark.parametrize("N", [256, 512, 768, 1024, 1280, 2560, 3072, 3584, 3840, 4608, 5120, 5632, 6144, 6400, 7680,
+                               10240, 12288, 12800, 16384, 17920, 18432, 20480, 24576, 4100])
 def test_16bit_norm_rows_on_the_measured_ring_shapes(op, dtype, N):
     # The planner's measured ring shapes for 16-bit norm rows take effect from
     # 64 rows an SM: LayerNorm rows of 257 to 768 units at 6 or 4 units a
