@@ -833,7 +833,8 @@ def run_sweep_wide(args):
     causal = args.causal and op == "softmax"
     code = {"f16": rs.RS_F16, "bf16": rs.RS_BF16}[dt]
     tol = {"f16": 2.0 ** -9, "bf16": 2.0 ** -6}[dt]  # a few units in the last place of the output
-    for N in WIDE_SWEEP_N:
+    widths = [int(v) for v in args.widths.split(",")] if getattr(args, "widths", None) else WIDE_SWEEP_N
+    for N in widths:
         M = (1 << 28) // N
         w = W.custom(M, N, dt, seed=5, kind="offset50" if op == "layernorm" else "normal1")
         x0 = W.generate(w, dev)
@@ -1114,6 +1115,9 @@ def main():
                          "operation through the planner's choice, the ring and the clusters (with --causal: the "
                          "causal softmax, mask period N)")
     ap.add_argument("--sweep-dtype", choices=["bf16", "f16"], default="bf16")
+    ap.add_argument("--widths", default=None,
+                    help="--sweep-wide: comma-separated row widths instead of 256..65536 (one width for a "
+                         "profiler capture)")
     ap.add_argument("--split", action="store_true",
                     help="instead of the benchmark line: the split-row softmax (few wide rows through "
                          "rowsoftmax_split_fwd against rowsoftmax_fwd, and the vocabulary-parallel partial and "
